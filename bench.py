@@ -1,0 +1,513 @@
+#!/usr/bin/env python
+"""Benchmark of the multi-LoRA hot path on one GB300 per rank.
+
+One step = one pass of the whole per-step path over one batch:
+lora_prepare_meta (token metadata) + lora_shrink + lora_expand, through the
+library's C ABI. The default workload is the decode batch the headline metric
+is quoted on: qkv_proj d_in=4096, packed slices [4096,1024,1024], r=16,
+64 slots, 256 one-token requests (10% slot 0), bf16.
+
+Timing: the step's inputs (slot table, x, y, token slots, metadata) are
+replicated on the device R times so that the rotation touches more than
+3x the 129 MB L2 between visits to a replica ("inputs larger than L2").
+Warm-up steps run eagerly; the K timed steps are CUDA-graph replays
+bracketed by CUDA events on the launching stream, with a barrier and
+torch.cuda.synchronize() on both sides; the value is the max over ranks.
+Per-kernel durations come from CUDA events recorded around every launch
+inside the captured graph. The end-to-end figure repeats the step through
+the same ABI with pinned host buffers: the copies in and out are inside its
+timed region.
+
+Multi-GPU (torchrun): data parallel over independent batches, one replica of
+the slot table per rank, no collective on the data path ("scaling": "weak").
+
+``--impl reference`` times the fp64 CPU oracle on the same workload (the
+only other place besides the cpu_baseline leg that runs ``oracle/``).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "LoRA-delta tokens/s and achieved HBM GB/s (decode) / TC TFLOP/s (prefill) vs peak"
+L2_BYTES = 129 * 2 ** 20
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+WORKLOADS = {
+    "decode_qkv": "decode BGMV: qkv_proj 4096->[4096,1024,1024], r=16, 64 slots, 256 tokens (10% slot 0)",
+    "prefill_gate_up": "prefill SGMV: gate_up_proj 4096->[14336,14336], r=64, 32 slots, 16 requests U[128,2048]",
+    "mixed_o_proj": "mixed: o_proj 4096->4096, 128 slots, ranks {8..64} pad 64, 1024 decode + 4x512 prefill",
+    "toy_fp32": "toy fp32: d=256, r=16, 8 slots, 6 requests (53 tokens)",
+}
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20000)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", choices=sorted(WORKLOADS), default="decode_qkv")
+    p.add_argument("--kind", choices=["auto", "bgmv", "sgmv"], default="auto")
+    p.add_argument("--replicas", type=int, default=0, help="device replicas (0: enough for 3x L2)")
+    p.add_argument("--graph-steps", type=int, default=0, help="steps per captured graph (0: auto)")
+    p.add_argument("--e2e-steps", type=int, default=200)
+    p.add_argument("--cpu-seconds", type=float, default=10.0)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-child", action="store_true", help=argparse.SUPPRESS)
+    return p.parse_args(argv)
+
+
+# ----------------------------------------------------------------------------- algorithmic model
+
+def algorithmic(inst, y_bytes_per_elem=2):
+    """Bytes and flops the method must move / do for one step on this batch.
+
+    Weights of every active adapter are read once (rank-aware), x rows of LoRA
+    tokens are read once, y rows of LoRA tokens are read and written once.
+    The fp32 shrink buffer is counted per kernel (it is the shrink's output and
+    the expand's input) but not in the step total.
+    """
+    import numpy as np
+    es = 2 if inst.dtype == "bf16" else 4
+    ts = inst.token_slot.astype(np.int64)
+    live = (ts > 0) & (ts < inst.num_slots)
+    T_L = int(live.sum())
+    ranks = np.zeros(inst.num_slots, np.int64)
+    for k, ad in inst.adapters.items():
+        ranks[k] = ad.rank
+    active = np.unique(ts[live])
+    n_s, d_in, d_out = inst.n_slices, inst.d_in, inst.d_out_total
+    w_a = int(sum(es * ranks[a] * n_s * d_in for a in active))
+    w_b = int(sum(es * ranks[a] * d_out for a in active))
+    x_b = es * T_L * d_in
+    y_b = 2 * y_bytes_per_elem * T_L * d_out
+    buf_b = 4 * n_s * T_L * inst.r_max
+    flops = int(sum(2 * ranks[a] * (n_s * d_in + d_out) * int((ts == a).sum()) for a in active))
+    return dict(T=int(len(ts)), T_L=T_L, active=int(len(active)), shrink_bytes=w_a + x_b + buf_b,
+                expand_bytes=w_b + buf_b + y_b, step_bytes=w_a + w_b + x_b + y_b, flops=flops,
+                shrink_flops=int(sum(2 * ranks[a] * n_s * d_in * int((ts == a).sum()) for a in active)),
+                expand_flops=int(sum(2 * ranks[a] * d_out * int((ts == a).sum()) for a in active)))
+
+
+def make_workload(name, seed_offset=0):
+    import workloads as wl
+    base = {"toy_fp32": 0, "decode_qkv": 2, "prefill_gate_up": 3, "mixed_o_proj": 4}[name]
+    return wl.make_instance(name, seed=base + 1000 * seed_offset if seed_offset else None)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            pk = json.load(f)
+        return float(pk["hbm_gbs"]), float(pk["bf16_tflops"]), "measured"
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "rank_adapter_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload, kernel):
+    """DRAM bytes per launch from the committed ncu summary, if it matches the current sources."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f)
+    ent = rec.get(workload, {}).get(kernel)
+    if not ent or ent.get("source_hash") != kernel_source_hash():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for name, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- CPU legs (oracle)
+
+def cpu_child(args):
+    """Time the oracle as it stands on this host's cores; prints one JSON line."""
+    import numpy as np
+    import oracle
+    inst = make_workload(args.workload)
+    alg = algorithmic(inst)
+    ads = oracle.adapters_f64(inst)
+    x = inst.to_f32(inst.x).astype(np.float64)
+    y = inst.to_f32(inst.y_in).astype(np.float64)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.prepare_meta(inst.token_slot, inst.num_slots)
+        oracle.apply_requests(x, y, ads, inst.out_sizes, inst.r_max, inst.req_lengths, inst.req_slots,
+                              inst.num_slots)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= args.cpu_seconds:
+            break
+    print(json.dumps({"value": reps * alg["T_L"] / el, "seconds": el, "reps": reps,
+                      "sec_per_step": el / reps}))
+
+
+def run_cpu_baseline(args):
+    cores = len(os.sched_getaffinity(0))
+    env = dict(os.environ)
+    for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[v] = str(cores)
+    cmd = [sys.executable, os.path.abspath(__file__), "--cpu-child", "--workload", args.workload,
+           "--cpu-seconds", str(args.cpu_seconds)]
+    p = subprocess.run(cmd, capture_output=True, text=True, env=env, cwd=ROOT)
+    if p.returncode != 0:
+        return {"value": None, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                "error": p.stderr.strip().splitlines()[-1:] }
+    r = json.loads(p.stdout.strip().splitlines()[-1])
+    return {"value": r["value"], "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{r['reps']} full steps of the {args.workload} batch (fp64 per-request loop, "
+                      f"numpy BLAS with {cores} threads), {r['seconds']:.1f} s",
+            "sec_per_step": r["sec_per_step"]}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    inst = make_workload(args.workload)
+    cfg = {"workload": args.workload, "desc": WORKLOADS[args.workload], "global_batch": inst.num_tokens,
+           "n_gpus_ignored": args.gpus}
+    cpu = run_cpu_baseline(argparse.Namespace(workload=args.workload,
+                                              cpu_seconds=max(1.0, args.cpu_seconds)))
+    v = cpu.get("value")
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": cfg,
+            "ms_per_step": (cpu["sec_per_step"] * 1e3) if v else None,
+            "cpu_baseline": cpu, "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                                         "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+# ----------------------------------------------------------------------------- GPU leg
+
+class Replica:
+    """One device copy of every input of a step, plus its metadata buffers and ctypes arguments."""
+
+    def __init__(self, ra, torch, inst, table_src, x_src, y_src, ts_src, kind):
+        self.table = ra.SlotTable(inst.d_in, inst.out_sizes, inst.num_slots, inst.r_max,
+                                  ra.LORA_BF16 if inst.dtype == "bf16" else ra.LORA_F32)
+        for dst, src in zip(self.table.A + self.table.B, table_src.A + table_src.B):
+            dst.copy_(src)
+        self.table.slot_rank.copy_(table_src.slot_rank)
+        self.table.slot_scale.copy_(table_src.slot_scale)
+        self.x = x_src.clone()
+        self.y = y_src.clone()
+        T = inst.num_tokens
+        self.meta = ra.TokenMeta(T, inst.num_slots)
+        self.meta.token_slot[:T].copy_(ts_src)
+        self.meta.set_num_tokens(T)
+        self.buf = torch.zeros(inst.n_slices, T, inst.r_max, dtype=torch.float32, device="cuda")
+        self.kind = kind
+        self.ydt = ra.LORA_BF16 if self.y.dtype == torch.bfloat16 else ra.LORA_F32
+
+    def bytes(self):
+        return self.table.nbytes() + self.x.numel() * self.x.element_size() + \
+            self.y.numel() * self.y.element_size()
+
+    def launch(self, ra, i, ev=None):
+        """Enqueue meta, shrink, expand on the current stream; ev: optional per-kernel event pairs."""
+        st = None
+        if ev is not None:
+            ev[0].record()
+        ra.check(ra.lora_prepare_meta(self.meta.c, st), "prepare_meta")
+        if ev is not None:
+            ev[1].record()
+        ra.check(ra.lora_shrink(self.table.desc, self.meta.c, self.x.data_ptr(), self.x.stride(0),
+                                self.buf.data_ptr(), self.kind, 0, 0, st), "shrink")
+        if ev is not None:
+            ev[2].record()
+        ra.check(ra.lora_expand(self.table.desc, self.meta.c, self.buf.data_ptr(), self.y.data_ptr(),
+                                self.y.stride(0), self.ydt, self.kind, st), "expand")
+        if ev is not None:
+            ev[3].record()
+
+
+def _external_events(torch):
+    try:
+        torch.cuda.Event(enable_timing=True, external=True)
+        return True
+    except TypeError:
+        return False
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    import rank_adapter_gb300 as ra
+
+    kind = {"auto": ra.LORA_AUTO, "bgmv": ra.LORA_BGMV, "sgmv": ra.LORA_SGMV}[args.kind]
+    inst = make_workload(args.workload, seed_offset=rank)
+    alg = algorithmic(inst)
+
+    def dev(a, dt):
+        a = np.ascontiguousarray(a)
+        if dt == "bf16":
+            return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).cuda()
+        return torch.from_numpy(a.astype(np.float32)).cuda()
+
+    # Master copy of the slot table, written through lora_set_slot.
+    master = ra.SlotTable(inst.d_in, inst.out_sizes, inst.num_slots, inst.r_max,
+                          ra.LORA_BF16 if inst.dtype == "bf16" else ra.LORA_F32)
+    for k, ad in sorted(inst.adapters.items()):
+        master.set_slot(k, ad.rank, ad.scale, [dev(a, inst.dtype) for a in ad.A], [dev(b, inst.dtype) for b in ad.B])
+        torch.cuda.synchronize()
+    x0 = dev(inst.x, inst.dtype)
+    y0 = dev(inst.y_in, inst.dtype)
+    ts0 = torch.from_numpy(inst.token_slot).cuda()
+
+    per = master.nbytes() + x0.numel() * x0.element_size() + y0.numel() * y0.element_size()
+    R = args.replicas or max(2, int(np.ceil(3 * L2_BYTES / per)))
+    reps = [Replica(ra, torch, inst, master, x0, y0, ts0, kind) for _ in range(R)]
+    torch.cuda.synchronize()
+
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        for i in range(max(3, args.warmup)):
+            reps[i % R].launch(ra, i)
+    stream.synchronize()
+
+    # Capture G steps (a multiple of R) into a graph; per-kernel events inside it if supported.
+    G = args.graph_steps or R * max(1, 64 // R)
+    G = min(G, max(1, args.steps))
+    ext = _external_events(torch)
+    evs = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)] for _ in range(G)] if ext else None
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for i in range(G):
+            reps[i % R].launch(ra, i, evs[i] if ext else None)
+    tail = args.steps % G
+    graph_tail = None
+    if tail:
+        graph_tail = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph_tail, stream=stream):
+            for i in range(tail):
+                reps[i % R].launch(ra, i)
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            graph.replay()
+    stream.synchronize()
+
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    clocks = ClockSampler(vis.split(",")[local].strip() if vis else str(local))
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        start.record()
+        for _ in range(args.steps // G):
+            graph.replay()
+        if graph_tail is not None:
+            graph_tail.replay()
+        end.record()
+    stream.synchronize()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.stop()
+    elapsed_ms = start.elapsed_time(end)
+
+    # Per-kernel durations: from the events of the last graph replay, else an eager pass primed
+    # by a sleep kernel so that the host has enqueued every launch before the GPU reaches it.
+    if ext and args.steps >= G:
+        durs = {k: [] for k in ("meta", "shrink", "expand")}
+        for e in evs:
+            durs["meta"].append(e[0].elapsed_time(e[1]))
+            durs["shrink"].append(e[1].elapsed_time(e[2]))
+            durs["expand"].append(e[2].elapsed_time(e[3]))
+        kernel_timing = f"CUDA events around each launch inside the captured graph (last replay, {G} steps)"
+    else:
+        n = min(200, max(R, args.steps))
+        evs2 = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n)]
+        with torch.cuda.stream(stream):
+            torch.cuda._sleep(int(2e8))
+            for i in range(n):
+                reps[i % R].launch(ra, i, evs2[i])
+        stream.synchronize()
+        durs = {"meta": [e[0].elapsed_time(e[1]) for e in evs2], "shrink": [e[1].elapsed_time(e[2]) for e in evs2],
+                "expand": [e[2].elapsed_time(e[3]) for e in evs2]}
+        kernel_timing = f"CUDA events around {n} eager launches enqueued behind a sleep kernel"
+    avg = {k: statistics.mean(v) for k, v in durs.items()}
+
+    # End to end: the same step through the ABI with pinned host buffers and copies in / out.
+    h_x = torch.empty_like(x0, device="cpu").pin_memory()
+    h_x.copy_(x0)
+    h_y = torch.empty_like(y0, device="cpu").pin_memory()
+    h_y.copy_(y0)
+    h_ts = torch.empty_like(ts0, device="cpu").pin_memory()
+    h_ts.copy_(ts0)
+    h_out = torch.empty_like(y0, device="cpu").pin_memory()
+    e2e_rep = reps[0]
+    h2d = h_x.numel() * h_x.element_size() + h_y.numel() * h_y.element_size() + h_ts.numel() * 4
+    d2h = h_out.numel() * h_out.element_size()
+    ne = max(3, args.e2e_steps)
+    T = inst.num_tokens
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            e2e_rep.x.copy_(h_x, non_blocking=True)
+            e2e_rep.y.copy_(h_y, non_blocking=True)
+            e2e_rep.meta.token_slot[:T].copy_(h_ts, non_blocking=True)
+            e2e_rep.launch(ra, i)
+            h_out.copy_(e2e_rep.y, non_blocking=True)
+    stream.synchronize()
+    if dist is not None:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        e0.record()
+        for i in range(ne):
+            e2e_rep.x.copy_(h_x, non_blocking=True)
+            e2e_rep.y.copy_(h_y, non_blocking=True)
+            e2e_rep.meta.token_slot[:T].copy_(h_ts, non_blocking=True)
+            e2e_rep.launch(ra, i)
+            h_out.copy_(e2e_rep.y, non_blocking=True)
+        e1.record()
+    stream.synchronize()
+    e2e_wall = time.perf_counter() - t0
+    e2e_ms = e0.elapsed_time(e1)
+
+    # Max over ranks.
+    vals = torch.tensor([elapsed_ms, e2e_ms, float(alg["T_L"])], dtype=torch.float64, device="cuda")
+    if dist is not None:
+        mx = vals.clone()
+        dist.all_reduce(mx, op=dist.ReduceOp.MAX)
+        tl = vals.clone()
+        dist.all_reduce(tl, op=dist.ReduceOp.SUM)
+        elapsed_ms, e2e_ms, total_TL = float(mx[0]), float(mx[1]), float(tl[2])
+    else:
+        total_TL = float(alg["T_L"])
+    launches = 3 * args.steps
+
+    if rank == 0:
+        hbm, tc, src = load_peaks()
+        step_ms = elapsed_ms / args.steps
+        kern = max(("shrink", "expand"), key=lambda k: avg[k])
+        kb = alg[f"{kern}_bytes"]
+        ach = kb / (avg[kern] * 1e-3) / 1e9
+        line = {
+            "metric": METRIC, "value": total_TL * args.steps / (elapsed_ms * 1e-3), "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": inst.dtype, "data": "synthetic",
+            "config": {"workload": args.workload, "desc": WORKLOADS[args.workload], "kind": args.kind,
+                       "global_batch": inst.num_tokens * world, "lora_tokens_per_gpu": alg["T_L"],
+                       "active_adapters": alg["active"], "parallelism": f"dp{world}",
+                       "l2": f"rotating {R} device replicas x {per / 2**20:.1f} MiB "
+                             f"(> 3x {L2_BYTES >> 20} MiB L2)",
+                       "timing": f"CUDA-graph replays of {G} steps, CUDA events on the launching stream"},
+            "gpu_launches": launches,
+            "step_hbm_gbs": alg["step_bytes"] / (step_ms * 1e-3) / 1e9,
+            "step_frac_of_hbm": alg["step_bytes"] / (step_ms * 1e-3) / 1e9 / hbm,
+            "kernel_us": {k: v * 1e3 for k, v in avg.items()},
+            "kernel_timing": kernel_timing,
+            "roofline": {"bound": "hbm", "kernel": kern, "achieved": ach, "peak": hbm, "unit": "GB/s",
+                         "frac": ach / hbm, "peak_source": src,
+                         "algorithmic_bytes_per_launch": kb,
+                         "traffic": profiled_traffic(args.workload, kern)},
+            "clocks": clocks.summary(),
+            "e2e": {"value": total_TL * ne / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / ne, "wall_s": e2e_wall,
+                    "path": "pinned host x, y_in, token_slot -> device; prepare_meta+shrink+expand; y -> host"},
+        }
+        if world == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = run_cpu_baseline(args)
+        print(json.dumps(line))
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.cpu_child:
+        cpu_child(args)
+        return 0
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

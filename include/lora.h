@@ -1,0 +1,216 @@
+/*
+ * rank_adapter_gb300 -- C ABI of the batched multi-LoRA delta on sm_103a.
+ *
+ * What the library computes (row-vector orientation of the handbook page
+ * "多 LoRA 服务：分段矩阵乘与适配器调度", section "不合并权重，批量计算"):
+ *
+ *     y[t] += scale[a] * (x[t] . A[a]) . B[a]      a = token_slot[t] != 0
+ *
+ * over a stacked GPU slot table of adapters; slot 0 means "no LoRA" and its
+ * rows of y are never touched. The delta is split into a shrink (x -> rank r,
+ * fp32 buffer) and an expand (buffer -> packed output slices, added into the
+ * caller's base-layer output), as in section "两个低秩 GEMM:shrink、expand 与
+ * fp32 中转缓冲" of the page "vLLM 源码完全拆解(十八): 多 LoRA 服务".
+ *
+ * Conventions for every entry point
+ * ---------------------------------
+ * - Ownership: the caller owns every buffer (allocated with torch or
+ *   cudaMalloc). The library allocates no device memory, keeps no pointer
+ *   after a call returns, and holds no state between calls.
+ * - Pointers named "device" must be device-accessible; all buffers must be
+ *   16-byte aligned, and leading dimensions (ldx, ldy) times the element size
+ *   must be multiples of 16 bytes.
+ * - Every call is asynchronous on `stream` (NULL = the legacy default
+ *   stream) and returns a lora_status. Argument errors are found on the host,
+ *   before anything is launched. LORA_ECUDA means a launch failed;
+ *   lora_last_cuda_error() returns the CUDA error code.
+ * - Device-side conditions never trap or hang: a token slot id outside
+ *   [0, num_slots) is treated as slot 0 and counted in meta->status
+ *   (read it with lora_query_status).
+ * - Grid sizes depend only on host-known bounds (num_tokens, num_slots,
+ *   shapes), never on device data, so a sequence of calls can be captured in
+ *   a CUDA graph once it has run eagerly once.
+ */
+#ifndef RANK_ADAPTER_GB300_LORA_H
+#define RANK_ADAPTER_GB300_LORA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st *lora_stream_t;
+
+typedef enum {
+  LORA_OK = 0,
+  LORA_EINVAL = 1,        /* bad argument: null pointer, bad shape, mismatched sizes */
+  LORA_ERANGE = 2,        /* a value outside its range: slot, rank, num_slots, num_tokens */
+  LORA_EALIGN = 3,        /* a pointer or leading dimension is not 16-byte aligned */
+  LORA_EUNSUPPORTED = 4,  /* valid but not implemented (e.g. SGMV on fp32 tables) */
+  LORA_ECUDA = 5,         /* a CUDA launch or copy failed; see lora_last_cuda_error() */
+  LORA_EBADSLOT = 6       /* lora_query_status: some token slot ids were out of range */
+} lora_status;
+
+typedef enum { LORA_F32 = 0, LORA_BF16 = 1 } lora_dtype;
+
+/* Which kernel family runs a shrink / expand.
+ * BGMV: per-segment streaming of each adapter's A/B on CUDA cores (decode).
+ * SGMV: tensor-core (tcgen05) tiles over same-adapter segments (prefill), bf16 only.
+ * AUTO: segments with fewer than LORA_SGMV_MIN_ROWS tokens go to BGMV, the
+ *       others to SGMV (fp32 tables: all BGMV). */
+typedef enum { LORA_AUTO = 0, LORA_BGMV = 1, LORA_SGMV = 2 } lora_kind;
+
+#define LORA_MAX_SLICES 4
+#define LORA_MAX_NUM_SLOTS 1024
+#define LORA_MAX_RANK 128
+#define LORA_MAX_TOKENS (1 << 24)
+#define LORA_SGMV_MIN_ROWS 64      /* AUTO threshold: segment rows routed to SGMV */
+#define LORA_SGMV_TILE_M 128       /* rows per SGMV tile (work-list granularity) */
+
+/*
+ * One LoRA-wrapped layer: the stacked slot table of one (packed) projection.
+ * Layout follows the stacked per-slice buffers of the vLLM page, section
+ * "包装层的形态" (lora_a_stacked / lora_b_stacked, one pair per packed slice),
+ * stored in row-vector orientation:
+ *   A[s]: device, [num_slots, d_in, r_max] row-major, dtype elements
+ *   B[s]: device, [num_slots, r_max, out_sizes[s]] row-major
+ *   slot_rank: device int32 [num_slots], rank of each slot (0 = empty)
+ *   slot_scale: device fp32 [num_slots], scale applied to the shrink result
+ * Slot 0 is reserved (kept zero, rank 0). Constraints: dtype in lora_dtype;
+ * 1 <= n_slices <= LORA_MAX_SLICES; d_in and every out_sizes[s] positive
+ * multiples of 8; r_max a power of two in [8, LORA_MAX_RANK];
+ * 1 <= num_slots <= LORA_MAX_NUM_SLOTS. The library only reads this struct.
+ */
+typedef struct {
+  int32_t dtype;
+  int32_t d_in;
+  int32_t n_slices;
+  int32_t out_sizes[LORA_MAX_SLICES];
+  int32_t num_slots;
+  int32_t r_max;
+  void *A[LORA_MAX_SLICES];
+  void *B[LORA_MAX_SLICES];
+  int32_t *slot_rank;
+  float *slot_scale;
+} lora_layer_desc;
+
+/*
+ * Per-step token metadata (LoRAKernelMeta of the vLLM page, section
+ * "LoRAKernelMeta:先按槽位排序"), relabelled so that slot 0 is no-LoRA.
+ * All pointers are device pointers owned by the caller:
+ *   token_slot  [num_tokens]     input: slot id of every token, batch order
+ *   sorted_rows [num_tokens]     token indices, stably sorted by slot
+ *   seg_slot    [num_slots]      slots present, ascending; then -1
+ *   seg_count   [num_slots]      tokens per segment; then 0
+ *   seg_start   [num_slots + 1]  first sorted row of each segment (leading 0),
+ *                                then num_tokens
+ *   num_segs, no_lora, status    [1] each: segments present; 1 if no token
+ *                                uses a real adapter; count of token ids that
+ *                                were outside [0, num_slots)
+ *   tiles       work lists the kernels read (segment lists per kernel family
+ *               and SGMV tile offsets); at least lora_meta_tiles_bytes(num_slots)
+ *               bytes. Its layout is private to the library.
+ */
+typedef struct {
+  const int32_t *token_slot;
+  int32_t num_tokens;
+  int32_t num_slots;
+  int32_t *sorted_rows;
+  int32_t *seg_slot;
+  int32_t *seg_count;
+  int32_t *seg_start;
+  int32_t *num_segs;
+  int32_t *no_lora;
+  int32_t *status;
+  void *tiles;
+  size_t tiles_bytes;
+} lora_meta;
+
+/*
+ * Write an adapter into slot `slot` of every packed slice (set_lora of the
+ * vLLM page, section "activate_adapter:把 CPU 上的低秩矩阵搬进 GPU 槽位").
+ *   A_src[s]: device, [d_in, rank] row-major; B_src[s]: device,
+ *   [rank, out_sizes[s]] row-major, desc->dtype elements; both arrays hold
+ *   desc->n_slices pointers. A slice whose A_src and B_src are both NULL is
+ *   zeroed (the adapter did not train it); exactly one NULL is LORA_EINVAL.
+ * The rank tail [rank, r_max) is zero-filled so the math stays exact, and
+ * slot_rank[slot] = rank, slot_scale[slot] = scale.
+ * Errors: slot outside [1, num_slots) or rank outside [1, r_max] -> LORA_ERANGE.
+ * The sources are only read during the call's kernels on `stream`.
+ */
+int lora_set_slot(const lora_layer_desc *desc, int32_t slot, int32_t rank, float scale,
+                  const void *const *A_src, const void *const *B_src, lora_stream_t stream);
+
+/*
+ * Zero slot `slot` of every slice and set its rank and scale to 0 (reset_lora
+ * of the same section). slot outside [1, num_slots) -> LORA_ERANGE.
+ */
+int lora_reset_slot(const lora_layer_desc *desc, int32_t slot, lora_stream_t stream);
+
+/*
+ * Build the per-step token metadata from meta->token_slot: a stable counting
+ * sort of token indices by slot, the segments, no_lora, status and the work
+ * lists, bit-exactly (LoRAKernelMeta.prepare_tensors of the vLLM page,
+ * section "LoRAKernelMeta:先按槽位排序"). One call per step serves every
+ * layer. num_tokens == 0 is valid (num_segs = 0, no_lora = 1).
+ * Errors: num_slots outside [1, LORA_MAX_NUM_SLOTS], num_tokens outside
+ * [0, LORA_MAX_TOKENS], a null output, tiles_bytes too small.
+ */
+int lora_prepare_meta(const lora_meta *meta, lora_stream_t stream);
+
+/*
+ * Shrink: for every token t whose slot a != 0 and every slice s,
+ *   buf[s, t, k] = slot_scale[a] * sum_j x[t, j] * A[s][a, j, k]   (k < rank a)
+ *   buf[s, t, k] = 0                                               (rank a <= k < r_max)
+ * (lora_shrink / add_shrink of the vLLM page, section "shrink 核"; the scale
+ * enters here as in section "PEFTHelper:认清 adapter 文件").
+ *   x:   device, [num_tokens, d_in] with row stride ldx elements, desc->dtype
+ *   buf: device fp32, [n_slices, num_tokens, r_max] contiguous; rows of
+ *        slot-0 tokens are not written
+ *   ws:  scratch; may be NULL when lora_workspace_bytes() returns 0
+ * bf16 inputs are multiplied exactly and accumulated in fp32 in a fixed
+ * order (results do not depend on the batch's other tokens).
+ */
+int lora_shrink(const lora_layer_desc *desc, const lora_meta *meta, const void *x, int64_t ldx,
+                float *buf, int32_t kind, void *ws, size_t ws_bytes, lora_stream_t stream);
+
+/*
+ * Expand: for every token t whose slot a != 0 and every slice s,
+ *   y[t, off_s + n] = y[t, off_s + n] + sum_{k < rank a} buf[s, t, k] * B[s][a, k, n]
+ * with off_s = out_sizes[0] + ... + out_sizes[s-1] (packed qkv / gate_up
+ * outputs; lora_expand of the vLLM page, section "expand 核"). The sum is
+ * formed in fp32 and added to y once; a bf16 y is rounded to nearest even.
+ * Rows of slot-0 tokens are not read or written.
+ *   buf: device fp32 [n_slices, num_tokens, r_max] as written by lora_shrink
+ *   y:   device, [num_tokens, sum(out_sizes)] with row stride ldy elements,
+ *        y_dtype (LORA_BF16 production; LORA_F32 for accuracy runs; an fp32
+ *        table requires LORA_F32)
+ */
+int lora_expand(const lora_layer_desc *desc, const lora_meta *meta, const float *buf, void *y,
+                int64_t ldy, int32_t y_dtype, int32_t kind, lora_stream_t stream);
+
+/* Scratch bytes lora_shrink needs for this layer and token bound (0: none). */
+size_t lora_workspace_bytes(const lora_layer_desc *desc, int32_t max_tokens, int32_t kind);
+
+/* Bytes the meta->tiles work-list buffer needs for a table of num_slots slots. */
+size_t lora_meta_tiles_bytes(int32_t num_slots);
+
+/*
+ * Synchronise `stream`, copy meta->status to *out (host) and return LORA_OK
+ * if it is 0, LORA_EBADSLOT if some token ids were out of range.
+ */
+int lora_query_status(const lora_meta *meta, int32_t *out, lora_stream_t stream);
+
+/* Static description of a lora_status value. */
+const char *lora_strerror(int status);
+
+/* CUDA error code of the last LORA_ECUDA returned on this host thread (0 if none). */
+int lora_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* RANK_ADAPTER_GB300_LORA_H */

@@ -1,0 +1,179 @@
+// Shared device helpers and internal launcher declarations for the sm_103a
+// multi-LoRA kernels. Nothing here is part of the C ABI (include/lora.h).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include <algorithm>
+
+#include "lora.h"
+
+namespace ra {
+
+// ------------------------------------------------------------------ element types
+
+template <typename T> struct Elem;
+template <> struct Elem<float> {
+  static constexpr int kVec = 4;  // elements per 16-byte vector
+  __device__ static inline float to_f(float v) { return v; }
+  __device__ static inline float from_f(float v) { return v; }
+};
+template <> struct Elem<__nv_bfloat16> {
+  static constexpr int kVec = 8;
+  __device__ static inline float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
+  __device__ static inline __nv_bfloat16 from_f(float v) { return __float2bfloat16_rn(v); }
+};
+
+// 8 consecutive elements widened to fp32 (one 16-byte vector of bf16, two of fp32).
+__device__ __forceinline__ void load8_f32(const __nv_bfloat16 *p, float (&v)[8]) {
+  uint4 u = __ldg(reinterpret_cast<const uint4 *>(p));
+  const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float2 f = __bfloat1622float2(h[i]);
+    v[2 * i] = f.x;
+    v[2 * i + 1] = f.y;
+  }
+}
+__device__ __forceinline__ void load8_f32(const float *p, float (&v)[8]) {
+  float4 a = __ldg(reinterpret_cast<const float4 *>(p));
+  float4 b = __ldg(reinterpret_cast<const float4 *>(p) + 1);
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+// Plain (coherent) loads for buffers the same grid may also write (y).
+__device__ __forceinline__ void load8_rw(const __nv_bfloat16 *p, float (&v)[8]) {
+  uint4 u = *reinterpret_cast<const uint4 *>(p);
+  const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float2 f = __bfloat1622float2(h[i]);
+    v[2 * i] = f.x;
+    v[2 * i + 1] = f.y;
+  }
+}
+__device__ __forceinline__ void load8_rw(const float *p, float (&v)[8]) {
+  float4 a = reinterpret_cast<const float4 *>(p)[0];
+  float4 b = reinterpret_cast<const float4 *>(p)[1];
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+__device__ __forceinline__ void store8(__nv_bfloat16 *p, const float (&v)[8]) {
+  uint4 u;
+  __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+  *reinterpret_cast<uint4 *>(p) = u;
+}
+__device__ __forceinline__ void store8(float *p, const float (&v)[8]) {
+  reinterpret_cast<float4 *>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
+  reinterpret_cast<float4 *>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
+}
+
+// ------------------------------------------------------------------ cluster / shared memory
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+// Full cluster barrier with release/acquire ordering of shared-memory writes.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+               "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+// Load a float4 from the same shared-memory offset in CTA `rank` of this cluster.
+__device__ __forceinline__ float4 ld_dsmem_f4(uint32_t local_addr, uint32_t rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(rank));
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(remote) : "memory");
+  return v;
+}
+
+// ------------------------------------------------------------------ work lists (meta->tiles)
+//
+// int32 layout written by the metadata kernel and read by shrink / expand:
+//   [0] n_all    LoRA segments (slot != 0)
+//   [1] n_small  LoRA segments with < LORA_SGMV_MIN_ROWS tokens
+//   [2] n_large  LoRA segments with >= LORA_SGMV_MIN_ROWS tokens
+//   [3] tiles_all    sum over all LoRA segments of ceil(count / LORA_SGMV_TILE_M)
+//   [4] tiles_large  the same over the large segments
+//   [5..7] reserved (0)
+//   then five arrays, S = num_slots:
+//   all_seg[S], small_seg[S], large_seg[S], all_tile_start[S+1], large_tile_start[S+1]
+struct WorkLists {
+  static constexpr int kHeader = 8;
+  __host__ __device__ static inline size_t ints(int S) { return kHeader + 5 * (size_t)S + 2; }
+  __host__ __device__ static inline int all_seg(int S) { (void)S; return kHeader; }
+  __host__ __device__ static inline int small_seg(int S) { return kHeader + S; }
+  __host__ __device__ static inline int large_seg(int S) { return kHeader + 2 * S; }
+  __host__ __device__ static inline int all_tile_start(int S) { return kHeader + 3 * S; }
+  __host__ __device__ static inline int large_tile_start(int S) { return kHeader + 4 * S + 1; }
+};
+
+enum ListSel { kListAll = 0, kListSmall = 1, kListLarge = 2 };
+
+// Device-side view of the metadata used by the compute kernels.
+struct MetaView {
+  const int32_t *sorted_rows;
+  const int32_t *seg_slot;
+  const int32_t *seg_count;
+  const int32_t *seg_start;
+  const int32_t *work;
+  int32_t num_tokens;
+  int32_t num_slots;
+};
+
+// ------------------------------------------------------------------ host helpers
+
+// Raise a kernel's dynamic shared-memory limit once per (kernel, device).
+cudaError_t set_max_dynamic_smem(const void *kernel, int bytes);
+
+// Launch with a thread-block cluster of `cluster_x` CTAs along x.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                           unsigned cluster_x, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cluster_x;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+// ------------------------------------------------------------------ internal launchers
+// Each returns a cudaError_t from the launch (cudaSuccess if nothing to launch).
+
+cudaError_t launch_slot_write(const lora_layer_desc &d, int slot, int rank, float scale,
+                              const void *const *A_src, const void *const *B_src, cudaStream_t st);
+cudaError_t launch_prepare_meta(const lora_meta &m, cudaStream_t st);
+cudaError_t launch_bgmv_shrink(const lora_layer_desc &d, const MetaView &mv, ListSel sel,
+                               const void *x, int64_t ldx, float *buf, cudaStream_t st);
+cudaError_t launch_bgmv_expand(const lora_layer_desc &d, const MetaView &mv, ListSel sel,
+                               const float *buf, void *y, int64_t ldy, int y_dtype, cudaStream_t st);
+bool sgmv_supported();
+cudaError_t launch_sgmv_shrink(const lora_layer_desc &d, const MetaView &mv, ListSel sel,
+                               const void *x, int64_t ldx, float *buf, cudaStream_t st);
+cudaError_t launch_sgmv_expand(const lora_layer_desc &d, const MetaView &mv, ListSel sel,
+                               const float *buf, void *y, int64_t ldy, int y_dtype, cudaStream_t st);
+
+}  // namespace ra

@@ -1,0 +1,211 @@
+// Host side of the C ABI declared in include/lora.h: argument validation,
+// dispatch to the kernel families, status codes. Nothing here allocates
+// device memory or keeps state between calls beyond per-(kernel, device)
+// launch attributes.
+#include <algorithm>
+#include <mutex>
+#include <set>
+#include <utility>
+
+#include "common.cuh"
+
+namespace ra {
+
+cudaError_t set_max_dynamic_smem(const void *kernel, int bytes) {
+  static std::mutex mu;
+  static std::set<std::pair<const void *, int>> done;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  if (done.count({kernel, dev})) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done.insert({kernel, dev});
+  return e;
+}
+
+}  // namespace ra
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+int cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return LORA_OK;
+  g_last_cuda_error = (int)e;
+  return LORA_ECUDA;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t elem_size(int dtype) { return dtype == LORA_BF16 ? 2 : 4; }
+
+int check_desc(const lora_layer_desc *d) {
+  if (d == nullptr) return LORA_EINVAL;
+  if (d->dtype != LORA_F32 && d->dtype != LORA_BF16) return LORA_EINVAL;
+  if (d->n_slices < 1 || d->n_slices > LORA_MAX_SLICES) return LORA_ERANGE;
+  if (d->d_in < 8 || d->d_in % 8 != 0) return LORA_EINVAL;
+  if (d->r_max < 8 || d->r_max > LORA_MAX_RANK || (d->r_max & (d->r_max - 1)) != 0) return LORA_ERANGE;
+  if (d->num_slots < 1 || d->num_slots > LORA_MAX_NUM_SLOTS) return LORA_ERANGE;
+  for (int s = 0; s < d->n_slices; ++s) {
+    if (d->out_sizes[s] < 8 || d->out_sizes[s] % 8 != 0) return LORA_EINVAL;
+    if (d->A[s] == nullptr || d->B[s] == nullptr) return LORA_EINVAL;
+    if (!aligned16(d->A[s]) || !aligned16(d->B[s])) return LORA_EALIGN;
+  }
+  if (d->slot_rank == nullptr || d->slot_scale == nullptr) return LORA_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(d->slot_rank) & 3u) || (reinterpret_cast<uintptr_t>(d->slot_scale) & 3u))
+    return LORA_EALIGN;
+  return LORA_OK;
+}
+
+int check_meta(const lora_meta *m) {
+  if (m == nullptr) return LORA_EINVAL;
+  if (m->num_slots < 1 || m->num_slots > LORA_MAX_NUM_SLOTS) return LORA_ERANGE;
+  if (m->num_tokens < 0 || m->num_tokens > LORA_MAX_TOKENS) return LORA_ERANGE;
+  if (m->num_tokens > 0 && (m->token_slot == nullptr || m->sorted_rows == nullptr)) return LORA_EINVAL;
+  if (!m->seg_slot || !m->seg_count || !m->seg_start || !m->num_segs || !m->no_lora || !m->status || !m->tiles)
+    return LORA_EINVAL;
+  if (m->tiles_bytes < lora_meta_tiles_bytes(m->num_slots)) return LORA_EINVAL;
+  if (reinterpret_cast<uintptr_t>(m->tiles) & 3u) return LORA_EALIGN;
+  return LORA_OK;
+}
+
+ra::MetaView view_of(const lora_meta *m) {
+  ra::MetaView v;
+  v.sorted_rows = m->sorted_rows;
+  v.seg_slot = m->seg_slot;
+  v.seg_count = m->seg_count;
+  v.seg_start = m->seg_start;
+  v.work = static_cast<const int32_t *>(m->tiles);
+  v.num_tokens = m->num_tokens;
+  v.num_slots = m->num_slots;
+  return v;
+}
+
+// The SGMV family exists for bf16 tables only.
+bool sgmv_available(const lora_layer_desc *d) { return d->dtype == LORA_BF16 && ra::sgmv_supported(); }
+
+}  // namespace
+
+extern "C" {
+
+const char *lora_strerror(int status) {
+  switch (status) {
+    case LORA_OK: return "success";
+    case LORA_EINVAL: return "invalid argument (null pointer, shape or size mismatch)";
+    case LORA_ERANGE: return "value out of range (slot, rank, num_slots, num_tokens or n_slices)";
+    case LORA_EALIGN: return "pointer or leading dimension not 16-byte aligned";
+    case LORA_EUNSUPPORTED: return "unsupported combination (e.g. SGMV on an fp32 table)";
+    case LORA_ECUDA: return "CUDA launch or copy failed (see lora_last_cuda_error)";
+    case LORA_EBADSLOT: return "some token slot ids were outside [0, num_slots) and were treated as slot 0";
+    default: return "unknown lora_status";
+  }
+}
+
+int lora_last_cuda_error(void) { return g_last_cuda_error; }
+
+size_t lora_meta_tiles_bytes(int32_t num_slots) {
+  if (num_slots < 1) return 0;
+  return ra::WorkLists::ints(num_slots) * sizeof(int32_t);
+}
+
+size_t lora_workspace_bytes(const lora_layer_desc *desc, int32_t max_tokens, int32_t kind) {
+  (void)desc;
+  (void)max_tokens;
+  (void)kind;
+  return 0;  // split-K partials are reduced in distributed shared memory
+}
+
+int lora_set_slot(const lora_layer_desc *desc, int32_t slot, int32_t rank, float scale,
+                  const void *const *A_src, const void *const *B_src, lora_stream_t stream) {
+  int st = check_desc(desc);
+  if (st != LORA_OK) return st;
+  if (slot < 1 || slot >= desc->num_slots) return LORA_ERANGE;
+  if (rank < 1 || rank > desc->r_max) return LORA_ERANGE;
+  if (A_src == nullptr || B_src == nullptr) return LORA_EINVAL;
+  for (int s = 0; s < desc->n_slices; ++s) {
+    if ((A_src[s] == nullptr) != (B_src[s] == nullptr)) return LORA_EINVAL;
+    if (B_src[s] != nullptr && !aligned16(B_src[s])) return LORA_EALIGN;
+    if (A_src[s] != nullptr && (reinterpret_cast<uintptr_t>(A_src[s]) % elem_size(desc->dtype))) return LORA_EALIGN;
+  }
+  return cuda_status(ra::launch_slot_write(*desc, slot, rank, scale, A_src, B_src, (cudaStream_t)stream));
+}
+
+int lora_reset_slot(const lora_layer_desc *desc, int32_t slot, lora_stream_t stream) {
+  int st = check_desc(desc);
+  if (st != LORA_OK) return st;
+  if (slot < 1 || slot >= desc->num_slots) return LORA_ERANGE;
+  return cuda_status(ra::launch_slot_write(*desc, slot, 0, 0.f, nullptr, nullptr, (cudaStream_t)stream));
+}
+
+int lora_prepare_meta(const lora_meta *meta, lora_stream_t stream) {
+  int st = check_meta(meta);
+  if (st != LORA_OK) return st;
+  return cuda_status(ra::launch_prepare_meta(*meta, (cudaStream_t)stream));
+}
+
+int lora_shrink(const lora_layer_desc *desc, const lora_meta *meta, const void *x, int64_t ldx,
+                float *buf, int32_t kind, void *ws, size_t ws_bytes, lora_stream_t stream) {
+  (void)ws;
+  (void)ws_bytes;
+  int st = check_desc(desc);
+  if (st != LORA_OK) return st;
+  st = check_meta(meta);
+  if (st != LORA_OK) return st;
+  if (meta->num_slots != desc->num_slots) return LORA_EINVAL;
+  if (kind != LORA_AUTO && kind != LORA_BGMV && kind != LORA_SGMV) return LORA_EINVAL;
+  if (kind == LORA_SGMV && !sgmv_available(desc)) return LORA_EUNSUPPORTED;
+  if (meta->num_tokens == 0) return LORA_OK;
+  if (x == nullptr || buf == nullptr) return LORA_EINVAL;
+  if (ldx < desc->d_in) return LORA_EINVAL;
+  if (!aligned16(x) || !aligned16(buf) || (ldx * (int64_t)elem_size(desc->dtype)) % 16 != 0) return LORA_EALIGN;
+  const ra::MetaView mv = view_of(meta);
+  cudaStream_t s = (cudaStream_t)stream;
+  if (kind == LORA_BGMV || (kind == LORA_AUTO && !sgmv_available(desc)))
+    return cuda_status(ra::launch_bgmv_shrink(*desc, mv, ra::kListAll, x, ldx, buf, s));
+  if (kind == LORA_SGMV)
+    return cuda_status(ra::launch_sgmv_shrink(*desc, mv, ra::kListAll, x, ldx, buf, s));
+  st = cuda_status(ra::launch_bgmv_shrink(*desc, mv, ra::kListSmall, x, ldx, buf, s));
+  if (st != LORA_OK) return st;
+  return cuda_status(ra::launch_sgmv_shrink(*desc, mv, ra::kListLarge, x, ldx, buf, s));
+}
+
+int lora_expand(const lora_layer_desc *desc, const lora_meta *meta, const float *buf, void *y,
+                int64_t ldy, int32_t y_dtype, int32_t kind, lora_stream_t stream) {
+  int st = check_desc(desc);
+  if (st != LORA_OK) return st;
+  st = check_meta(meta);
+  if (st != LORA_OK) return st;
+  if (meta->num_slots != desc->num_slots) return LORA_EINVAL;
+  if (kind != LORA_AUTO && kind != LORA_BGMV && kind != LORA_SGMV) return LORA_EINVAL;
+  if (y_dtype != LORA_F32 && y_dtype != LORA_BF16) return LORA_EINVAL;
+  if (desc->dtype == LORA_F32 && y_dtype != LORA_F32) return LORA_EUNSUPPORTED;
+  if (kind == LORA_SGMV && !sgmv_available(desc)) return LORA_EUNSUPPORTED;
+  if (meta->num_tokens == 0) return LORA_OK;
+  if (y == nullptr || buf == nullptr) return LORA_EINVAL;
+  int64_t total = 0;
+  for (int s = 0; s < desc->n_slices; ++s) total += desc->out_sizes[s];
+  if (ldy < total) return LORA_EINVAL;
+  if (!aligned16(y) || !aligned16(buf) || (ldy * (int64_t)elem_size(y_dtype)) % 16 != 0) return LORA_EALIGN;
+  const ra::MetaView mv = view_of(meta);
+  cudaStream_t s = (cudaStream_t)stream;
+  if (kind == LORA_BGMV || (kind == LORA_AUTO && !sgmv_available(desc)))
+    return cuda_status(ra::launch_bgmv_expand(*desc, mv, ra::kListAll, buf, y, ldy, y_dtype, s));
+  if (kind == LORA_SGMV)
+    return cuda_status(ra::launch_sgmv_expand(*desc, mv, ra::kListAll, buf, y, ldy, y_dtype, s));
+  st = cuda_status(ra::launch_bgmv_expand(*desc, mv, ra::kListSmall, buf, y, ldy, y_dtype, s));
+  if (st != LORA_OK) return st;
+  return cuda_status(ra::launch_sgmv_expand(*desc, mv, ra::kListLarge, buf, y, ldy, y_dtype, s));
+}
+
+int lora_query_status(const lora_meta *meta, int32_t *out, lora_stream_t stream) {
+  if (meta == nullptr || meta->status == nullptr || out == nullptr) return LORA_EINVAL;
+  int32_t v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, meta->status, sizeof(int32_t), cudaMemcpyDeviceToHost, (cudaStream_t)stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_status(e);
+  *out = v;
+  return v == 0 ? LORA_OK : LORA_EBADSLOT;
+}
+
+}  // extern "C"

@@ -1,0 +1,205 @@
+// Token metadata (LoRAKernelMeta.prepare_tensors of the page "vLLM 源码完全拆解(十八):
+// 多 LoRA 服务", section "LoRAKernelMeta:先按槽位排序"): a stable counting sort of
+// token indices by slot, the segments present (ascending slot, with counts and
+// start offsets that begin at 0), the no-LoRA flag, and the work lists the
+// shrink / expand kernels read.
+//
+// One CTA of 32 warps. Each warp owns a contiguous range of tokens and keeps a
+// private histogram row in shared memory; a per-slot pass turns the histograms
+// into exclusive per-(warp, slot) offsets; the scatter pass walks every warp's
+// range in batch order and ranks equal slots inside each 32-token chunk with
+// __match_any_sync. Warp ranges are in batch order, so the sort is stable and
+// its result does not depend on scheduling.
+#include "common.cuh"
+
+namespace ra {
+namespace {
+
+constexpr int kThreads = 1024;
+constexpr int kWarps = kThreads / 32;
+
+struct MetaArgs {
+  const int32_t *token_slot;
+  int32_t T, S;
+  int32_t *sorted_rows, *seg_slot, *seg_count, *seg_start, *num_segs, *no_lora, *status;
+  int32_t *work;
+};
+
+__device__ __forceinline__ uint32_t lanemask_lt() {
+  uint32_t m;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+  return m;
+}
+
+// Exclusive prefix sum of one value per thread over the whole CTA; all threads call it.
+__device__ int block_excl_scan(int v, int *warp_tmp, int &total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_tmp[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = warp_tmp[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    warp_tmp[lane] = w;
+  }
+  __syncthreads();
+  const int prefix = (warp > 0 ? warp_tmp[warp - 1] : 0) + x - v;
+  total = warp_tmp[kWarps - 1];
+  __syncthreads();
+  return prefix;
+}
+
+__global__ void __launch_bounds__(kThreads, 1) prepare_meta_kernel(MetaArgs a) {
+  extern __shared__ int32_t sm[];
+  const int S = a.S, T = a.T;
+  int32_t *hist = sm;  // [kWarps][S]: counts, then absolute write offsets
+  __shared__ int warp_tmp[kWarps];
+  __shared__ int s_bad;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+  for (int i = tid; i < kWarps * S; i += kThreads) hist[i] = 0;
+  if (tid == 0) s_bad = 0;
+  __syncthreads();
+
+  // Pass 1: per-warp histograms over contiguous token ranges.
+  const int per = (T + kWarps - 1) / kWarps;
+  const int t0 = min(T, warp * per), t1 = min(T, t0 + per);
+  int bad = 0;
+  for (int base = t0; base < t1; base += 32) {
+    const int t = base + lane;
+    const bool valid = t < t1;
+    int s = 0;
+    if (valid) {
+      s = a.token_slot[t];
+      if (s < 0 || s >= S) { s = 0; ++bad; }
+    }
+    const uint32_t act = __ballot_sync(0xffffffffu, valid);
+    if (valid) {
+      const uint32_t peers = __match_any_sync(act, s);
+      if (lane == __ffs(peers) - 1) hist[warp * S + s] += __popc(peers);
+    }
+    __syncwarp();
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) bad += __shfl_xor_sync(0xffffffffu, bad, o);
+  if (lane == 0 && bad) atomicAdd(&s_bad, bad);
+  __syncthreads();
+
+  // Per slot (thread = slot): total count and exclusive offsets inside the slot.
+  int tot = 0;
+  if (tid < S) {
+    for (int w = 0; w < kWarps; ++w) {
+      const int c = hist[w * S + tid];
+      hist[w * S + tid] = tot;
+      tot += c;
+    }
+  }
+  int total;
+  const int base = block_excl_scan(tid < S ? tot : 0, warp_tmp, total);  // first sorted row of slot
+  if (tid < S)
+    for (int w = 0; w < kWarps; ++w) hist[w * S + tid] += base;
+
+  const bool present = tid < S && tot > 0;
+  const bool lora = present && tid != 0;
+  const bool small = lora && tot < LORA_SGMV_MIN_ROWS;
+  const bool large = lora && tot >= LORA_SGMV_MIN_ROWS;
+  const int tiles = lora ? (tot + LORA_SGMV_TILE_M - 1) / LORA_SGMV_TILE_M : 0;
+  int nsegs, n_all, n_small, n_large, tiles_all, tiles_large;
+  const int seg_idx = block_excl_scan(present ? 1 : 0, warp_tmp, nsegs);
+  const int all_idx = block_excl_scan(lora ? 1 : 0, warp_tmp, n_all);
+  const int small_idx = block_excl_scan(small ? 1 : 0, warp_tmp, n_small);
+  const int large_idx = block_excl_scan(large ? 1 : 0, warp_tmp, n_large);
+  const int tile_all0 = block_excl_scan(tiles, warp_tmp, tiles_all);
+  const int tile_large0 = block_excl_scan(large ? tiles : 0, warp_tmp, tiles_large);
+
+  int32_t *W = a.work;
+  if (present) {
+    a.seg_slot[seg_idx] = tid;
+    a.seg_count[seg_idx] = tot;
+    a.seg_start[seg_idx] = base;
+  }
+  if (lora) {
+    W[WorkLists::all_seg(S) + all_idx] = seg_idx;
+    W[WorkLists::all_tile_start(S) + all_idx] = tile_all0;
+  }
+  if (small) W[WorkLists::small_seg(S) + small_idx] = seg_idx;
+  if (large) {
+    W[WorkLists::large_seg(S) + large_idx] = seg_idx;
+    W[WorkLists::large_tile_start(S) + large_idx] = tile_large0;
+  }
+  // Tails and scalars.
+  for (int i = tid; i <= S; i += kThreads) {
+    if (i < S && i >= nsegs) { a.seg_slot[i] = -1; a.seg_count[i] = 0; }
+    if (i >= nsegs) a.seg_start[i] = T;
+    if (i < S) {
+      if (i >= n_all) W[WorkLists::all_seg(S) + i] = -1;
+      if (i >= n_small) W[WorkLists::small_seg(S) + i] = -1;
+      if (i >= n_large) W[WorkLists::large_seg(S) + i] = -1;
+    }
+    if (i >= n_all) W[WorkLists::all_tile_start(S) + i] = tiles_all;
+    if (i >= n_large) W[WorkLists::large_tile_start(S) + i] = tiles_large;
+  }
+  if (tid == 0) {
+    W[0] = n_all; W[1] = n_small; W[2] = n_large; W[3] = tiles_all; W[4] = tiles_large;
+    W[5] = 0; W[6] = 0; W[7] = 0;
+    *a.num_segs = nsegs;
+    *a.status = s_bad;
+  }
+  // Thread 0 holds the slot-0 count (no-LoRA tokens and out-of-range ids).
+  if (tid == 0) *a.no_lora = (T - tot == 0) ? 1 : 0;
+
+  // Pass 2: stable scatter of token indices.
+  for (int b = t0; b < t1; b += 32) {
+    const int t = b + lane;
+    const bool valid = t < t1;
+    int s = 0;
+    if (valid) {
+      s = a.token_slot[t];
+      if (s < 0 || s >= S) s = 0;
+    }
+    const uint32_t act = __ballot_sync(0xffffffffu, valid);
+    uint32_t peers = 0;
+    if (valid) {
+      peers = __match_any_sync(act, s);
+      const int pos = hist[warp * S + s] + __popc(peers & lanemask_lt());
+      a.sorted_rows[pos] = t;
+    }
+    __syncwarp();
+    if (valid && lane == __ffs(peers) - 1) hist[warp * S + s] += __popc(peers);
+    __syncwarp();
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_prepare_meta(const lora_meta &m, cudaStream_t st) {
+  MetaArgs a;
+  a.token_slot = m.token_slot;
+  a.T = m.num_tokens;
+  a.S = m.num_slots;
+  a.sorted_rows = m.sorted_rows;
+  a.seg_slot = m.seg_slot;
+  a.seg_count = m.seg_count;
+  a.seg_start = m.seg_start;
+  a.num_segs = m.num_segs;
+  a.no_lora = m.no_lora;
+  a.status = m.status;
+  a.work = static_cast<int32_t *>(m.tiles);
+  const size_t smem = (size_t)kWarps * m.num_slots * sizeof(int32_t);
+  cudaError_t e = set_max_dynamic_smem((const void *)prepare_meta_kernel,
+                                       (int)((size_t)kWarps * LORA_MAX_NUM_SLOTS * sizeof(int32_t)));
+  if (e != cudaSuccess) return e;
+  prepare_meta_kernel<<<1, kThreads, smem, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace ra
