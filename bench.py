@@ -59,6 +59,8 @@ def parse_args(argv=None):
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", choices=sorted(WORKLOADS), default="decode_qkv")
     p.add_argument("--kind", choices=["auto", "bgmv", "sgmv"], default="auto")
+    p.add_argument("--path", choices=["fused", "split"], default="fused",
+                   help="fused: prepare_meta + lora_apply; split: prepare_meta + lora_shrink + lora_expand")
     p.add_argument("--replicas", type=int, default=0, help="device replicas (0: enough for 3x L2)")
     p.add_argument("--graph-steps", type=int, default=0, help="steps per captured graph (0: auto)")
     p.add_argument("--e2e-steps", type=int, default=200)
@@ -275,14 +277,22 @@ class Replica:
         return self.table.nbytes() + self.x.numel() * self.x.element_size() + \
             self.y.numel() * self.y.element_size()
 
-    def launch(self, ra, i, ev=None):
-        """Enqueue meta, shrink, expand on the current stream; ev: optional per-kernel event pairs."""
+    def launch(self, ra, i, ev=None, path="fused"):
+        """Enqueue one step on the current stream: prepare_meta then lora_apply (path "fused")
+        or lora_shrink + lora_expand (path "split"). ev: optional events around each call."""
         st = None
         if ev is not None:
             ev[0].record()
         ra.check(ra.lora_prepare_meta(self.meta.c, st), "prepare_meta")
         if ev is not None:
             ev[1].record()
+        if path == "fused":
+            buf = self.buf.data_ptr() if self.kind != ra.LORA_BGMV else 0
+            ra.check(ra.lora_apply(self.table.desc, self.meta.c, self.x.data_ptr(), self.x.stride(0), buf,
+                                   self.y.data_ptr(), self.y.stride(0), self.ydt, self.kind, st), "apply")
+            if ev is not None:
+                ev[2].record()
+            return
         ra.check(ra.lora_shrink(self.table.desc, self.meta.c, self.x.data_ptr(), self.x.stride(0),
                                 self.buf.data_ptr(), self.kind, 0, 0, st), "shrink")
         if ev is not None:
@@ -299,6 +309,73 @@ def _external_events(torch):
         return True
     except TypeError:
         return False
+
+
+KERNELS = {"fused": ("meta", "apply"), "split": ("meta", "shrink", "expand")}
+
+
+def time_path(torch, ra, reps, stream, path, steps, G, clocks=None, dist=None):
+    """Time `steps` steps of one path as CUDA-graph replays of G steps each (rotating replicas).
+
+    Returns (elapsed_ms over all steps, per-kernel mean durations in ms, how they were timed).
+    """
+    R = len(reps)
+    names = KERNELS[path]
+    ext = _external_events(torch)
+    evs = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(len(names) + 1)]
+           for _ in range(G)] if ext else None
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for i in range(G):
+            reps[i % R].launch(ra, i, evs[i] if ext else None, path=path)
+    tail = steps % G
+    graph_tail = None
+    if tail:
+        graph_tail = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph_tail, stream=stream):
+            for i in range(tail):
+                reps[i % R].launch(ra, i, path=path)
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            graph.replay()
+    stream.synchronize()
+
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    if clocks is not None:
+        clocks.start()
+        time.sleep(0.3)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        start.record()
+        for _ in range(steps // G):
+            graph.replay()
+        if graph_tail is not None:
+            graph_tail.replay()
+        end.record()
+    stream.synchronize()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    if clocks is not None:
+        clocks.stop()
+    elapsed_ms = start.elapsed_time(end)
+
+    if ext and steps >= G:
+        durs = {k: [e[j].elapsed_time(e[j + 1]) for e in evs] for j, k in enumerate(names)}
+        how = f"CUDA events around each call inside the captured graph (last replay, {G} steps)"
+    else:
+        n = min(200, max(R, steps))
+        evs2 = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)] for _ in range(n)]
+        with torch.cuda.stream(stream):
+            torch.cuda._sleep(int(2e8))
+            for i in range(n):
+                reps[i % R].launch(ra, i, evs2[i], path=path)
+        stream.synchronize()
+        durs = {k: [e[j].elapsed_time(e[j + 1]) for e in evs2] for j, k in enumerate(names)}
+        how = f"CUDA events around {n} eager launches enqueued behind a sleep kernel"
+    return elapsed_ms, {k: statistics.mean(v) for k, v in durs.items()}, how
 
 
 def run_ours(args):
@@ -342,73 +419,17 @@ def run_ours(args):
     stream = torch.cuda.Stream()
     with torch.cuda.stream(stream):
         for i in range(max(3, args.warmup)):
-            reps[i % R].launch(ra, i)
+            reps[i % R].launch(ra, i, path=args.path)
     stream.synchronize()
 
-    # Capture G steps (a multiple of R) into a graph; per-kernel events inside it if supported.
     G = args.graph_steps or R * max(1, 64 // R)
     G = min(G, max(1, args.steps))
-    ext = _external_events(torch)
-    evs = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)] for _ in range(G)] if ext else None
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        for i in range(G):
-            reps[i % R].launch(ra, i, evs[i] if ext else None)
-    tail = args.steps % G
-    graph_tail = None
-    if tail:
-        graph_tail = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph_tail, stream=stream):
-            for i in range(tail):
-                reps[i % R].launch(ra, i)
-    with torch.cuda.stream(stream):
-        for _ in range(2):
-            graph.replay()
-    stream.synchronize()
-
     vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
     clocks = ClockSampler(vis.split(",")[local].strip() if vis else str(local))
-    if dist is not None:
-        dist.barrier()
-    torch.cuda.synchronize()
-    clocks.start()
-    time.sleep(0.3)
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        start.record()
-        for _ in range(args.steps // G):
-            graph.replay()
-        if graph_tail is not None:
-            graph_tail.replay()
-        end.record()
-    stream.synchronize()
-    if dist is not None:
-        dist.barrier()
-    torch.cuda.synchronize()
-    clocks.stop()
-    elapsed_ms = start.elapsed_time(end)
-
-    # Per-kernel durations: from the events of the last graph replay, else an eager pass primed
-    # by a sleep kernel so that the host has enqueued every launch before the GPU reaches it.
-    if ext and args.steps >= G:
-        durs = {k: [] for k in ("meta", "shrink", "expand")}
-        for e in evs:
-            durs["meta"].append(e[0].elapsed_time(e[1]))
-            durs["shrink"].append(e[1].elapsed_time(e[2]))
-            durs["expand"].append(e[2].elapsed_time(e[3]))
-        kernel_timing = f"CUDA events around each launch inside the captured graph (last replay, {G} steps)"
-    else:
-        n = min(200, max(R, args.steps))
-        evs2 = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n)]
-        with torch.cuda.stream(stream):
-            torch.cuda._sleep(int(2e8))
-            for i in range(n):
-                reps[i % R].launch(ra, i, evs2[i])
-        stream.synchronize()
-        durs = {"meta": [e[0].elapsed_time(e[1]) for e in evs2], "shrink": [e[1].elapsed_time(e[2]) for e in evs2],
-                "expand": [e[2].elapsed_time(e[3]) for e in evs2]}
-        kernel_timing = f"CUDA events around {n} eager launches enqueued behind a sleep kernel"
-    avg = {k: statistics.mean(v) for k, v in durs.items()}
+    elapsed_ms, avg, kernel_timing = time_path(torch, ra, reps, stream, args.path, args.steps, G, clocks, dist)
+    other = "split" if args.path == "fused" else "fused"
+    other_steps = min(args.steps, 20 * G)
+    o_ms, o_avg, _ = time_path(torch, ra, reps, stream, other, other_steps, G)
 
     # End to end: the same step through the ABI with pinned host buffers and copies in / out.
     h_x = torch.empty_like(x0, device="cpu").pin_memory()
@@ -423,13 +444,17 @@ def run_ours(args):
     d2h = h_out.numel() * h_out.element_size()
     ne = max(3, args.e2e_steps)
     T = inst.num_tokens
+
+    def e2e_step(i):
+        e2e_rep.x.copy_(h_x, non_blocking=True)
+        e2e_rep.y.copy_(h_y, non_blocking=True)
+        e2e_rep.meta.token_slot[:T].copy_(h_ts, non_blocking=True)
+        e2e_rep.launch(ra, i, path=args.path)
+        h_out.copy_(e2e_rep.y, non_blocking=True)
+
     with torch.cuda.stream(stream):
         for i in range(3):
-            e2e_rep.x.copy_(h_x, non_blocking=True)
-            e2e_rep.y.copy_(h_y, non_blocking=True)
-            e2e_rep.meta.token_slot[:T].copy_(h_ts, non_blocking=True)
-            e2e_rep.launch(ra, i)
-            h_out.copy_(e2e_rep.y, non_blocking=True)
+            e2e_step(i)
     stream.synchronize()
     if dist is not None:
         dist.barrier()
@@ -438,11 +463,7 @@ def run_ours(args):
     with torch.cuda.stream(stream):
         e0.record()
         for i in range(ne):
-            e2e_rep.x.copy_(h_x, non_blocking=True)
-            e2e_rep.y.copy_(h_y, non_blocking=True)
-            e2e_rep.meta.token_slot[:T].copy_(h_ts, non_blocking=True)
-            e2e_rep.launch(ra, i)
-            h_out.copy_(e2e_rep.y, non_blocking=True)
+            e2e_step(i)
         e1.record()
     stream.synchronize()
     e2e_wall = time.perf_counter() - t0
@@ -458,13 +479,14 @@ def run_ours(args):
         elapsed_ms, e2e_ms, total_TL = float(mx[0]), float(mx[1]), float(tl[2])
     else:
         total_TL = float(alg["T_L"])
-    launches = 3 * args.steps
+    launches = len(KERNELS[args.path]) * args.steps
 
     if rank == 0:
         hbm, tc, src = load_peaks()
         step_ms = elapsed_ms / args.steps
-        kern = max(("shrink", "expand"), key=lambda k: avg[k])
-        kb = alg[f"{kern}_bytes"]
+        kbytes = {"apply": alg["step_bytes"], "shrink": alg["shrink_bytes"], "expand": alg["expand_bytes"]}
+        kern = max((k for k in avg if k != "meta"), key=lambda k: avg[k])
+        kb = kbytes[kern]
         ach = kb / (avg[kern] * 1e-3) / 1e9
         line = {
             "metric": METRIC, "value": total_TL * args.steps / (elapsed_ms * 1e-3), "unit": "tokens/s",
@@ -472,16 +494,20 @@ def run_ours(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": inst.dtype, "data": "synthetic",
             "config": {"workload": args.workload, "desc": WORKLOADS[args.workload], "kind": args.kind,
-                       "global_batch": inst.num_tokens * world, "lora_tokens_per_gpu": alg["T_L"],
-                       "active_adapters": alg["active"], "parallelism": f"dp{world}",
+                       "path": args.path, "global_batch": inst.num_tokens * world,
+                       "lora_tokens_per_gpu": alg["T_L"], "active_adapters": alg["active"],
+                       "parallelism": f"dp{world}",
                        "l2": f"rotating {R} device replicas x {per / 2**20:.1f} MiB "
                              f"(> 3x {L2_BYTES >> 20} MiB L2)",
                        "timing": f"CUDA-graph replays of {G} steps, CUDA events on the launching stream"},
             "gpu_launches": launches,
+            "step_algorithmic_bytes": alg["step_bytes"],
             "step_hbm_gbs": alg["step_bytes"] / (step_ms * 1e-3) / 1e9,
             "step_frac_of_hbm": alg["step_bytes"] / (step_ms * 1e-3) / 1e9 / hbm,
             "kernel_us": {k: v * 1e3 for k, v in avg.items()},
             "kernel_timing": kernel_timing,
+            f"{other}_path": {"ms_per_step": o_ms / other_steps, "kernel_us": {k: v * 1e3 for k, v in o_avg.items()},
+                              "steps": other_steps},
             "roofline": {"bound": "hbm", "kernel": kern, "achieved": ach, "peak": hbm, "unit": "GB/s",
                          "frac": ach / hbm, "peak_source": src,
                          "algorithmic_bytes_per_launch": kb,
@@ -489,7 +515,7 @@ def run_ours(args):
             "clocks": clocks.summary(),
             "e2e": {"value": total_TL * ne / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / ne, "wall_s": e2e_wall,
-                    "path": "pinned host x, y_in, token_slot -> device; prepare_meta+shrink+expand; y -> host"},
+                    "path": "pinned host x, y_in, token_slot -> device; one step; y -> host"},
         }
         if world == 1 and not args.no_cpu_baseline:
             line["cpu_baseline"] = run_cpu_baseline(args)

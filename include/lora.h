@@ -192,6 +192,24 @@ int lora_shrink(const lora_layer_desc *desc, const lora_meta *meta, const void *
 int lora_expand(const lora_layer_desc *desc, const lora_meta *meta, const float *buf, void *y,
                 int64_t ldy, int32_t y_dtype, int32_t kind, lora_stream_t stream);
 
+/*
+ * Fused shrink + expand: the whole delta for every LoRA token in one pass,
+ *   y[t, off_s + n] += sum_k (scale[a] * x[t] . A[s][a])[k] * B[s][a, k, n]
+ * with the same arithmetic, rounding and slot-0 rule as lora_shrink followed
+ * by lora_expand (results are bitwise equal for segments that run in the
+ * BGMV family). In the BGMV family one thread-block cluster per (segment,
+ * slice) reduces the rank-r row in distributed shared memory and adds it
+ * into y without an fp32 round trip through global memory (the
+ * "batched gather" form of the handbook page, section "不合并权重，批量计算").
+ *   buf: device fp32 [n_slices, num_tokens, r_max] or NULL. When non-NULL it
+ *        also receives the shrink result. It must be non-NULL when any
+ *        segment runs in the SGMV family (kind LORA_SGMV, or LORA_AUTO on a
+ *        bf16 table), which goes through the buffer.
+ * Other arguments and errors as lora_shrink / lora_expand.
+ */
+int lora_apply(const lora_layer_desc *desc, const lora_meta *meta, const void *x, int64_t ldx, float *buf,
+               void *y, int64_t ldy, int32_t y_dtype, int32_t kind, lora_stream_t stream);
+
 /* Scratch bytes lora_shrink needs for this layer and token bound (0: none). */
 size_t lora_workspace_bytes(const lora_layer_desc *desc, int32_t max_tokens, int32_t kind);
 

@@ -25,9 +25,9 @@ __all__ = [
     "LORA_EBADSLOT", "LORA_F32", "LORA_BF16", "LORA_AUTO", "LORA_BGMV", "LORA_SGMV",
     "LORA_MAX_SLICES", "LORA_MAX_NUM_SLOTS", "LORA_MAX_RANK", "LORA_SGMV_MIN_ROWS", "LORA_SGMV_TILE_M",
     "LayerDesc", "Meta", "LoraError", "lib_path", "exported_symbols",
-    "lora_set_slot", "lora_reset_slot", "lora_prepare_meta", "lora_shrink", "lora_expand",
+    "lora_set_slot", "lora_reset_slot", "lora_prepare_meta", "lora_shrink", "lora_expand", "lora_apply",
     "lora_workspace_bytes", "lora_meta_tiles_bytes", "lora_query_status", "lora_strerror",
-    "lora_last_cuda_error", "SlotTable", "TokenMeta", "shrink", "expand", "check",
+    "lora_last_cuda_error", "SlotTable", "TokenMeta", "shrink", "expand", "apply", "check",
 ]
 
 LORA_OK, LORA_EINVAL, LORA_ERANGE, LORA_EALIGN, LORA_EUNSUPPORTED, LORA_ECUDA, LORA_EBADSLOT = range(7)
@@ -85,6 +85,7 @@ _sig = {
     "lora_prepare_meta": (_i32, [_P(Meta), _vp]),
     "lora_shrink": (_i32, [_P(LayerDesc), _P(Meta), _vp, ctypes.c_int64, _vp, _i32, _vp, ctypes.c_size_t, _vp]),
     "lora_expand": (_i32, [_P(LayerDesc), _P(Meta), _vp, _vp, ctypes.c_int64, _i32, _i32, _vp]),
+    "lora_apply": (_i32, [_P(LayerDesc), _P(Meta), _vp, ctypes.c_int64, _vp, _vp, ctypes.c_int64, _i32, _i32, _vp]),
     "lora_workspace_bytes": (ctypes.c_size_t, [_P(LayerDesc), _i32, _i32]),
     "lora_meta_tiles_bytes": (ctypes.c_size_t, [_i32]),
     "lora_query_status": (_i32, [_P(Meta), _P(_i32), _vp]),
@@ -153,6 +154,12 @@ def lora_shrink(desc: LayerDesc, meta: Meta, x: int, ldx: int, buf: int, kind: i
 def lora_expand(desc: LayerDesc, meta: Meta, buf: int, y: int, ldy: int, y_dtype: int,
                 kind: int = LORA_AUTO, stream=None) -> int:
     return _lib.lora_expand(ctypes.byref(desc), ctypes.byref(meta), buf, y, ldy, y_dtype, kind, _stream(stream))
+
+
+def lora_apply(desc: LayerDesc, meta: Meta, x: int, ldx: int, buf: int, y: int, ldy: int, y_dtype: int,
+               kind: int = LORA_AUTO, stream=None) -> int:
+    return _lib.lora_apply(ctypes.byref(desc), ctypes.byref(meta), x, ldx, buf or None, y, ldy, y_dtype, kind,
+                           _stream(stream))
 
 
 def lora_workspace_bytes(desc: LayerDesc, max_tokens: int, kind: int = LORA_AUTO) -> int:
@@ -295,3 +302,11 @@ def expand(table: SlotTable, meta: TokenMeta, buf, y, kind: int = LORA_AUTO, str
     ydt = LORA_BF16 if y.dtype == torch.bfloat16 else LORA_F32
     check(lora_expand(table.desc, meta.c, buf.data_ptr(), y.data_ptr(), y.stride(0), ydt, kind, stream),
           "lora_expand")
+
+
+def apply(table: SlotTable, meta: TokenMeta, x, y, buf=None, kind: int = LORA_AUTO, stream=None) -> None:
+    """Fused shrink + expand: y[t, off_s:] += (scale * x[t] @ A_s) @ B_s (see lora_apply)."""
+    import torch
+    ydt = LORA_BF16 if y.dtype == torch.bfloat16 else LORA_F32
+    check(lora_apply(table.desc, meta.c, x.data_ptr(), x.stride(0), buf.data_ptr() if buf is not None else 0,
+                     y.data_ptr(), y.stride(0), ydt, kind, stream), "lora_apply")

@@ -3,267 +3,524 @@
 // each token gathers its own adapter and does a small matrix-vector product).
 //
 // Decode is bound by reading each active adapter's A and B once from HBM
-// (page "vLLM 源码完全拆解(十八): 多 LoRA 服务", section "成本与边界": the extra
-// access per layer is about 2 r (d_in + d_out) elements). So the kernels are
-// organised around the weights, not the tokens: work units are (segment,
-// slice, chunk of the weight matrix), every unit streams its chunk once with
-// 16-byte loads, and applies it to all tokens of its segment.
+// (page "vLLM 源码完全拆解(十八): 多 LoRA 服务", section "成本与边界": about
+// 2 r (d_in + d_out) extra elements per layer), so the kernels are organised
+// around the weights. A work unit is one (segment, slice). Its weights stream
+// once through shared memory with 16-byte cp.async copies issued at CTA
+// start; every thread widens a 16-byte weight vector to fp32 once and applies
+// it to all tokens of a 4-token tile held in registers.
 //
-// Shrink: a cluster of CS CTAs splits d_in into CS chunks; each CTA reduces
-// its chunk with warp shuffles, and CTA 0 sums the CS partials over
-// distributed shared memory in a fixed order (deterministic split-K without
-// global scratch, atomics or spin waits).
-// Expand: one CTA per (segment, slice, 1024-column chunk) reads its B chunk
-// once and adds buf . B into the token rows of y.
+// * shrink: a cluster of CS CTAs splits d_in into CS chunks. Inside a CTA the
+//   row-group partials are combined with a recursive-halving shuffle
+//   reduce-scatter and a fixed-order sum over warps; the CS CTA partials meet
+//   in distributed shared memory, summed in cluster-rank order
+//   (deterministic split-K without global scratch, atomics or spin waits).
+// * apply (fused): after that reduction every CTA holds the full rank-r rows
+//   u = s * x A of the tile and adds u B into its share of the slice's output
+//   columns; its first B pass was prefetched at CTA start, behind the A
+//   stream. Results are bitwise those of shrink followed by expand.
+// * expand: one CTA per (segment, slice, column chunk).
 #include "common.cuh"
 
 namespace ra {
 namespace {
 
-constexpr int kTT = 8;              // tokens per tile
-constexpr int kShrinkThreads = 256;
-constexpr int kShrinkWarps = kShrinkThreads / 32;
-constexpr int kExpandThreads = 128;
-constexpr int kExpandCols = kExpandThreads * 8;
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kTT = 4;                 // tokens per tile
+constexpr int kAChunkBytes = 65536;    // A bytes a CTA stages at once (else a 2-stage stream)
+constexpr int kAStageBytes = 32768;    // stage size of that stream
+constexpr int kBPassBytes = 32768;     // B bytes staged per pass
 
-struct ShrinkArgs {
+struct Geo {
+  int d_in, r_max, kc;   // kc: d_in rows per cluster CTA
+  int sc_rows, nstage;   // A rows per stage; 1 = whole chunk resident
+  int pw;                // B columns per pass
+  int off_a, off_x, off_red, off_cpart, off_u, off_rows, off_b, smem;
+};
+
+struct BgmvArgs {
   const void *x;
   int64_t ldx;
   const void *A[LORA_MAX_SLICES];
-  float *buf;
+  const void *B[LORA_MAX_SLICES];
+  float *buf;  // may be null for the fused kernel
+  void *y;
+  int64_t ldy;
+  int out_sizes[LORA_MAX_SLICES];
+  int out_off[LORA_MAX_SLICES];
   MetaView mv;
-  int list_off, list_cnt;   // segment list inside the work lists, and its count index
-  int d_in, r_max, kc;      // kc: d_in rows per cluster CTA
+  int list_off, list_cnt;
   const int32_t *slot_rank;
   const float *slot_scale;
+  Geo g;
 };
 
-// NV = 16-byte vectors per A row (r_max / elements per vector).
-template <typename TW, int NV>
-__global__ void __launch_bounds__(kShrinkThreads) bgmv_shrink_kernel(ShrinkArgs a) {
-  constexpr int VEC = Elem<TW>::kVec;
-  constexpr int NRG = kShrinkThreads / NV;  // row groups
-  extern __shared__ __align__(16) unsigned char smem[];
-  const int cs = (int)cluster_nctarank(), crank = (int)cluster_ctarank();
-  const int item = blockIdx.x / cs;
-  const int slice = blockIdx.y;
+struct Unit {
+  int slot, cnt, start, r_a;
+  float scale;
+};
+
+__device__ __forceinline__ bool load_unit(const BgmvArgs &a, int item, Unit &u) {
   const int32_t *W = a.mv.work;
-  if (item >= W[a.list_cnt]) return;  // the whole cluster leaves together
+  if (item >= W[a.list_cnt]) return false;
   const int seg = W[a.list_off + item];
-  const int slot = a.mv.seg_slot[seg];
-  const int cnt = a.mv.seg_count[seg];
-  const int start = a.mv.seg_start[seg];
-  const int r_max = a.r_max;
-  const int r_a = min(max(a.slot_rank[slot], 0), r_max);
-  const float scale = a.slot_scale[slot];
-  const int j0 = crank * a.kc;
-  const int len = max(0, min(a.d_in, j0 + a.kc) - j0);
-  const TW *Ab = static_cast<const TW *>(a.A[slice]) + ((int64_t)slot * a.d_in + j0) * r_max;
-  float *bufs = a.buf + (int64_t)slice * a.mv.num_tokens * r_max;
+  u.slot = a.mv.seg_slot[seg];
+  u.cnt = a.mv.seg_count[seg];
+  u.start = a.mv.seg_start[seg];
+  u.r_a = min(max(a.slot_rank[u.slot], 0), a.g.r_max);
+  u.scale = a.slot_scale[u.slot];
+  return true;
+}
 
-  TW *xs = reinterpret_cast<TW *>(smem);                                    // [kTT][kc]
-  float *wpart = reinterpret_cast<float *>(smem + (size_t)kTT * a.kc * sizeof(TW));  // [warps][kTT][r_max]
-  float *cpart = wpart + kShrinkWarps * kTT * r_max;                        // [kTT][r_max]
-
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int v = tid % NV, rg = tid / NV;
-  const bool vactive = v * VEC < r_a;
-  const int xv_row = len / VEC;
-
-  for (int tok0 = 0; tok0 < cnt; tok0 += kTT) {
-    const int nt = min(kTT, cnt - tok0);
-    for (int i = tid; i < nt * xv_row; i += kShrinkThreads) {
-      const int t = i / xv_row, c = i % xv_row;
-      const int row = a.mv.sorted_rows[start + tok0 + t];
-      const uint4 val = __ldg(reinterpret_cast<const uint4 *>(
-          static_cast<const TW *>(a.x) + (int64_t)row * a.ldx + j0) + c);
-      reinterpret_cast<uint4 *>(xs + t * a.kc)[c] = val;
+// 16 bytes of weights widened to fp32.
+template <typename TW>
+__device__ __forceinline__ void widen16(const uint4 &q, float *f) {
+  if constexpr (sizeof(TW) == 2) {
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      f[2 * i] = __uint_as_float(w[i] << 16);
+      f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
     }
-    __syncthreads();
+  } else {
+    f[0] = __uint_as_float(q.x); f[1] = __uint_as_float(q.y);
+    f[2] = __uint_as_float(q.z); f[3] = __uint_as_float(q.w);
+  }
+}
 
-    float acc[kTT][VEC];
+// 4 consecutive elements of a row, widened (8 bytes of bf16 or 16 of fp32).
+template <typename T>
+__device__ __forceinline__ void load4(const T *p, float *f) {
+  if constexpr (sizeof(T) == 2) {
+    const uint2 q = *reinterpret_cast<const uint2 *>(p);
+    f[0] = __uint_as_float(q.x << 16); f[1] = __uint_as_float(q.x & 0xffff0000u);
+    f[2] = __uint_as_float(q.y << 16); f[3] = __uint_as_float(q.y & 0xffff0000u);
+  } else {
+    const float4 q = *reinterpret_cast<const float4 *>(p);
+    f[0] = q.x; f[1] = q.y; f[2] = q.z; f[3] = q.w;
+  }
+}
+template <typename T>
+__device__ __forceinline__ void store4(T *p, const float *f) {
+  if constexpr (sizeof(T) == 2) {
+    uint2 q;
+    __nv_bfloat162 lo = __floats2bfloat162_rn(f[0], f[1]), hi = __floats2bfloat162_rn(f[2], f[3]);
+    q.x = *reinterpret_cast<uint32_t *>(&lo);
+    q.y = *reinterpret_cast<uint32_t *>(&hi);
+    *reinterpret_cast<uint2 *>(p) = q;
+  } else {
+    *reinterpret_cast<float4 *>(p) = make_float4(f[0], f[1], f[2], f[3]);
+  }
+}
+
+// Sum N values per lane over the lanes that share bits [0, log2(NV)) of the
+// lane id (recursive halving). Afterwards lane keeps N / (32 / NV) sums in
+// vals[0..) whose positions in the original array start at the returned offset.
+template <int N, int NV>
+__device__ __forceinline__ int reduce_scatter(float (&vals)[N]) {
+  const int lane = threadIdx.x & 31;
+  int off = 0;
+#pragma unroll
+  for (int lvl = 0, o = NV; o < 32; ++lvl, o <<= 1) {
+    const int cnt = N >> lvl;
+    const int half = cnt >> 1;
+    if (half == 0) break;
+    const bool up = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < N / 2; ++i) {
+      if (i < half) {
+        const float send = up ? vals[i] : vals[i + half];
+        const float keep = up ? vals[i + half] : vals[i];
+        vals[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+      }
+    }
+    if (up) off += half;
+  }
+  return off;
+}
+
+// Add u . B into y for tokens [0, nt) over columns [pc0, pc0 + pcn) of a
+// slice. Bs: B rows 0..r_a-1 of those columns (row stride pw); uT: u
+// transposed, [r_max][kTT]. One thread per 4 columns, all tokens of the tile.
+template <typename TW, typename TY>
+__device__ __forceinline__ void expand_pass(const TW *Bs, int pw, const float *uT, int r_a, const int *rows,
+                                            int nt, TY *y, int64_t ldy, int col_base, int pcn) {
+  for (int cq = threadIdx.x * 4; cq < pcn; cq += kThreads * 4) {
+    float acc[kTT][4];
 #pragma unroll
     for (int t = 0; t < kTT; ++t)
 #pragma unroll
-      for (int e = 0; e < VEC; ++e) acc[t][e] = 0.f;
-    if (vactive) {
-      constexpr int U = 4;
-      for (int jb = rg; jb < len; jb += U * NRG) {
-        uint4 av[U];
+      for (int e = 0; e < 4; ++e) acc[t][e] = 0.f;
+    const TW *bp = Bs + cq;
+#pragma unroll 4
+    for (int k = 0; k < r_a; ++k) {
+      float b[4];
+      load4(bp + k * pw, b);
+      const float4 u4 = *reinterpret_cast<const float4 *>(uT + k * kTT);
+      const float uu[kTT] = {u4.x, u4.y, u4.z, u4.w};
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-          const int j = jb + u * NRG;
-          if (j < len) av[u] = __ldg(reinterpret_cast<const uint4 *>(Ab + (int64_t)j * r_max) + v);
-        }
+      for (int t = 0; t < kTT; ++t)
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-          const int j = jb + u * NRG;
-          if (j < len) {
-            const TW *ap = reinterpret_cast<const TW *>(&av[u]);
-            float af[VEC];
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) af[e] = Elem<TW>::to_f(ap[e]);
-#pragma unroll
-            for (int t = 0; t < kTT; ++t) {
-              if (t < nt) {
-                const float xv = Elem<TW>::to_f(xs[t * a.kc + j]);
-#pragma unroll
-                for (int e = 0; e < VEC; ++e) acc[t][e] = fmaf(xv, af[e], acc[t][e]);
-              }
-            }
-          }
-        }
-      }
+        for (int e = 0; e < 4; ++e) acc[t][e] = fmaf(uu[t], b[e], acc[t][e]);
     }
-    // Reduce over the lanes that share this thread's vector column.
 #pragma unroll
     for (int t = 0; t < kTT; ++t) {
       if (t < nt) {
+        TY *yp = y + (int64_t)rows[t] * ldy + col_base + cq;
+        float yv[4];
+        load4(yp, yv);
 #pragma unroll
-        for (int o = NV; o < 32; o <<= 1)
-#pragma unroll
-          for (int e = 0; e < VEC; ++e) acc[t][e] += __shfl_xor_sync(0xffffffffu, acc[t][e], o);
+        for (int e = 0; e < 4; ++e) yv[e] += acc[t][e];
+        store4(yp, yv);
       }
     }
-    if (lane < NV) {
-      for (int t = 0; t < nt; ++t)
+  }
+}
+
+// B rows 0..r_a-1, columns [pc0, pc0 + pcn) of one slot -> Bs (row stride pw). A warp per row.
+template <typename TW>
+__device__ __forceinline__ void issue_b(TW *Bs, int pw, const TW *Bslot, int out_s, int r_a, int pc0, int pcn) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int upr = pcn * (int)sizeof(TW) / 16;
+  for (int k = warp; k < r_a; k += kWarps) {
+    const char *src = reinterpret_cast<const char *>(Bslot + (int64_t)k * out_s + pc0);
+    char *dst = reinterpret_cast<char *>(Bs + k * pw);
+    for (int c = lane; c < upr; c += 32) cp_async16(dst + c * 16, src + c * 16);
+  }
+}
+
+// Shrink (kApply = false) or fused shrink + expand (kApply = true).
+// Grid: (CS * max_items, n_slices), cluster (CS, 1, 1).
+template <typename TW, typename TY, int NV, bool kApply>
+__global__ void __launch_bounds__(kThreads, kApply ? 2 : 3) bgmv_kernel(BgmvArgs a) {
+  constexpr int VEC = Elem<TW>::kVec;
+  constexpr int NRG = kThreads / NV;   // row groups
+  constexpr int NVAL = kTT * VEC;      // accumulators per thread
+  constexpr int LPV = 32 / NV;         // lanes sharing one vector column (1 when NV == 32)
+  constexpr int NKEEP = NVAL / (LPV > NVAL ? NVAL : LPV);
+  extern __shared__ __align__(16) unsigned char smem[];
+  const Geo &g = a.g;
+  const int cs = (int)cluster_nctarank(), crank = (int)cluster_ctarank();
+  const int item = blockIdx.x / cs, slice = blockIdx.y;
+  Unit u;
+  if (!load_unit(a, item, u)) return;  // uniform over the cluster
+  const int r_max = g.r_max;
+  const int j0 = crank * g.kc;
+  const int len = max(0, min(g.d_in - j0, g.kc));
+  const int nsc = (len + g.sc_rows - 1) / g.sc_rows;
+  const int nva = (u.r_a + VEC - 1) / VEC;
+  const TW *Ab = static_cast<const TW *>(a.A[slice]) + ((int64_t)u.slot * g.d_in + j0) * r_max;
+  const TW *x = static_cast<const TW *>(a.x);
+  TW *As = reinterpret_cast<TW *>(smem + g.off_a);
+  float *xT = reinterpret_cast<float *>(smem + g.off_x);       // [kc][kTT]
+  float *wred = reinterpret_cast<float *>(smem + g.off_red);   // [kWarps][kTT][r_max]
+  float *cpart = reinterpret_cast<float *>(smem + g.off_cpart);// [kTT][r_max]
+  float *uT = reinterpret_cast<float *>(smem + g.off_u);       // [r_max][kTT]
+  int *rows = reinterpret_cast<int *>(smem + g.off_rows);
+  TW *Bs = reinterpret_cast<TW *>(smem + g.off_b);
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int v = tid % NV, rq = tid / NV;
+
+  const int out_s = a.out_sizes[slice];
+  const int per = ((out_s + cs - 1) / cs + 7) & ~7;
+  const int c0 = min(out_s, crank * per), c1 = min(out_s, c0 + per);
+  const int npass = (c1 - c0 + g.pw - 1) / g.pw;
+  const TW *Bslot = static_cast<const TW *>(a.B[slice]) + (int64_t)u.slot * r_max * out_s;
+
+  // A stage `sc` (rows sc*sc_rows ..) into buffer `stage`: one flat copy, rank tail skipped.
+  auto issue_a = [&](int sc, int stage) {
+    const int r0 = sc * g.sc_rows, nr = min(g.sc_rows, len - r0);
+    const uint4 *src = reinterpret_cast<const uint4 *>(Ab + (int64_t)r0 * r_max);
+    uint4 *dst = reinterpret_cast<uint4 *>(As + stage * g.sc_rows * r_max);
+    for (int i = tid; i < nr * NV; i += kThreads)
+      if ((i & (NV - 1)) < nva) cp_async16(dst + i, src + i);
+  };
+
+  int committed = 0, g_b = -1;
+  const int ntiles = (u.cnt + kTT - 1) / kTT;
+  for (int tile = 0; tile < ntiles; ++tile) {
+    const int tok0 = tile * kTT, nt = min(kTT, u.cnt - tok0);
+    if (tid < kTT) rows[tid] = tid < nt ? a.mv.sorted_rows[u.start + tok0 + tid] : 0;
+    int g_s0 = -1, g_s1 = -1;
+    if (tile == 0 || g.nstage > 1) {
+      if (nsc > 0) issue_a(0, 0);
+      cp_async_commit();
+      g_s0 = committed++;
+      if (nsc > 1) {
+        issue_a(1, 1);
+        cp_async_commit();
+        g_s1 = committed++;
+      }
+    }
+    if (kApply && tile == 0 && npass > 0) {
+      issue_b<TW>(Bs, g.pw, Bslot, out_s, u.r_a, c0, min(g.pw, c1 - c0));
+      cp_async_commit();
+      g_b = committed++;
+    }
+    __syncthreads();  // rows visible
+    // x rows of the tile, widened and transposed to [row][token] (absent tokens 0):
+    // a thread per pair of rows, so a warp stores 32 consecutive 32-byte runs.
+    for (int p = tid; p < (len >> 1); p += kThreads) {
+      float f0[kTT], f1[kTT];
 #pragma unroll
-        for (int e = 0; e < VEC; ++e) wpart[(warp * kTT + t) * r_max + v * VEC + e] = acc[t][e];
+      for (int t = 0; t < kTT; ++t) {
+        f0[t] = 0.f;
+        f1[t] = 0.f;
+        if (t < nt) {
+          const TW *xp = x + (int64_t)rows[t] * a.ldx + j0 + 2 * p;
+          if constexpr (sizeof(TW) == 2) {
+            const uint32_t w = __ldg(reinterpret_cast<const unsigned int *>(xp));
+            f0[t] = __uint_as_float(w << 16);
+            f1[t] = __uint_as_float(w & 0xffff0000u);
+          } else {
+            const float2 w = __ldg(reinterpret_cast<const float2 *>(xp));
+            f0[t] = w.x;
+            f1[t] = w.y;
+          }
+        }
+      }
+      reinterpret_cast<float4 *>(xT)[2 * p] = make_float4(f0[0], f0[1], f0[2], f0[3]);
+      reinterpret_cast<float4 *>(xT)[2 * p + 1] = make_float4(f1[0], f1[1], f1[2], f1[3]);
+    }
+
+    float acc[NVAL];
+#pragma unroll
+    for (int i = 0; i < NVAL; ++i) acc[i] = 0.f;
+    for (int sc = 0; sc < max(nsc, 1); ++sc) {
+      if (g.nstage > 1 || tile == 0) cp_async_wait_upto(committed - 1 - ((sc & 1) ? g_s1 : g_s0));
+      __syncthreads();
+      if (nsc > 0 && v < nva) {
+        const int r0 = sc * g.sc_rows, nr = min(g.sc_rows, len - r0);
+        const TW *Ast = As + (g.nstage > 1 ? (sc & 1) * g.sc_rows * r_max : 0) + v * VEC;
+        const float *xt = xT + r0 * kTT;
+#pragma unroll 2
+        for (int jj = rq; jj < nr; jj += NRG) {
+          float af[VEC];
+          widen16<TW>(*reinterpret_cast<const uint4 *>(Ast + jj * r_max), af);
+          const float4 x4 = *reinterpret_cast<const float4 *>(xt + jj * kTT);
+          const float xv[kTT] = {x4.x, x4.y, x4.z, x4.w};
+#pragma unroll
+          for (int t = 0; t < kTT; ++t)
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) acc[t * VEC + e] = fmaf(xv[t], af[e], acc[t * VEC + e]);
+        }
+      }
+      if (g.nstage > 1 && sc + 2 < nsc) {
+        __syncthreads();  // buffer sc & 1 is free again
+        issue_a(sc + 2, sc & 1);
+        cp_async_commit();
+        if (sc & 1) g_s1 = committed++; else g_s0 = committed++;
+      }
+    }
+    // Row groups inside a warp, then warps in order, then cluster CTAs in rank order.
+    const int off = reduce_scatter<NVAL, NV>(acc);
+#pragma unroll
+    for (int i = 0; i < NKEEP; ++i) {
+      const int idx = off + i, t = idx / VEC, e = idx % VEC;
+      wred[(warp * kTT + t) * r_max + v * VEC + e] = acc[i];
     }
     __syncthreads();
-    for (int i = tid; i < nt * r_max; i += kShrinkThreads) {
-      const int t = i / r_max, k = i % r_max;
+    for (int i = tid; i < kTT * r_max; i += kThreads) {
       float s = 0.f;
 #pragma unroll
-      for (int w = 0; w < kShrinkWarps; ++w) s += wpart[(w * kTT + t) * r_max + k];
-      cpart[t * r_max + k] = s;
+      for (int w = 0; w < kWarps; ++w) s += wred[w * kTT * r_max + i];
+      cpart[i] = s;
     }
     cluster_sync();
-    if (crank == 0) {
-      const int r4 = r_max / 4;
-      for (int i = tid; i < nt * r4; i += kShrinkThreads) {
-        const int t = i / r4, k = (i % r4) * 4;
-        const uint32_t la = smem_addr(cpart + t * r_max + k);
+    if (kApply || crank == 0) {
+      const int r4 = r_max >> 2;
+      for (int i = tid; i < nt * r4; i += kThreads) {
+        const int tt = i / r4, k = (i - tt * r4) * 4;
+        const uint32_t la = smem_addr(cpart + tt * r_max + k);
         float4 s = ld_dsmem_f4(la, 0);
         for (int c = 1; c < cs; ++c) {
           const float4 p = ld_dsmem_f4(la, (uint32_t)c);
           s.x += p.x; s.y += p.y; s.z += p.z; s.w += p.w;
         }
-        float4 o;
-        o.x = (k + 0 < r_a) ? scale * s.x : 0.f;
-        o.y = (k + 1 < r_a) ? scale * s.y : 0.f;
-        o.z = (k + 2 < r_a) ? scale * s.z : 0.f;
-        o.w = (k + 3 < r_a) ? scale * s.w : 0.f;
-        const int row = a.mv.sorted_rows[start + tok0 + t];
-        *reinterpret_cast<float4 *>(bufs + (int64_t)row * r_max + k) = o;
+        const float o[4] = {(k + 0 < u.r_a) ? u.scale * s.x : 0.f, (k + 1 < u.r_a) ? u.scale * s.y : 0.f,
+                            (k + 2 < u.r_a) ? u.scale * s.z : 0.f, (k + 3 < u.r_a) ? u.scale * s.w : 0.f};
+        if (kApply) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) uT[(k + e) * kTT + tt] = o[e];
+        }
+        if (crank == 0 && a.buf != nullptr)
+          *reinterpret_cast<float4 *>(a.buf + ((int64_t)slice * a.mv.num_tokens + rows[tt]) * r_max + k) =
+              make_float4(o[0], o[1], o[2], o[3]);
+      }
+      if (kApply) {  // absent tokens of the tile contribute nothing
+        for (int i = tid; i < (kTT - nt) * r_max; i += kThreads) {
+          const int tt = nt + i / r_max, k = i % r_max;
+          uT[k * kTT + tt] = 0.f;
+        }
       }
     }
-    cluster_sync();  // partials stay alive until CTA 0 has read them; buffers are reused next tile
+    cluster_sync();  // partials read; other CTAs may reuse their buffers or exit
+
+    if constexpr (kApply) {
+      TY *y = static_cast<TY *>(a.y);
+      for (int pass = 0; pass < npass; ++pass) {
+        const int pc0 = c0 + pass * g.pw, pcn = min(g.pw, c1 - pc0);
+        const bool resident = (pass == 0 && tile == 0) || (npass == 1 && tile > 0);
+        if (!resident) {
+          __syncthreads();
+          issue_b<TW>(Bs, g.pw, Bslot, out_s, u.r_a, pc0, pcn);
+          cp_async_commit();
+          g_b = committed++;
+        }
+        cp_async_wait_upto(committed - 1 - g_b);
+        __syncthreads();
+        expand_pass<TW, TY>(Bs, g.pw, uT, u.r_a, rows, nt, y, a.ldy, a.out_off[slice] + pc0, pcn);
+      }
+    }
+    __syncthreads();  // rows / xT / uT are rewritten by the next tile
   }
+  cp_async_wait_upto(0);
 }
 
+// Standalone expand. Grid: (column chunks over all slices, max_items).
 struct ExpandArgs {
-  const float *buf;
-  void *y;
-  int64_t ldy;
-  const void *B[LORA_MAX_SLICES];
-  MetaView mv;
-  int list_off, list_cnt;
-  int r_max;
-  int out_sizes[LORA_MAX_SLICES];
-  int out_off[LORA_MAX_SLICES];
+  BgmvArgs b;
   int chunk_start[LORA_MAX_SLICES + 1];
   int n_slices;
-  const int32_t *slot_rank;
 };
 
 template <typename TW, typename TY>
-__global__ void __launch_bounds__(kExpandThreads) bgmv_expand_kernel(ExpandArgs a) {
+__global__ void __launch_bounds__(kThreads) bgmv_expand_kernel(ExpandArgs ea) {
+  const BgmvArgs &a = ea.b;
+  const Geo &g = a.g;
   extern __shared__ __align__(16) unsigned char smem[];
-  const int32_t *W = a.mv.work;
-  const int item = blockIdx.y;
-  if (item >= W[a.list_cnt]) return;
+  Unit u;
+  if (!load_unit(a, blockIdx.y, u)) return;
   int s = 0;
-  while (s + 1 < a.n_slices && (int)blockIdx.x >= a.chunk_start[s + 1]) ++s;
+  while (s + 1 < ea.n_slices && (int)blockIdx.x >= ea.chunk_start[s + 1]) ++s;
   const int out_s = a.out_sizes[s];
-  const int n0 = ((int)blockIdx.x - a.chunk_start[s]) * kExpandCols + threadIdx.x * 8;
-  const bool active = n0 < out_s;
-  const int seg = W[a.list_off + item];
-  const int slot = a.mv.seg_slot[seg];
-  const int cnt = a.mv.seg_count[seg];
-  const int start = a.mv.seg_start[seg];
-  const int r_max = a.r_max;
-  const int r_a = min(max(a.slot_rank[slot], 0), r_max);
-  const TW *Bb = static_cast<const TW *>(a.B[s]) + (int64_t)slot * r_max * out_s + n0;
+  const int pc0 = ((int)blockIdx.x - ea.chunk_start[s]) * g.pw;
+  const int pcn = min(g.pw, out_s - pc0);
+  const int r_max = g.r_max;
+  TW *Bs = reinterpret_cast<TW *>(smem + g.off_b);
+  float *uT = reinterpret_cast<float *>(smem + g.off_u);
+  int *rows = reinterpret_cast<int *>(smem + g.off_rows);
+  const TW *Bslot = static_cast<const TW *>(a.B[s]) + (int64_t)u.slot * r_max * out_s;
   const float *bufs = a.buf + (int64_t)s * a.mv.num_tokens * r_max;
-  TY *y = static_cast<TY *>(a.y);
-
-  float *us = reinterpret_cast<float *>(smem);   // [kTT][r_max]
-  __shared__ int rows[kTT];
-
-  for (int tok0 = 0; tok0 < cnt; tok0 += kTT) {
-    const int nt = min(kTT, cnt - tok0);
-    if (threadIdx.x < nt) rows[threadIdx.x] = a.mv.sorted_rows[start + tok0 + threadIdx.x];
+  issue_b<TW>(Bs, g.pw, Bslot, out_s, u.r_a, pc0, pcn);
+  cp_async_commit();
+  const int ntiles = (u.cnt + kTT - 1) / kTT;
+  for (int tile = 0; tile < ntiles; ++tile) {
+    const int tok0 = tile * kTT, nt = min(kTT, u.cnt - tok0);
+    if (threadIdx.x < kTT) rows[threadIdx.x] = threadIdx.x < nt ? a.mv.sorted_rows[u.start + tok0 + threadIdx.x] : 0;
     __syncthreads();
-    for (int i = threadIdx.x; i < nt * r_max; i += kExpandThreads) {
-      const int t = i / r_max, k = i % r_max;
-      us[i] = (k < r_a) ? bufs[(int64_t)rows[t] * r_max + k] : 0.f;
+    for (int i = threadIdx.x; i < kTT * r_max; i += kThreads) {
+      const int tt = i / r_max, k = i - tt * r_max;
+      uT[k * kTT + tt] = (tt < nt && k < u.r_a) ? bufs[(int64_t)rows[tt] * r_max + k] : 0.f;
     }
+    cp_async_wait_upto(0);
     __syncthreads();
-    if (active) {
-      float acc[kTT][8];
-#pragma unroll
-      for (int t = 0; t < kTT; ++t)
-#pragma unroll
-        for (int e = 0; e < 8; ++e) acc[t][e] = 0.f;
-      constexpr int U = 4;
-      for (int kb = 0; kb < r_a; kb += U) {
-        float bv[U][8];
-#pragma unroll
-        for (int u = 0; u < U; ++u)
-          if (kb + u < r_a) load8_f32(Bb + (int64_t)(kb + u) * out_s, bv[u]);
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-          if (kb + u < r_a) {
-#pragma unroll
-            for (int t = 0; t < kTT; ++t) {
-              if (t < nt) {
-                const float uk = us[t * r_max + kb + u];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) acc[t][e] = fmaf(uk, bv[u][e], acc[t][e]);
-              }
-            }
-          }
-        }
-      }
-#pragma unroll
-      for (int t = 0; t < kTT; ++t) {
-        if (t < nt) {
-          TY *yp = y + (int64_t)rows[t] * a.ldy + a.out_off[s] + n0;
-          float yv[8];
-          load8_rw(yp, yv);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) yv[e] += acc[t][e];
-          store8(yp, yv);
-        }
-      }
-    }
+    expand_pass<TW, TY>(Bs, g.pw, uT, u.r_a, rows, nt, static_cast<TY *>(a.y), a.ldy, a.out_off[s] + pc0, pcn);
     __syncthreads();
   }
 }
 
-int list_off_of(ListSel sel, int S) {
-  return sel == kListSmall ? WorkLists::small_seg(S)
-       : sel == kListLarge ? WorkLists::large_seg(S) : WorkLists::all_seg(S);
-}
-int list_cnt_of(ListSel sel) { return sel == kListSmall ? 1 : sel == kListLarge ? 2 : 0; }
+int align16(int v) { return (v + 15) & ~15; }
 
-template <typename TW, int NV>
-cudaError_t shrink_nv(const ShrinkArgs &a, dim3 grid, size_t smem, int cs, cudaStream_t st) {
-  auto k = bgmv_shrink_kernel<TW, NV>;
-  cudaError_t e = set_max_dynamic_smem((const void *)k, 200 * 1024);
+int cluster_size(int d_in) {
+  int cs = d_in / 1024;
+  return cs < 1 ? 1 : (cs > 8 ? 8 : cs);
+}
+
+// Shared-memory geometry. mode: 0 shrink, 1 expand, 2 fused apply.
+Geo make_geo(const lora_layer_desc &d, int cs, int mode) {
+  Geo g{};
+  const int es = d.dtype == LORA_BF16 ? 2 : 4;
+  const int vec = 16 / es;
+  g.d_in = d.d_in;
+  g.r_max = d.r_max;
+  g.kc = (((d.d_in + cs - 1) / cs) + 7) & ~7;
+  const int row_bytes = d.r_max * es;
+  if (g.kc * row_bytes <= kAChunkBytes) {
+    g.sc_rows = g.kc;
+    g.nstage = 1;
+  } else {
+    g.sc_rows = (kAStageBytes / row_bytes) & ~7;
+    if (g.sc_rows < 8) g.sc_rows = 8;
+    g.nstage = 2;
+  }
+  int pw = (kBPassBytes / row_bytes) & ~7;
+  if (pw < 8) pw = 8;
+  int max_cols = 0;
+  for (int s = 0; s < d.n_slices; ++s) {
+    const int per = mode == 2 ? ((((d.out_sizes[s] + cs - 1) / cs) + 7) & ~7) : d.out_sizes[s];
+    max_cols = per > max_cols ? per : max_cols;
+  }
+  if (pw > max_cols) pw = max_cols;
+  g.pw = pw;
+  int off = 0;
+  g.off_a = off;
+  if (mode != 1) off += align16(g.nstage * g.sc_rows * row_bytes);
+  g.off_x = off;
+  if (mode != 1) off += align16(g.kc * kTT * 4);
+  g.off_red = off;
+  if (mode != 1) off += align16(kWarps * kTT * d.r_max * 4);
+  g.off_cpart = off;
+  if (mode != 1) off += align16(kTT * d.r_max * 4);
+  g.off_u = off;
+  off += align16(kTT * d.r_max * 4);
+  g.off_rows = off;
+  off += align16(kTT * 4);
+  g.off_b = off;
+  if (mode != 0) off += align16(d.r_max * pw * es);
+  g.smem = off;
+  (void)vec;
+  return g;
+}
+
+void fill_common(BgmvArgs &a, const lora_layer_desc &d, const MetaView &mv, ListSel sel) {
+  const int S = mv.num_slots;
+  a.list_off = sel == kListSmall ? WorkLists::small_seg(S) : sel == kListLarge ? WorkLists::large_seg(S)
+                                                                               : WorkLists::all_seg(S);
+  a.list_cnt = sel == kListSmall ? 1 : sel == kListLarge ? 2 : 0;
+  a.mv = mv;
+  int off = 0;
+  for (int s = 0; s < d.n_slices; ++s) {
+    a.A[s] = d.A[s];
+    a.B[s] = d.B[s];
+    a.out_sizes[s] = d.out_sizes[s];
+    a.out_off[s] = off;
+    off += d.out_sizes[s];
+  }
+  a.slot_rank = d.slot_rank;
+  a.slot_scale = d.slot_scale;
+}
+
+template <typename TW, typename TY, bool kApply, int NV>
+cudaError_t launch_nv(const BgmvArgs &a, dim3 grid, int cs, cudaStream_t st) {
+  auto k = bgmv_kernel<TW, TY, NV, kApply>;
+  cudaError_t e = set_max_dynamic_smem((const void *)k, 227 * 1024);
   if (e != cudaSuccess) return e;
-  return launch_cluster(k, grid, dim3(kShrinkThreads), smem, st, (unsigned)cs, a);
+  return launch_cluster(k, grid, dim3(kThreads), (size_t)a.g.smem, st, (unsigned)cs, a);
+}
+
+template <typename TW, typename TY, bool kApply>
+cudaError_t dispatch_nv(BgmvArgs &a, dim3 grid, int cs, int r_max, cudaStream_t st) {
+  const int nv = r_max / Elem<TW>::kVec;
+  if constexpr (sizeof(TW) == 2) {
+    switch (nv) {
+      case 1: return launch_nv<TW, TY, kApply, 1>(a, grid, cs, st);
+      case 2: return launch_nv<TW, TY, kApply, 2>(a, grid, cs, st);
+      case 4: return launch_nv<TW, TY, kApply, 4>(a, grid, cs, st);
+      case 8: return launch_nv<TW, TY, kApply, 8>(a, grid, cs, st);
+      case 16: return launch_nv<TW, TY, kApply, 16>(a, grid, cs, st);
+    }
+  } else {
+    switch (nv) {
+      case 2: return launch_nv<TW, TY, kApply, 2>(a, grid, cs, st);
+      case 4: return launch_nv<TW, TY, kApply, 4>(a, grid, cs, st);
+      case 8: return launch_nv<TW, TY, kApply, 8>(a, grid, cs, st);
+      case 16: return launch_nv<TW, TY, kApply, 16>(a, grid, cs, st);
+      case 32: return launch_nv<TW, TY, kApply, 32>(a, grid, cs, st);
+    }
+  }
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace
@@ -272,78 +529,66 @@ cudaError_t launch_bgmv_shrink(const lora_layer_desc &d, const MetaView &mv, Lis
                                const void *x, int64_t ldx, float *buf, cudaStream_t st) {
   const int max_items = std::min(mv.num_slots - 1, mv.num_tokens);
   if (max_items <= 0) return cudaSuccess;
-  ShrinkArgs a{};
+  BgmvArgs a{};
+  fill_common(a, d, mv, sel);
   a.x = x;
   a.ldx = ldx;
-  for (int s = 0; s < d.n_slices; ++s) a.A[s] = d.A[s];
   a.buf = buf;
-  a.mv = mv;
-  a.list_off = list_off_of(sel, mv.num_slots);
-  a.list_cnt = list_cnt_of(sel);
-  a.d_in = d.d_in;
-  a.r_max = d.r_max;
-  int cs = d.d_in / 512;
-  cs = cs < 1 ? 1 : (cs > 8 ? 8 : cs);
-  a.kc = ((d.d_in + cs - 1) / cs + 7) / 8 * 8;
-  a.slot_rank = d.slot_rank;
-  a.slot_scale = d.slot_scale;
-  const size_t es = d.dtype == LORA_BF16 ? 2 : 4;
-  const size_t smem = (size_t)kTT * a.kc * es + (size_t)(kShrinkWarps + 1) * kTT * d.r_max * sizeof(float);
+  const int cs = cluster_size(d.d_in);
+  a.g = make_geo(d, cs, 0);
+  dim3 grid((unsigned)(cs * max_items), (unsigned)d.n_slices);
+  if (d.dtype == LORA_BF16) return dispatch_nv<__nv_bfloat16, float, false>(a, grid, cs, d.r_max, st);
+  return dispatch_nv<float, float, false>(a, grid, cs, d.r_max, st);
+}
+
+cudaError_t launch_bgmv_apply(const lora_layer_desc &d, const MetaView &mv, ListSel sel, const void *x,
+                              int64_t ldx, float *buf, void *y, int64_t ldy, int y_dtype, cudaStream_t st) {
+  const int max_items = std::min(mv.num_slots - 1, mv.num_tokens);
+  if (max_items <= 0) return cudaSuccess;
+  BgmvArgs a{};
+  fill_common(a, d, mv, sel);
+  a.x = x;
+  a.ldx = ldx;
+  a.buf = buf;
+  a.y = y;
+  a.ldy = ldy;
+  const int cs = cluster_size(d.d_in);
+  a.g = make_geo(d, cs, 2);
   dim3 grid((unsigned)(cs * max_items), (unsigned)d.n_slices);
   if (d.dtype == LORA_BF16) {
-    switch (d.r_max / 8) {
-      case 1: return shrink_nv<__nv_bfloat16, 1>(a, grid, smem, cs, st);
-      case 2: return shrink_nv<__nv_bfloat16, 2>(a, grid, smem, cs, st);
-      case 4: return shrink_nv<__nv_bfloat16, 4>(a, grid, smem, cs, st);
-      case 8: return shrink_nv<__nv_bfloat16, 8>(a, grid, smem, cs, st);
-      case 16: return shrink_nv<__nv_bfloat16, 16>(a, grid, smem, cs, st);
-    }
-  } else {
-    switch (d.r_max / 4) {
-      case 2: return shrink_nv<float, 2>(a, grid, smem, cs, st);
-      case 4: return shrink_nv<float, 4>(a, grid, smem, cs, st);
-      case 8: return shrink_nv<float, 8>(a, grid, smem, cs, st);
-      case 16: return shrink_nv<float, 16>(a, grid, smem, cs, st);
-      case 32: return shrink_nv<float, 32>(a, grid, smem, cs, st);
-    }
+    if (y_dtype == LORA_BF16) return dispatch_nv<__nv_bfloat16, __nv_bfloat16, true>(a, grid, cs, d.r_max, st);
+    return dispatch_nv<__nv_bfloat16, float, true>(a, grid, cs, d.r_max, st);
   }
-  return cudaErrorInvalidValue;
+  return dispatch_nv<float, float, true>(a, grid, cs, d.r_max, st);
 }
 
 cudaError_t launch_bgmv_expand(const lora_layer_desc &d, const MetaView &mv, ListSel sel,
                                const float *buf, void *y, int64_t ldy, int y_dtype, cudaStream_t st) {
   const int max_items = std::min(mv.num_slots - 1, mv.num_tokens);
   if (max_items <= 0) return cudaSuccess;
-  ExpandArgs a{};
-  a.buf = buf;
+  ExpandArgs ea{};
+  BgmvArgs &a = ea.b;
+  fill_common(a, d, mv, sel);
+  a.buf = const_cast<float *>(buf);
   a.y = y;
   a.ldy = ldy;
-  a.mv = mv;
-  a.list_off = list_off_of(sel, mv.num_slots);
-  a.list_cnt = list_cnt_of(sel);
-  a.r_max = d.r_max;
-  a.n_slices = d.n_slices;
-  int off = 0, chunks = 0;
+  a.g = make_geo(d, 1, 1);
+  int chunks = 0;
   for (int s = 0; s < d.n_slices; ++s) {
-    a.B[s] = d.B[s];
-    a.out_sizes[s] = d.out_sizes[s];
-    a.out_off[s] = off;
-    a.chunk_start[s] = chunks;
-    off += d.out_sizes[s];
-    chunks += (d.out_sizes[s] + kExpandCols - 1) / kExpandCols;
+    ea.chunk_start[s] = chunks;
+    chunks += (d.out_sizes[s] + a.g.pw - 1) / a.g.pw;
   }
-  a.chunk_start[d.n_slices] = chunks;
-  a.slot_rank = d.slot_rank;
-  const size_t smem = (size_t)kTT * d.r_max * sizeof(float);
+  ea.chunk_start[d.n_slices] = chunks;
+  ea.n_slices = d.n_slices;
   dim3 grid((unsigned)chunks, (unsigned)max_items);
-  if (d.dtype == LORA_BF16) {
-    if (y_dtype == LORA_BF16)
-      bgmv_expand_kernel<__nv_bfloat16, __nv_bfloat16><<<grid, kExpandThreads, smem, st>>>(a);
-    else
-      bgmv_expand_kernel<__nv_bfloat16, float><<<grid, kExpandThreads, smem, st>>>(a);
-  } else {
-    bgmv_expand_kernel<float, float><<<grid, kExpandThreads, smem, st>>>(a);
-  }
+  const size_t smem = (size_t)a.g.smem;
+  void (*k)(ExpandArgs);
+  if (d.dtype == LORA_BF16 && y_dtype == LORA_BF16) k = bgmv_expand_kernel<__nv_bfloat16, __nv_bfloat16>;
+  else if (d.dtype == LORA_BF16) k = bgmv_expand_kernel<__nv_bfloat16, float>;
+  else k = bgmv_expand_kernel<float, float>;
+  cudaError_t e = set_max_dynamic_smem((const void *)k, 227 * 1024);
+  if (e != cudaSuccess) return e;
+  k<<<grid, kThreads, smem, st>>>(ea);
   return cudaGetLastError();
 }
 

@@ -102,6 +102,22 @@ __device__ __forceinline__ float4 ld_dsmem_f4(uint32_t local_addr, uint32_t rank
   return v;
 }
 
+// ------------------------------------------------------------------ asynchronous copies
+// 16-byte global -> shared copies (cp.async, L2-only caching). Completion is
+// waited for per commit group; no thread spins on memory.
+
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(smem)), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Wait until at most n of the most recently committed groups are still pending.
+__device__ __forceinline__ void cp_async_wait_upto(int n) {
+  if (n <= 0) asm volatile("cp.async.wait_group 0;" ::: "memory");
+  else if (n == 1) asm volatile("cp.async.wait_group 1;" ::: "memory");
+  else if (n == 2) asm volatile("cp.async.wait_group 2;" ::: "memory");
+  else asm volatile("cp.async.wait_group 3;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ work lists (meta->tiles)
 //
 // int32 layout written by the metadata kernel and read by shrink / expand:
@@ -171,6 +187,8 @@ cudaError_t launch_bgmv_shrink(const lora_layer_desc &d, const MetaView &mv, Lis
 cudaError_t launch_bgmv_expand(const lora_layer_desc &d, const MetaView &mv, ListSel sel,
                                const float *buf, void *y, int64_t ldy, int y_dtype, cudaStream_t st);
 bool sgmv_supported();
+cudaError_t launch_bgmv_apply(const lora_layer_desc &d, const MetaView &mv, ListSel sel, const void *x,
+                              int64_t ldx, float *buf, void *y, int64_t ldy, int y_dtype, cudaStream_t st);
 cudaError_t launch_sgmv_shrink(const lora_layer_desc &d, const MetaView &mv, ListSel sel,
                                const void *x, int64_t ldx, float *buf, cudaStream_t st);
 cudaError_t launch_sgmv_expand(const lora_layer_desc &d, const MetaView &mv, ListSel sel,

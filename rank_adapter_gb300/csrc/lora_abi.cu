@@ -198,6 +198,42 @@ int lora_expand(const lora_layer_desc *desc, const lora_meta *meta, const float 
   return cuda_status(ra::launch_sgmv_expand(*desc, mv, ra::kListLarge, buf, y, ldy, y_dtype, s));
 }
 
+int lora_apply(const lora_layer_desc *desc, const lora_meta *meta, const void *x, int64_t ldx, float *buf,
+               void *y, int64_t ldy, int32_t y_dtype, int32_t kind, lora_stream_t stream) {
+  int st = check_desc(desc);
+  if (st != LORA_OK) return st;
+  st = check_meta(meta);
+  if (st != LORA_OK) return st;
+  if (meta->num_slots != desc->num_slots) return LORA_EINVAL;
+  if (kind != LORA_AUTO && kind != LORA_BGMV && kind != LORA_SGMV) return LORA_EINVAL;
+  if (y_dtype != LORA_F32 && y_dtype != LORA_BF16) return LORA_EINVAL;
+  if (desc->dtype == LORA_F32 && y_dtype != LORA_F32) return LORA_EUNSUPPORTED;
+  if (kind == LORA_SGMV && !sgmv_available(desc)) return LORA_EUNSUPPORTED;
+  if (meta->num_tokens == 0) return LORA_OK;
+  const bool uses_sgmv = kind == LORA_SGMV || (kind == LORA_AUTO && sgmv_available(desc));
+  if (x == nullptr || y == nullptr || (uses_sgmv && buf == nullptr)) return LORA_EINVAL;
+  int64_t total = 0;
+  for (int s = 0; s < desc->n_slices; ++s) total += desc->out_sizes[s];
+  if (ldx < desc->d_in || ldy < total) return LORA_EINVAL;
+  if (!aligned16(x) || !aligned16(y) || (buf != nullptr && !aligned16(buf)) ||
+      (ldx * (int64_t)elem_size(desc->dtype)) % 16 != 0 || (ldy * (int64_t)elem_size(y_dtype)) % 16 != 0)
+    return LORA_EALIGN;
+  const ra::MetaView mv = view_of(meta);
+  cudaStream_t s = (cudaStream_t)stream;
+  if (!uses_sgmv)
+    return cuda_status(ra::launch_bgmv_apply(*desc, mv, ra::kListAll, x, ldx, buf, y, ldy, y_dtype, s));
+  if (kind == LORA_SGMV) {
+    st = cuda_status(ra::launch_sgmv_shrink(*desc, mv, ra::kListAll, x, ldx, buf, s));
+    if (st != LORA_OK) return st;
+    return cuda_status(ra::launch_sgmv_expand(*desc, mv, ra::kListAll, buf, y, ldy, y_dtype, s));
+  }
+  st = cuda_status(ra::launch_bgmv_apply(*desc, mv, ra::kListSmall, x, ldx, buf, y, ldy, y_dtype, s));
+  if (st != LORA_OK) return st;
+  st = cuda_status(ra::launch_sgmv_shrink(*desc, mv, ra::kListLarge, x, ldx, buf, s));
+  if (st != LORA_OK) return st;
+  return cuda_status(ra::launch_sgmv_expand(*desc, mv, ra::kListLarge, buf, y, ldy, y_dtype, s));
+}
+
 int lora_query_status(const lora_meta *meta, int32_t *out, lora_stream_t stream) {
   if (meta == nullptr || meta->status == nullptr || out == nullptr) return LORA_EINVAL;
   int32_t v = 0;

@@ -31,42 +31,53 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
   return m;
 }
 
-// Exclusive prefix sum of one value per thread over the whole CTA; all threads call it.
-__device__ int block_excl_scan(int v, int *warp_tmp, int &total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int x = v;
+__device__ __forceinline__ int warp_incl_scan(int x) {
+  const int lane = threadIdx.x & 31;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    int y = __shfl_up_sync(0xffffffffu, x, o);
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
     if (lane >= o) x += y;
   }
-  if (lane == 31) warp_tmp[warp] = x;
-  __syncthreads();
-  if (warp == 0) {
-    int w = warp_tmp[lane];
+  return x;
+}
+
+// Exclusive prefix sums of N values per thread over the whole CTA, with one
+// pair of barriers for all N. All threads call it.
+template <int N>
+__device__ void block_excl_scan_n(const int (&v)[N], int (&excl)[N], int (&total)[N], int *tmp /*[N][kWarps]*/) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl[N];
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      int y = __shfl_up_sync(0xffffffffu, w, o);
-      if (lane >= o) w += y;
-    }
-    warp_tmp[lane] = w;
+  for (int i = 0; i < N; ++i) {
+    incl[i] = warp_incl_scan(v[i]);
+    if (lane == 31) tmp[i * kWarps + warp] = incl[i];
   }
   __syncthreads();
-  const int prefix = (warp > 0 ? warp_tmp[warp - 1] : 0) + x - v;
-  total = warp_tmp[kWarps - 1];
+  if (warp == 0) {
+#pragma unroll
+    for (int i = 0; i < N; ++i) tmp[i * kWarps + lane] = warp_incl_scan(tmp[i * kWarps + lane]);
+  }
   __syncthreads();
-  return prefix;
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    excl[i] = (warp > 0 ? tmp[i * kWarps + warp - 1] : 0) + incl[i] - v[i];
+    total[i] = tmp[i * kWarps + kWarps - 1];
+  }
+  __syncthreads();
 }
 
 __global__ void __launch_bounds__(kThreads, 1) prepare_meta_kernel(MetaArgs a) {
   extern __shared__ int32_t sm[];
   const int S = a.S, T = a.T;
-  int32_t *hist = sm;  // [kWarps][S]: counts, then absolute write offsets
-  __shared__ int warp_tmp[kWarps];
+  const int hs = S + 1;             // odd row stride: a warp reading one slot's column hits 32 banks
+  int32_t *hist = sm;               // [kWarps][hs]: counts, then offsets inside each slot
+  int32_t *tot_s = sm + kWarps * hs;   // [S]
+  int32_t *base_s = tot_s + S;         // [S]
+  __shared__ int tmp[7 * kWarps];
   __shared__ int s_bad;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
-  for (int i = tid; i < kWarps * S; i += kThreads) hist[i] = 0;
+  for (int i = tid; i < kWarps * hs; i += kThreads) hist[i] = 0;
   if (tid == 0) s_bad = 0;
   __syncthreads();
 
@@ -74,8 +85,8 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_meta_kernel(MetaArgs a) {
   const int per = (T + kWarps - 1) / kWarps;
   const int t0 = min(T, warp * per), t1 = min(T, t0 + per);
   int bad = 0;
-  for (int base = t0; base < t1; base += 32) {
-    const int t = base + lane;
+  for (int b = t0; b < t1; b += 32) {
+    const int t = b + lane;
     const bool valid = t < t1;
     int s = 0;
     if (valid) {
@@ -85,7 +96,7 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_meta_kernel(MetaArgs a) {
     const uint32_t act = __ballot_sync(0xffffffffu, valid);
     if (valid) {
       const uint32_t peers = __match_any_sync(act, s);
-      if (lane == __ffs(peers) - 1) hist[warp * S + s] += __popc(peers);
+      if (lane == __ffs(peers) - 1) hist[warp * hs + s] += __popc(peers);
     }
     __syncwarp();
   }
@@ -94,32 +105,29 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_meta_kernel(MetaArgs a) {
   if (lane == 0 && bad) atomicAdd(&s_bad, bad);
   __syncthreads();
 
-  // Per slot (thread = slot): total count and exclusive offsets inside the slot.
-  int tot = 0;
-  if (tid < S) {
-    for (int w = 0; w < kWarps; ++w) {
-      const int c = hist[w * S + tid];
-      hist[w * S + tid] = tot;
-      tot += c;
-    }
+  // Per slot, across the 32 warp rows: exclusive offsets (one warp scan per slot).
+  for (int s = warp; s < S; s += kWarps) {
+    const int c = hist[lane * hs + s];
+    const int incl = warp_incl_scan(c);
+    hist[lane * hs + s] = incl - c;
+    if (lane == 31) tot_s[s] = incl;
   }
-  int total;
-  const int base = block_excl_scan(tid < S ? tot : 0, warp_tmp, total);  // first sorted row of slot
-  if (tid < S)
-    for (int w = 0; w < kWarps; ++w) hist[w * S + tid] += base;
+  __syncthreads();
 
+  // One merged scan: slot bases, segment / list indices and tile offsets.
+  const int tot = tid < S ? tot_s[tid] : 0;
   const bool present = tid < S && tot > 0;
   const bool lora = present && tid != 0;
   const bool small = lora && tot < LORA_SGMV_MIN_ROWS;
   const bool large = lora && tot >= LORA_SGMV_MIN_ROWS;
   const int tiles = lora ? (tot + LORA_SGMV_TILE_M - 1) / LORA_SGMV_TILE_M : 0;
-  int nsegs, n_all, n_small, n_large, tiles_all, tiles_large;
-  const int seg_idx = block_excl_scan(present ? 1 : 0, warp_tmp, nsegs);
-  const int all_idx = block_excl_scan(lora ? 1 : 0, warp_tmp, n_all);
-  const int small_idx = block_excl_scan(small ? 1 : 0, warp_tmp, n_small);
-  const int large_idx = block_excl_scan(large ? 1 : 0, warp_tmp, n_large);
-  const int tile_all0 = block_excl_scan(tiles, warp_tmp, tiles_all);
-  const int tile_large0 = block_excl_scan(large ? tiles : 0, warp_tmp, tiles_large);
+  const int vals[7] = {tot, present, lora, small, large, tiles, large ? tiles : 0};
+  int ex[7], tl[7];
+  block_excl_scan_n<7>(vals, ex, tl, tmp);
+  const int base = ex[0], seg_idx = ex[1], all_idx = ex[2], small_idx = ex[3], large_idx = ex[4];
+  const int nsegs = tl[1], n_all = tl[2], n_small = tl[3], n_large = tl[4];
+  const int tiles_all = tl[5], tiles_large = tl[6];
+  if (tid < S) base_s[tid] = base;
 
   int32_t *W = a.work;
   if (present) {
@@ -129,14 +137,13 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_meta_kernel(MetaArgs a) {
   }
   if (lora) {
     W[WorkLists::all_seg(S) + all_idx] = seg_idx;
-    W[WorkLists::all_tile_start(S) + all_idx] = tile_all0;
+    W[WorkLists::all_tile_start(S) + all_idx] = ex[5];
   }
   if (small) W[WorkLists::small_seg(S) + small_idx] = seg_idx;
   if (large) {
     W[WorkLists::large_seg(S) + large_idx] = seg_idx;
-    W[WorkLists::large_tile_start(S) + large_idx] = tile_large0;
+    W[WorkLists::large_tile_start(S) + large_idx] = ex[6];
   }
-  // Tails and scalars.
   for (int i = tid; i <= S; i += kThreads) {
     if (i < S && i >= nsegs) { a.seg_slot[i] = -1; a.seg_count[i] = 0; }
     if (i >= nsegs) a.seg_start[i] = T;
@@ -153,9 +160,9 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_meta_kernel(MetaArgs a) {
     W[5] = 0; W[6] = 0; W[7] = 0;
     *a.num_segs = nsegs;
     *a.status = s_bad;
+    *a.no_lora = (T - tot == 0) ? 1 : 0;   // thread 0 holds the slot-0 count
   }
-  // Thread 0 holds the slot-0 count (no-LoRA tokens and out-of-range ids).
-  if (tid == 0) *a.no_lora = (T - tot == 0) ? 1 : 0;
+  __syncthreads();
 
   // Pass 2: stable scatter of token indices.
   for (int b = t0; b < t1; b += 32) {
@@ -170,11 +177,10 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_meta_kernel(MetaArgs a) {
     uint32_t peers = 0;
     if (valid) {
       peers = __match_any_sync(act, s);
-      const int pos = hist[warp * S + s] + __popc(peers & lanemask_lt());
-      a.sorted_rows[pos] = t;
+      a.sorted_rows[base_s[s] + hist[warp * hs + s] + __popc(peers & lanemask_lt())] = t;
     }
     __syncwarp();
-    if (valid && lane == __ffs(peers) - 1) hist[warp * S + s] += __popc(peers);
+    if (valid && lane == __ffs(peers) - 1) hist[warp * hs + s] += __popc(peers);
     __syncwarp();
   }
 }
@@ -194,9 +200,10 @@ cudaError_t launch_prepare_meta(const lora_meta &m, cudaStream_t st) {
   a.no_lora = m.no_lora;
   a.status = m.status;
   a.work = static_cast<int32_t *>(m.tiles);
-  const size_t smem = (size_t)kWarps * m.num_slots * sizeof(int32_t);
+  const size_t smem = ((size_t)kWarps * (m.num_slots + 1) + 2 * (size_t)m.num_slots) * sizeof(int32_t);
   cudaError_t e = set_max_dynamic_smem((const void *)prepare_meta_kernel,
-                                       (int)((size_t)kWarps * LORA_MAX_NUM_SLOTS * sizeof(int32_t)));
+                                       (int)(((size_t)kWarps * (LORA_MAX_NUM_SLOTS + 1) + 2 * LORA_MAX_NUM_SLOTS) *
+                                             sizeof(int32_t)));
   if (e != cudaSuccess) return e;
   prepare_meta_kernel<<<1, kThreads, smem, st>>>(a);
   return cudaGetLastError();

@@ -50,8 +50,9 @@ def load_table(inst, device="cuda") -> ra.SlotTable:
 
 
 def run_gpu(inst, table=None, kind=ra.LORA_AUTO, y_dtype="f32", token_slot=None, ldx_pad=0, ldy_pad=0,
-            y_in=None):
-    """Run prepare_meta + shrink + expand; returns (buf, y, meta) on the host.
+            y_in=None, path="split"):
+    """Run prepare_meta + shrink + expand (path "split") or prepare_meta +
+    lora_apply (path "apply"); returns (buf, y, meta) on the host.
 
     buf is pre-filled with NaN so rows the shrink must not write stay NaN.
     """
@@ -74,8 +75,11 @@ def run_gpu(inst, table=None, kind=ra.LORA_AUTO, y_dtype="f32", token_slot=None,
     meta = ra.TokenMeta(max(T, 1), inst.num_slots)
     meta.prepare(torch.from_numpy(ts).cuda())
     buf = torch.full((inst.n_slices, T, inst.r_max), float("nan"), dtype=torch.float32, device="cuda")
-    ra.shrink(table, meta, x, buf, kind)
-    ra.expand(table, meta, buf, y, kind)
+    if path == "split":
+        ra.shrink(table, meta, x, buf, kind)
+        ra.expand(table, meta, buf, y, kind)
+    else:
+        ra.apply(table, meta, x, y, buf=buf, kind=kind)
     torch.cuda.synchronize()
     return buf.cpu().numpy(), y.float().cpu().numpy(), meta
 

@@ -12,8 +12,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 @pytest.fixture(scope="module")
 def ra():
-    from rank_adapter_gb300 import build_lib
-    build_lib.build()
+    import __graft_entry__
+    __graft_entry__._load_build_lib().build()
     import rank_adapter_gb300
     return rank_adapter_gb300
 
