@@ -112,7 +112,7 @@ typedef struct {
  *                                were outside [0, num_slots)
  *   tiles       work lists the kernels read (segment lists per kernel family
  *               and SGMV tile offsets); at least lora_meta_tiles_bytes(num_slots)
- *               bytes. Its layout is private to the library.
+ *               bytes, 16-byte aligned. Its layout is private to the library.
  */
 typedef struct {
   const int32_t *token_slot;

@@ -31,12 +31,13 @@ constexpr int kTT = 4;                 // tokens per tile
 constexpr int kAChunkBytes = 65536;    // A bytes a CTA stages at once (else a 2-stage stream)
 constexpr int kAStageBytes = 32768;    // stage size of that stream
 constexpr int kBPassBytes = 32768;     // B bytes staged per pass
+constexpr int kSmallTable = 256;       // slot tables up to this size: rank / scale copied whole
 
 struct Geo {
   int d_in, r_max, kc;   // kc: d_in rows per cluster CTA
   int sc_rows, nstage;   // A rows per stage; 1 = whole chunk resident
   int pw;                // B columns per pass
-  int off_a, off_x, off_red, off_cpart, off_u, off_rows, off_b, smem;
+  int off_a, off_x, off_red, off_cpart, off_u, off_rows, off_b, off_rs, smem;
 };
 
 struct BgmvArgs {
@@ -50,7 +51,7 @@ struct BgmvArgs {
   int out_sizes[LORA_MAX_SLICES];
   int out_off[LORA_MAX_SLICES];
   MetaView mv;
-  int list_off, list_cnt;
+  int list;    // int offset of the unit-record list inside the work lists
   const int32_t *slot_rank;
   const float *slot_scale;
   Geo g;
@@ -61,15 +62,33 @@ struct Unit {
   float scale;
 };
 
-__device__ __forceinline__ bool load_unit(const BgmvArgs &a, int item, Unit &u) {
-  const int32_t *W = a.mv.work;
-  if (item >= W[a.list_cnt]) return false;
-  const int seg = W[a.list_off + item];
-  u.slot = a.mv.seg_slot[seg];
-  u.cnt = a.mv.seg_count[seg];
-  u.start = a.mv.seg_start[seg];
-  u.r_a = min(max(a.slot_rank[u.slot], 0), a.g.r_max);
-  u.scale = a.slot_scale[u.slot];
+// One unit record (segment, slot, count, start, first rows) and the slot's
+// rank and scale. Small slot tables are copied whole into shared memory in
+// parallel with the record, so everything arrives in one round trip.
+// The record's first rows go to rows[0..kTT). Returns false (uniformly over
+// the CTA and its cluster) for an unused record.
+__device__ __forceinline__ bool load_unit(const BgmvArgs &a, int item, Unit &u, int32_t *rank_s, float *scale_s,
+                                          int *rows) {
+  const int S = a.mv.num_slots;
+  const bool small_table = S <= kSmallTable;
+  if (small_table) {
+    for (int i = threadIdx.x; i < S; i += kThreads) {
+      rank_s[i] = a.slot_rank[i];
+      scale_s[i] = a.slot_scale[i];
+    }
+  }
+  const int4 *rec = reinterpret_cast<const int4 *>(a.mv.work + a.list + item * WorkLists::kRec);
+  const int4 h = rec[0], r = rec[1];
+  if (h.y < 0) return false;
+  u.slot = h.y;
+  u.cnt = h.z;
+  u.start = h.w;
+  if (threadIdx.x < kTT)
+    rows[threadIdx.x] = threadIdx.x == 0 ? r.x : threadIdx.x == 1 ? r.y : threadIdx.x == 2 ? r.z : r.w;
+  __syncthreads();
+  const int rk = small_table ? rank_s[u.slot] : a.slot_rank[u.slot];
+  u.r_a = min(max(rk, 0), a.g.r_max);
+  u.scale = small_table ? scale_s[u.slot] : a.slot_scale[u.slot];
   return true;
 }
 
@@ -193,18 +212,27 @@ __device__ __forceinline__ void issue_b(TW *Bs, int pw, const TW *Bslot, int out
 // Shrink (kApply = false) or fused shrink + expand (kApply = true).
 // Grid: (CS * max_items, n_slices), cluster (CS, 1, 1).
 template <typename TW, typename TY, int NV, bool kApply>
-__global__ void __launch_bounds__(kThreads, kApply ? 2 : 3) bgmv_kernel(BgmvArgs a) {
+__global__ void __launch_bounds__(kThreads, kApply ? 3 : 4) bgmv_kernel(BgmvArgs a) {
   constexpr int VEC = Elem<TW>::kVec;
   constexpr int NRG = kThreads / NV;   // row groups
   constexpr int NVAL = kTT * VEC;      // accumulators per thread
-  constexpr int LPV = 32 / NV;         // lanes sharing one vector column (1 when NV == 32)
+  constexpr int LPV = 32 / NV;         // lanes sharing one vector column
   constexpr int NKEEP = NVAL / (LPV > NVAL ? NVAL : LPV);
   extern __shared__ __align__(16) unsigned char smem[];
   const Geo &g = a.g;
   const int cs = (int)cluster_nctarank(), crank = (int)cluster_ctarank();
   const int item = blockIdx.x / cs, slice = blockIdx.y;
+  TW *As = reinterpret_cast<TW *>(smem + g.off_a);
+  TW *xs = reinterpret_cast<TW *>(smem + g.off_x);             // [kTT][kc] raw x rows
+  float *wred = reinterpret_cast<float *>(smem + g.off_red);   // [kWarps][kTT][r_max]
+  float *cpart = reinterpret_cast<float *>(smem + g.off_cpart);// [kTT][r_max]
+  float *uT = reinterpret_cast<float *>(smem + g.off_u);       // [r_max][kTT]
+  int *rows = reinterpret_cast<int *>(smem + g.off_rows);
+  TW *Bs = reinterpret_cast<TW *>(smem + g.off_b);
+  int32_t *rank_s = reinterpret_cast<int32_t *>(smem + g.off_rs);
+  float *scale_s = reinterpret_cast<float *>(rank_s + kSmallTable);
   Unit u;
-  if (!load_unit(a, item, u)) return;  // uniform over the cluster
+  if (!load_unit(a, item, u, rank_s, scale_s, rows)) return;  // uniform over the cluster
   const int r_max = g.r_max;
   const int j0 = crank * g.kc;
   const int len = max(0, min(g.d_in - j0, g.kc));
@@ -212,14 +240,7 @@ __global__ void __launch_bounds__(kThreads, kApply ? 2 : 3) bgmv_kernel(BgmvArgs
   const int nva = (u.r_a + VEC - 1) / VEC;
   const TW *Ab = static_cast<const TW *>(a.A[slice]) + ((int64_t)u.slot * g.d_in + j0) * r_max;
   const TW *x = static_cast<const TW *>(a.x);
-  TW *As = reinterpret_cast<TW *>(smem + g.off_a);
-  float *xT = reinterpret_cast<float *>(smem + g.off_x);       // [kc][kTT]
-  float *wred = reinterpret_cast<float *>(smem + g.off_red);   // [kWarps][kTT][r_max]
-  float *cpart = reinterpret_cast<float *>(smem + g.off_cpart);// [kTT][r_max]
-  float *uT = reinterpret_cast<float *>(smem + g.off_u);       // [r_max][kTT]
-  int *rows = reinterpret_cast<int *>(smem + g.off_rows);
-  TW *Bs = reinterpret_cast<TW *>(smem + g.off_b);
-  const int tid = threadIdx.x, warp = tid >> 5;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int v = tid % NV, rq = tid / NV;
 
   const int out_s = a.out_sizes[slice];
@@ -227,8 +248,10 @@ __global__ void __launch_bounds__(kThreads, kApply ? 2 : 3) bgmv_kernel(BgmvArgs
   const int c0 = min(out_s, crank * per), c1 = min(out_s, c0 + per);
   const int npass = (c1 - c0 + g.pw - 1) / g.pw;
   const TW *Bslot = static_cast<const TW *>(a.B[slice]) + (int64_t)u.slot * r_max * out_s;
+  TY *y = static_cast<TY *>(a.y);
+  const int col_base = a.out_off[slice] + c0;
 
-  // A stage `sc` (rows sc*sc_rows ..) into buffer `stage`: one flat copy, rank tail skipped.
+  // A stage `sc` into buffer `stage`: one flat copy of contiguous rows, rank tail skipped.
   auto issue_a = [&](int sc, int stage) {
     const int r0 = sc * g.sc_rows, nr = min(g.sc_rows, len - r0);
     const uint4 *src = reinterpret_cast<const uint4 *>(Ab + (int64_t)r0 * r_max);
@@ -241,65 +264,59 @@ __global__ void __launch_bounds__(kThreads, kApply ? 2 : 3) bgmv_kernel(BgmvArgs
   const int ntiles = (u.cnt + kTT - 1) / kTT;
   for (int tile = 0; tile < ntiles; ++tile) {
     const int tok0 = tile * kTT, nt = min(kTT, u.cnt - tok0);
-    if (tid < kTT) rows[tid] = tid < nt ? a.mv.sorted_rows[u.start + tok0 + tid] : 0;
+    if (tile > 0) {
+      __syncthreads();
+      if (tid < nt) rows[tid] = a.mv.sorted_rows[u.start + tok0 + tid];
+      __syncthreads();
+    }
+    // One group: the first A stage and this tile's x rows (a warp per row).
     int g_s0 = -1, g_s1 = -1;
     if (tile == 0 || g.nstage > 1) {
       if (nsc > 0) issue_a(0, 0);
+    }
+    {
+      const int upr = len / VEC;
+      for (int t = warp; t < nt; t += kWarps) {
+        const TW *src = x + (int64_t)rows[t] * a.ldx + j0;
+        for (int c = lane; c < upr; c += 32) cp_async16(xs + t * g.kc + c * VEC, src + c * VEC);
+      }
+    }
+    cp_async_commit();
+    g_s0 = committed++;
+    if ((tile == 0 || g.nstage > 1) && nsc > 1) {
+      issue_a(1, 1);
       cp_async_commit();
-      g_s0 = committed++;
-      if (nsc > 1) {
-        issue_a(1, 1);
+      g_s1 = committed++;
+    }
+    if constexpr (kApply) {
+      if (tile == 0 && npass > 0) {
+        issue_b<TW>(Bs, g.pw, Bslot, out_s, u.r_a, c0, min(g.pw, c1 - c0));
         cp_async_commit();
-        g_s1 = committed++;
+        g_b = committed++;
       }
-    }
-    if (kApply && tile == 0 && npass > 0) {
-      issue_b<TW>(Bs, g.pw, Bslot, out_s, u.r_a, c0, min(g.pw, c1 - c0));
-      cp_async_commit();
-      g_b = committed++;
-    }
-    __syncthreads();  // rows visible
-    // x rows of the tile, widened and transposed to [row][token] (absent tokens 0):
-    // a thread per pair of rows, so a warp stores 32 consecutive 32-byte runs.
-    for (int p = tid; p < (len >> 1); p += kThreads) {
-      float f0[kTT], f1[kTT];
-#pragma unroll
-      for (int t = 0; t < kTT; ++t) {
-        f0[t] = 0.f;
-        f1[t] = 0.f;
-        if (t < nt) {
-          const TW *xp = x + (int64_t)rows[t] * a.ldx + j0 + 2 * p;
-          if constexpr (sizeof(TW) == 2) {
-            const uint32_t w = __ldg(reinterpret_cast<const unsigned int *>(xp));
-            f0[t] = __uint_as_float(w << 16);
-            f1[t] = __uint_as_float(w & 0xffff0000u);
-          } else {
-            const float2 w = __ldg(reinterpret_cast<const float2 *>(xp));
-            f0[t] = w.x;
-            f1[t] = w.y;
-          }
-        }
+      // The y rows this CTA will update, pulled into L2 while the shrink runs.
+      if (tid < nt && c1 > c0) {
+        prefetch_l2(y + (int64_t)rows[tid] * a.ldy + col_base, (uint32_t)((c1 - c0) * sizeof(TY)));
       }
-      reinterpret_cast<float4 *>(xT)[2 * p] = make_float4(f0[0], f0[1], f0[2], f0[3]);
-      reinterpret_cast<float4 *>(xT)[2 * p + 1] = make_float4(f1[0], f1[1], f1[2], f1[3]);
     }
 
     float acc[NVAL];
 #pragma unroll
     for (int i = 0; i < NVAL; ++i) acc[i] = 0.f;
     for (int sc = 0; sc < max(nsc, 1); ++sc) {
-      if (g.nstage > 1 || tile == 0) cp_async_wait_upto(committed - 1 - ((sc & 1) ? g_s1 : g_s0));
+      cp_async_wait_upto(committed - 1 - ((sc & 1) ? g_s1 : g_s0));
       __syncthreads();
       if (nsc > 0 && v < nva) {
         const int r0 = sc * g.sc_rows, nr = min(g.sc_rows, len - r0);
         const TW *Ast = As + (g.nstage > 1 ? (sc & 1) * g.sc_rows * r_max : 0) + v * VEC;
-        const float *xt = xT + r0 * kTT;
+        const TW *xt = xs + r0;
 #pragma unroll 2
         for (int jj = rq; jj < nr; jj += NRG) {
           float af[VEC];
           widen16<TW>(*reinterpret_cast<const uint4 *>(Ast + jj * r_max), af);
-          const float4 x4 = *reinterpret_cast<const float4 *>(xt + jj * kTT);
-          const float xv[kTT] = {x4.x, x4.y, x4.z, x4.w};
+          float xv[kTT];
+#pragma unroll
+          for (int t = 0; t < kTT; ++t) xv[t] = Elem<TW>::to_f(xt[t * g.kc + jj]);
 #pragma unroll
           for (int t = 0; t < kTT; ++t)
 #pragma unroll
@@ -314,6 +331,7 @@ __global__ void __launch_bounds__(kThreads, kApply ? 2 : 3) bgmv_kernel(BgmvArgs
       }
     }
     // Row groups inside a warp, then warps in order, then cluster CTAs in rank order.
+    // Entries of absent tokens (t >= nt) carry garbage and are never used.
     const int off = reduce_scatter<NVAL, NV>(acc);
 #pragma unroll
     for (int i = 0; i < NKEEP; ++i) {
@@ -321,7 +339,7 @@ __global__ void __launch_bounds__(kThreads, kApply ? 2 : 3) bgmv_kernel(BgmvArgs
       wred[(warp * kTT + t) * r_max + v * VEC + e] = acc[i];
     }
     __syncthreads();
-    for (int i = tid; i < kTT * r_max; i += kThreads) {
+    for (int i = tid; i < nt * r_max; i += kThreads) {
       float s = 0.f;
 #pragma unroll
       for (int w = 0; w < kWarps; ++w) s += wred[w * kTT * r_max + i];
@@ -358,7 +376,6 @@ __global__ void __launch_bounds__(kThreads, kApply ? 2 : 3) bgmv_kernel(BgmvArgs
     cluster_sync();  // partials read; other CTAs may reuse their buffers or exit
 
     if constexpr (kApply) {
-      TY *y = static_cast<TY *>(a.y);
       for (int pass = 0; pass < npass; ++pass) {
         const int pc0 = c0 + pass * g.pw, pcn = min(g.pw, c1 - pc0);
         const bool resident = (pass == 0 && tile == 0) || (npass == 1 && tile > 0);
@@ -373,7 +390,6 @@ __global__ void __launch_bounds__(kThreads, kApply ? 2 : 3) bgmv_kernel(BgmvArgs
         expand_pass<TW, TY>(Bs, g.pw, uT, u.r_a, rows, nt, y, a.ldy, a.out_off[slice] + pc0, pcn);
       }
     }
-    __syncthreads();  // rows / xT / uT are rewritten by the next tile
   }
   cp_async_wait_upto(0);
 }
@@ -386,45 +402,52 @@ struct ExpandArgs {
 };
 
 template <typename TW, typename TY>
-__global__ void __launch_bounds__(kThreads) bgmv_expand_kernel(ExpandArgs ea) {
+__global__ void __launch_bounds__(kThreads, 4) bgmv_expand_kernel(ExpandArgs ea) {
   const BgmvArgs &a = ea.b;
   const Geo &g = a.g;
   extern __shared__ __align__(16) unsigned char smem[];
+  TW *Bs = reinterpret_cast<TW *>(smem + g.off_b);
+  float *uT = reinterpret_cast<float *>(smem + g.off_u);
+  int *rows = reinterpret_cast<int *>(smem + g.off_rows);
+  int32_t *rank_s = reinterpret_cast<int32_t *>(smem + g.off_rs);
+  float *scale_s = reinterpret_cast<float *>(rank_s + kSmallTable);
   Unit u;
-  if (!load_unit(a, blockIdx.y, u)) return;
+  if (!load_unit(a, blockIdx.y, u, rank_s, scale_s, rows)) return;
   int s = 0;
   while (s + 1 < ea.n_slices && (int)blockIdx.x >= ea.chunk_start[s + 1]) ++s;
   const int out_s = a.out_sizes[s];
   const int pc0 = ((int)blockIdx.x - ea.chunk_start[s]) * g.pw;
   const int pcn = min(g.pw, out_s - pc0);
   const int r_max = g.r_max;
-  TW *Bs = reinterpret_cast<TW *>(smem + g.off_b);
-  float *uT = reinterpret_cast<float *>(smem + g.off_u);
-  int *rows = reinterpret_cast<int *>(smem + g.off_rows);
   const TW *Bslot = static_cast<const TW *>(a.B[s]) + (int64_t)u.slot * r_max * out_s;
   const float *bufs = a.buf + (int64_t)s * a.mv.num_tokens * r_max;
+  TY *y = static_cast<TY *>(a.y);
+  const int col_base = a.out_off[s] + pc0;
   issue_b<TW>(Bs, g.pw, Bslot, out_s, u.r_a, pc0, pcn);
   cp_async_commit();
   const int ntiles = (u.cnt + kTT - 1) / kTT;
   for (int tile = 0; tile < ntiles; ++tile) {
     const int tok0 = tile * kTT, nt = min(kTT, u.cnt - tok0);
-    if (threadIdx.x < kTT) rows[threadIdx.x] = threadIdx.x < nt ? a.mv.sorted_rows[u.start + tok0 + threadIdx.x] : 0;
-    __syncthreads();
+    if (tile > 0) {
+      __syncthreads();
+      if (threadIdx.x < nt) rows[threadIdx.x] = a.mv.sorted_rows[u.start + tok0 + threadIdx.x];
+      __syncthreads();
+    }
+    if (threadIdx.x < nt) prefetch_l2(y + (int64_t)rows[threadIdx.x] * a.ldy + col_base, (uint32_t)(pcn * sizeof(TY)));
     for (int i = threadIdx.x; i < kTT * r_max; i += kThreads) {
       const int tt = i / r_max, k = i - tt * r_max;
       uT[k * kTT + tt] = (tt < nt && k < u.r_a) ? bufs[(int64_t)rows[tt] * r_max + k] : 0.f;
     }
     cp_async_wait_upto(0);
     __syncthreads();
-    expand_pass<TW, TY>(Bs, g.pw, uT, u.r_a, rows, nt, static_cast<TY *>(a.y), a.ldy, a.out_off[s] + pc0, pcn);
-    __syncthreads();
+    expand_pass<TW, TY>(Bs, g.pw, uT, u.r_a, rows, nt, y, a.ldy, col_base, pcn);
   }
 }
 
 int align16(int v) { return (v + 15) & ~15; }
 
 int cluster_size(int d_in) {
-  int cs = d_in / 1024;
+  int cs = d_in / 512;
   return cs < 1 ? 1 : (cs > 8 ? 8 : cs);
 }
 
@@ -432,7 +455,6 @@ int cluster_size(int d_in) {
 Geo make_geo(const lora_layer_desc &d, int cs, int mode) {
   Geo g{};
   const int es = d.dtype == LORA_BF16 ? 2 : 4;
-  const int vec = 16 / es;
   g.d_in = d.d_in;
   g.r_max = d.r_max;
   g.kc = (((d.d_in + cs - 1) / cs) + 7) & ~7;
@@ -455,10 +477,12 @@ Geo make_geo(const lora_layer_desc &d, int cs, int mode) {
   if (pw > max_cols) pw = max_cols;
   g.pw = pw;
   int off = 0;
+  g.off_rs = off;
+  off += align16(2 * kSmallTable * 4);
   g.off_a = off;
   if (mode != 1) off += align16(g.nstage * g.sc_rows * row_bytes);
   g.off_x = off;
-  if (mode != 1) off += align16(g.kc * kTT * 4);
+  if (mode != 1) off += align16(kTT * g.kc * es);
   g.off_red = off;
   if (mode != 1) off += align16(kWarps * kTT * d.r_max * 4);
   g.off_cpart = off;
@@ -470,15 +494,11 @@ Geo make_geo(const lora_layer_desc &d, int cs, int mode) {
   g.off_b = off;
   if (mode != 0) off += align16(d.r_max * pw * es);
   g.smem = off;
-  (void)vec;
   return g;
 }
 
 void fill_common(BgmvArgs &a, const lora_layer_desc &d, const MetaView &mv, ListSel sel) {
-  const int S = mv.num_slots;
-  a.list_off = sel == kListSmall ? WorkLists::small_seg(S) : sel == kListLarge ? WorkLists::large_seg(S)
-                                                                               : WorkLists::all_seg(S);
-  a.list_cnt = sel == kListSmall ? 1 : sel == kListLarge ? 2 : 0;
+  a.list = WorkLists::list(mv.num_slots, sel);
   a.mv = mv;
   int off = 0;
   for (int s = 0; s < d.n_slices; ++s) {

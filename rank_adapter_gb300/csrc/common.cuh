@@ -110,6 +110,10 @@ __device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(smem)), "l"(gmem) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Ask the memory system to bring [p, p + bytes) into L2 (no completion to wait for).
+__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
 // Wait until at most n of the most recently committed groups are still pending.
 __device__ __forceinline__ void cp_async_wait_upto(int n) {
   if (n <= 0) asm volatile("cp.async.wait_group 0;" ::: "memory");
@@ -127,16 +131,17 @@ __device__ __forceinline__ void cp_async_wait_upto(int n) {
 //   [3] tiles_all    sum over all LoRA segments of ceil(count / LORA_SGMV_TILE_M)
 //   [4] tiles_large  the same over the large segments
 //   [5..7] reserved (0)
-//   then five arrays, S = num_slots:
-//   all_seg[S], small_seg[S], large_seg[S], all_tile_start[S+1], large_tile_start[S+1]
+//   then three lists of S = num_slots unit records (all, small, large), each
+//   record 8 ints: {segment, slot, count, first sorted row, first 4 token rows}
+//   (rows past the count are -1; unused records are all -1),
+//   then all_tile_start[S+1] and large_tile_start[S+1] (cumulative tile counts).
 struct WorkLists {
   static constexpr int kHeader = 8;
-  __host__ __device__ static inline size_t ints(int S) { return kHeader + 5 * (size_t)S + 2; }
-  __host__ __device__ static inline int all_seg(int S) { (void)S; return kHeader; }
-  __host__ __device__ static inline int small_seg(int S) { return kHeader + S; }
-  __host__ __device__ static inline int large_seg(int S) { return kHeader + 2 * S; }
-  __host__ __device__ static inline int all_tile_start(int S) { return kHeader + 3 * S; }
-  __host__ __device__ static inline int large_tile_start(int S) { return kHeader + 4 * S + 1; }
+  static constexpr int kRec = 8;
+  __host__ __device__ static inline size_t ints(int S) { return kHeader + 3 * (size_t)kRec * S + 2 * ((size_t)S + 1); }
+  __host__ __device__ static inline int list(int S, int which) { return kHeader + which * kRec * S; }
+  __host__ __device__ static inline int all_tile_start(int S) { return kHeader + 3 * kRec * S; }
+  __host__ __device__ static inline int large_tile_start(int S) { return kHeader + 3 * kRec * S + S + 1; }
 };
 
 enum ListSel { kListAll = 0, kListSmall = 1, kListLarge = 2 };

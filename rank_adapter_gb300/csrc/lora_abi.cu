@@ -66,7 +66,7 @@ int check_meta(const lora_meta *m) {
   if (!m->seg_slot || !m->seg_count || !m->seg_start || !m->num_segs || !m->no_lora || !m->status || !m->tiles)
     return LORA_EINVAL;
   if (m->tiles_bytes < lora_meta_tiles_bytes(m->num_slots)) return LORA_EINVAL;
-  if (reinterpret_cast<uintptr_t>(m->tiles) & 3u) return LORA_EALIGN;
+  if (!aligned16(m->tiles)) return LORA_EALIGN;
   return LORA_OK;
 }
 

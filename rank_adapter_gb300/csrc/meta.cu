@@ -70,9 +70,11 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_meta_kernel(MetaArgs a) {
   extern __shared__ int32_t sm[];
   const int S = a.S, T = a.T;
   const int hs = S + 1;             // odd row stride: a warp reading one slot's column hits 32 banks
-  int32_t *hist = sm;               // [kWarps][hs]: counts, then offsets inside each slot
-  int32_t *tot_s = sm + kWarps * hs;   // [S]
-  int32_t *base_s = tot_s + S;         // [S]
+  int32_t *hist = sm;                  // [kWarps][hs]: counts, then offsets inside each slot
+  int32_t *tot_s = sm + kWarps * hs;   // [S] tokens per slot
+  int32_t *base_s = tot_s + S;         // [S] first sorted row of each slot
+  int32_t *rec_a = base_s + S;         // [S] int offset of the slot's record in the "all" list, or -1
+  int32_t *rec_k = rec_a + S;          // [S] int offset of its record in the small or large list
   __shared__ int tmp[7 * kWarps];
   __shared__ int s_bad;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -124,34 +126,54 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_meta_kernel(MetaArgs a) {
   const int vals[7] = {tot, present, lora, small, large, tiles, large ? tiles : 0};
   int ex[7], tl[7];
   block_excl_scan_n<7>(vals, ex, tl, tmp);
-  const int base = ex[0], seg_idx = ex[1], all_idx = ex[2], small_idx = ex[3], large_idx = ex[4];
+  const int base = ex[0], seg_idx = ex[1];
   const int nsegs = tl[1], n_all = tl[2], n_small = tl[3], n_large = tl[4];
   const int tiles_all = tl[5], tiles_large = tl[6];
-  if (tid < S) base_s[tid] = base;
+  constexpr int R = WorkLists::kRec;
 
   int32_t *W = a.work;
+  if (tid < S) {
+    base_s[tid] = base;
+    rec_a[tid] = lora ? WorkLists::list(S, kListAll) + ex[2] * R : -1;
+    rec_k[tid] = small ? WorkLists::list(S, kListSmall) + ex[3] * R
+               : large ? WorkLists::list(S, kListLarge) + ex[4] * R : -1;
+  }
   if (present) {
     a.seg_slot[seg_idx] = tid;
     a.seg_count[seg_idx] = tot;
     a.seg_start[seg_idx] = base;
   }
   if (lora) {
-    W[WorkLists::all_seg(S) + all_idx] = seg_idx;
-    W[WorkLists::all_tile_start(S) + all_idx] = ex[5];
+    const int4 head = make_int4(seg_idx, tid, tot, base);
+    const int4 none = make_int4(-1, -1, -1, -1);
+    int32_t *ra_ = W + WorkLists::list(S, kListAll) + ex[2] * R;
+    int32_t *rk_ = W + (small ? WorkLists::list(S, kListSmall) + ex[3] * R : WorkLists::list(S, kListLarge) + ex[4] * R);
+    reinterpret_cast<int4 *>(ra_)[0] = head;
+    reinterpret_cast<int4 *>(ra_)[1] = none;
+    reinterpret_cast<int4 *>(rk_)[0] = head;
+    reinterpret_cast<int4 *>(rk_)[1] = none;
+    W[WorkLists::all_tile_start(S) + ex[2]] = ex[5];
+    if (large) W[WorkLists::large_tile_start(S) + ex[4]] = ex[6];
   }
-  if (small) W[WorkLists::small_seg(S) + small_idx] = seg_idx;
-  if (large) {
-    W[WorkLists::large_seg(S) + large_idx] = seg_idx;
-    W[WorkLists::large_tile_start(S) + large_idx] = ex[6];
+  // Unused records, tails, scalars.
+  const int4 none = make_int4(-1, -1, -1, -1);
+  for (int i = tid; i < S; i += kThreads) {
+    if (i >= n_all) {
+      reinterpret_cast<int4 *>(W + WorkLists::list(S, kListAll) + i * R)[0] = none;
+      reinterpret_cast<int4 *>(W + WorkLists::list(S, kListAll) + i * R)[1] = none;
+    }
+    if (i >= n_small) {
+      reinterpret_cast<int4 *>(W + WorkLists::list(S, kListSmall) + i * R)[0] = none;
+      reinterpret_cast<int4 *>(W + WorkLists::list(S, kListSmall) + i * R)[1] = none;
+    }
+    if (i >= n_large) {
+      reinterpret_cast<int4 *>(W + WorkLists::list(S, kListLarge) + i * R)[0] = none;
+      reinterpret_cast<int4 *>(W + WorkLists::list(S, kListLarge) + i * R)[1] = none;
+    }
   }
   for (int i = tid; i <= S; i += kThreads) {
     if (i < S && i >= nsegs) { a.seg_slot[i] = -1; a.seg_count[i] = 0; }
     if (i >= nsegs) a.seg_start[i] = T;
-    if (i < S) {
-      if (i >= n_all) W[WorkLists::all_seg(S) + i] = -1;
-      if (i >= n_small) W[WorkLists::small_seg(S) + i] = -1;
-      if (i >= n_large) W[WorkLists::large_seg(S) + i] = -1;
-    }
     if (i >= n_all) W[WorkLists::all_tile_start(S) + i] = tiles_all;
     if (i >= n_large) W[WorkLists::large_tile_start(S) + i] = tiles_large;
   }
@@ -164,7 +186,8 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_meta_kernel(MetaArgs a) {
   }
   __syncthreads();
 
-  // Pass 2: stable scatter of token indices.
+  // Pass 2: stable scatter of token indices; the first 4 rows of each LoRA
+  // segment also go into its unit records.
   for (int b = t0; b < t1; b += 32) {
     const int t = b + lane;
     const bool valid = t < t1;
@@ -177,7 +200,12 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_meta_kernel(MetaArgs a) {
     uint32_t peers = 0;
     if (valid) {
       peers = __match_any_sync(act, s);
-      a.sorted_rows[base_s[s] + hist[warp * hs + s] + __popc(peers & lanemask_lt())] = t;
+      const int rel = hist[warp * hs + s] + __popc(peers & lanemask_lt());
+      a.sorted_rows[base_s[s] + rel] = t;
+      if (rel < 4 && rec_a[s] >= 0) {
+        W[rec_a[s] + 4 + rel] = t;
+        W[rec_k[s] + 4 + rel] = t;
+      }
     }
     __syncwarp();
     if (valid && lane == __ffs(peers) - 1) hist[warp * hs + s] += __popc(peers);
@@ -200,9 +228,9 @@ cudaError_t launch_prepare_meta(const lora_meta &m, cudaStream_t st) {
   a.no_lora = m.no_lora;
   a.status = m.status;
   a.work = static_cast<int32_t *>(m.tiles);
-  const size_t smem = ((size_t)kWarps * (m.num_slots + 1) + 2 * (size_t)m.num_slots) * sizeof(int32_t);
+  const size_t smem = ((size_t)kWarps * (m.num_slots + 1) + 4 * (size_t)m.num_slots) * sizeof(int32_t);
   cudaError_t e = set_max_dynamic_smem((const void *)prepare_meta_kernel,
-                                       (int)(((size_t)kWarps * (LORA_MAX_NUM_SLOTS + 1) + 2 * LORA_MAX_NUM_SLOTS) *
+                                       (int)(((size_t)kWarps * (LORA_MAX_NUM_SLOTS + 1) + 4 * LORA_MAX_NUM_SLOTS) *
                                              sizeof(int32_t)));
   if (e != cudaSuccess) return e;
   prepare_meta_kernel<<<1, kThreads, smem, st>>>(a);

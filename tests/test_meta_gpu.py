@@ -35,20 +35,33 @@ def _run(ra, ts, S):
 
 def _work_lists(ref, S):
     """The work lists by their definition: LoRA segments (slot != 0), split at
-    LORA_SGMV_MIN_ROWS, with cumulative counts of 128-row tiles."""
+    LORA_SGMV_MIN_ROWS, as 8-int records {segment, slot, count, start, first 4
+    rows (-1 past the count)}, unused records all -1, then cumulative counts of
+    128-row tiles over all LoRA segments and over the large ones."""
     import rank_adapter_gb300 as ra
     n = ref["num_segs"]
-    segs = [i for i in range(n) if ref["seg_slot"][i] != 0]
-    cnt = ref["seg_count"]
+    slot, cnt, start, rows = ref["seg_slot"], ref["seg_count"], ref["seg_start"], ref["sorted_rows"]
+    segs = [i for i in range(n) if slot[i] != 0]
     small = [i for i in segs if cnt[i] < ra.LORA_SGMV_MIN_ROWS]
     large = [i for i in segs if cnt[i] >= ra.LORA_SGMV_MIN_ROWS]
-    tiles = lambda lst: [(cnt[i] + ra.LORA_SGMV_TILE_M - 1) // ra.LORA_SGMV_TILE_M for i in lst]
-    pad = lambda lst, v: list(lst) + [v] * (S - len(lst))
-    cum = lambda lst: list(np.concatenate([[0], np.cumsum(tiles(lst))]).astype(int))
+
+    def rec(i):
+        return [i, slot[i], cnt[i], start[i]] + [int(rows[start[i] + j]) if j < cnt[i] else -1 for j in range(4)]
+
+    def lst(L):
+        out = []
+        for i in L:
+            out += rec(i)
+        return out + [-1] * 8 * (S - len(L))
+
+    def cum(L):
+        c = [0]
+        for i in L:
+            c.append(c[-1] + (int(cnt[i]) + ra.LORA_SGMV_TILE_M - 1) // ra.LORA_SGMV_TILE_M)
+        return c + [c[-1]] * (S + 1 - len(c))
+
     ca, cl = cum(segs), cum(large)
-    w = [len(segs), len(small), len(large), ca[-1], cl[-1], 0, 0, 0]
-    w += pad(segs, -1) + pad(small, -1) + pad(large, -1)
-    w += ca + [ca[-1]] * (S + 1 - len(ca)) + cl + [cl[-1]] * (S + 1 - len(cl))
+    w = [len(segs), len(small), len(large), ca[-1], cl[-1], 0, 0, 0] + lst(segs) + lst(small) + lst(large) + ca + cl
     return np.asarray(w, np.int32)
 
 
