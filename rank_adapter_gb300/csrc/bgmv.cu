@@ -645,7 +645,7 @@ int resident_clusters(const void *k, int cs, int smem) {
 template <typename TW, typename TY, bool kApply, int NV>
 cudaError_t launch_nv(const BgmvArgs &a, int cs, int max_units, cudaStream_t st) {
   auto k = bgmv_kernel<TW, TY, NV, kApply>;
-  cudaError_t e = set_max_dynamic_smem((const void *)k, 227 * 1024);
+  cudaError_t e = set_max_dynamic_smem((const void *)k, a.g.smem);
   if (e != cudaSuccess) return e;
   int ncl = resident_clusters((const void *)k, cs, a.g.smem);
   if (ncl > max_units) ncl = max_units;
@@ -738,7 +738,7 @@ cudaError_t launch_bgmv_expand(const lora_layer_desc &d, const MetaView &mv, Lis
   if (d.dtype == LORA_BF16 && y_dtype == LORA_BF16) k = bgmv_expand_kernel<__nv_bfloat16, __nv_bfloat16>;
   else if (d.dtype == LORA_BF16) k = bgmv_expand_kernel<__nv_bfloat16, float>;
   else k = bgmv_expand_kernel<float, float>;
-  cudaError_t e = set_max_dynamic_smem((const void *)k, 227 * 1024);
+  cudaError_t e = set_max_dynamic_smem((const void *)k, (int)smem);
   if (e != cudaSuccess) return e;
   k<<<grid, kThreads, smem, st>>>(ea);
   return cudaGetLastError();

@@ -159,7 +159,7 @@ struct MetaView {
 
 // ------------------------------------------------------------------ host helpers
 
-// Raise a kernel's dynamic shared-memory limit once per (kernel, device).
+// Raise a kernel's dynamic shared-memory limit to at least `bytes` (per kernel and device).
 cudaError_t set_max_dynamic_smem(const void *kernel, int bytes);
 
 // Launch with a thread-block cluster of `cluster_x` CTAs along x.

@@ -4,7 +4,7 @@
 // launch attributes.
 #include <algorithm>
 #include <mutex>
-#include <set>
+#include <map>
 #include <utility>
 
 #include "common.cuh"
@@ -13,14 +13,16 @@ namespace ra {
 
 cudaError_t set_max_dynamic_smem(const void *kernel, int bytes) {
   static std::mutex mu;
-  static std::set<std::pair<const void *, int>> done;
+  static std::map<std::pair<const void *, int>, int> granted;  // (kernel, device) -> limit set so far
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lock(mu);
-  if (done.count({kernel, dev})) return cudaSuccess;
+  auto it = granted.find({kernel, dev});
+  if (it != granted.end() && it->second >= bytes) return cudaSuccess;
+  if (bytes <= 48 * 1024) return cudaSuccess;  // within the default limit
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e == cudaSuccess) done.insert({kernel, dev});
+  if (e == cudaSuccess) granted[{kernel, dev}] = bytes;
   return e;
 }
 
@@ -29,6 +31,10 @@ cudaError_t set_max_dynamic_smem(const void *kernel, int bytes) {
 namespace {
 
 thread_local int g_last_cuda_error = 0;
+
+// Clear a launch error left in this library's runtime state by an earlier
+// failed call, so that it is not reported against the next one.
+void clear_stale_error() { (void)cudaGetLastError(); }
 
 int cuda_status(cudaError_t e) {
   if (e == cudaSuccess) return LORA_OK;
@@ -118,6 +124,7 @@ size_t lora_workspace_bytes(const lora_layer_desc *desc, int32_t max_tokens, int
 
 int lora_set_slot(const lora_layer_desc *desc, int32_t slot, int32_t rank, float scale,
                   const void *const *A_src, const void *const *B_src, lora_stream_t stream) {
+  clear_stale_error();
   int st = check_desc(desc);
   if (st != LORA_OK) return st;
   if (slot < 1 || slot >= desc->num_slots) return LORA_ERANGE;
@@ -132,6 +139,7 @@ int lora_set_slot(const lora_layer_desc *desc, int32_t slot, int32_t rank, float
 }
 
 int lora_reset_slot(const lora_layer_desc *desc, int32_t slot, lora_stream_t stream) {
+  clear_stale_error();
   int st = check_desc(desc);
   if (st != LORA_OK) return st;
   if (slot < 1 || slot >= desc->num_slots) return LORA_ERANGE;
@@ -139,6 +147,7 @@ int lora_reset_slot(const lora_layer_desc *desc, int32_t slot, lora_stream_t str
 }
 
 int lora_prepare_meta(const lora_meta *meta, lora_stream_t stream) {
+  clear_stale_error();
   int st = check_meta(meta);
   if (st != LORA_OK) return st;
   return cuda_status(ra::launch_prepare_meta(*meta, (cudaStream_t)stream));
@@ -146,6 +155,7 @@ int lora_prepare_meta(const lora_meta *meta, lora_stream_t stream) {
 
 int lora_shrink(const lora_layer_desc *desc, const lora_meta *meta, const void *x, int64_t ldx,
                 float *buf, int32_t kind, void *ws, size_t ws_bytes, lora_stream_t stream) {
+  clear_stale_error();
   (void)ws;
   (void)ws_bytes;
   int st = check_desc(desc);
@@ -172,6 +182,7 @@ int lora_shrink(const lora_layer_desc *desc, const lora_meta *meta, const void *
 
 int lora_expand(const lora_layer_desc *desc, const lora_meta *meta, const float *buf, void *y,
                 int64_t ldy, int32_t y_dtype, int32_t kind, lora_stream_t stream) {
+  clear_stale_error();
   int st = check_desc(desc);
   if (st != LORA_OK) return st;
   st = check_meta(meta);
@@ -200,6 +211,7 @@ int lora_expand(const lora_layer_desc *desc, const lora_meta *meta, const float 
 
 int lora_apply(const lora_layer_desc *desc, const lora_meta *meta, const void *x, int64_t ldx, float *buf,
                void *y, int64_t ldy, int32_t y_dtype, int32_t kind, lora_stream_t stream) {
+  clear_stale_error();
   int st = check_desc(desc);
   if (st != LORA_OK) return st;
   st = check_meta(meta);

@@ -229,9 +229,7 @@ cudaError_t launch_prepare_meta(const lora_meta &m, cudaStream_t st) {
   a.status = m.status;
   a.work = static_cast<int32_t *>(m.tiles);
   const size_t smem = ((size_t)kWarps * (m.num_slots + 1) + 4 * (size_t)m.num_slots) * sizeof(int32_t);
-  cudaError_t e = set_max_dynamic_smem((const void *)prepare_meta_kernel,
-                                       (int)(((size_t)kWarps * (LORA_MAX_NUM_SLOTS + 1) + 4 * LORA_MAX_NUM_SLOTS) *
-                                             sizeof(int32_t)));
+  cudaError_t e = set_max_dynamic_smem((const void *)prepare_meta_kernel, (int)smem);
   if (e != cudaSuccess) return e;
   prepare_meta_kernel<<<1, kThreads, smem, st>>>(a);
   return cudaGetLastError();
