@@ -239,6 +239,8 @@ __global__ void __launch_bounds__(kThreads, 2) bgmv_kernel(BgmvArgs a) {
   constexpr int LPV = 32 / NV;          // lanes sharing one vector column
   constexpr int NKEEP = NVAL / (LPV > NVAL ? NVAL : LPV);
   extern __shared__ __align__(16) unsigned char smem[];
+  pdl_wait();
+  pdl_trigger();
   const Geo &g = a.g;
   const int item = (int)blockIdx.x % a.max_items;
   const int slice = a.slice_order[blockIdx.x / a.max_items];
@@ -389,6 +391,8 @@ __global__ void __launch_bounds__(kThreads, 2) bgmv_kernel(BgmvArgs a) {
 template <typename TW, typename TY>
 __global__ void __launch_bounds__(kThreads, 4) bgmv_expand_kernel(BgmvArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
+  pdl_wait();
+  pdl_trigger();
   const Geo &g = a.g;
   int s = 0;
   while (s + 1 < a.n_slices && (int)blockIdx.x >= a.chunk_start[s + 1]) ++s;
@@ -497,8 +501,7 @@ cudaError_t launch_nv(const BgmvArgs &a, cudaStream_t st) {
   auto k = bgmv_kernel<TW, TY, NV, kApply>;
   cudaError_t e = set_max_dynamic_smem((const void *)k, a.g.smem);
   if (e != cudaSuccess) return e;
-  k<<<a.max_items * a.n_slices, kThreads, a.g.smem, st>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(k, dim3((unsigned)(a.max_items * a.n_slices)), dim3(kThreads), (size_t)a.g.smem, st, 1u, a);
 }
 
 template <typename TW, typename TY, bool kApply>
@@ -576,8 +579,7 @@ cudaError_t launch_bgmv_expand(const lora_layer_desc &d, const MetaView &mv, Lis
   else k = bgmv_expand_kernel<float, float>;
   cudaError_t e = set_max_dynamic_smem((const void *)k, a.g.smem);
   if (e != cudaSuccess) return e;
-  k<<<grid, kThreads, a.g.smem, st>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(k, grid, dim3(kThreads), (size_t)a.g.smem, st, 1u, a);
 }
 
 }  // namespace ra

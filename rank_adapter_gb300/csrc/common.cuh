@@ -157,27 +157,45 @@ struct MetaView {
   int32_t num_slots;
 };
 
+// ------------------------------------------------------------------ programmatic dependent launch
+// Every kernel of this library is launched with programmatic stream
+// serialization, so it may be scheduled while its predecessor on the stream
+// drains. Each kernel therefore waits for the predecessor's completion (and
+// memory flush) before its first global-memory access of any kind, and lets
+// its own successor be scheduled right away; only launch latency overlaps,
+// never data.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ------------------------------------------------------------------ host helpers
 
 // Raise a kernel's dynamic shared-memory limit to at least `bytes` (per kernel and device).
 cudaError_t set_max_dynamic_smem(const void *kernel, int bytes);
 
-// Launch with a thread-block cluster of `cluster_x` CTAs along x.
+// Launch with programmatic stream serialization (see pdl_wait) and, when
+// cluster_x > 1, thread-block clusters of cluster_x CTAs along x.
 template <typename... KArgs, typename... Args>
-cudaError_t launch_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
-                           unsigned cluster_x, Args... args) {
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       unsigned cluster_x, Args... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = cluster_x;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
+  if (cluster_x > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = cluster_x;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = n;
   return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 

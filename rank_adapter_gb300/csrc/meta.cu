@@ -78,6 +78,8 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_meta_kernel(MetaArgs a) {
   __shared__ int tmp[7 * kWarps];
   __shared__ int s_bad;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  pdl_wait();
+  pdl_trigger();
 
   for (int i = tid; i < kWarps * hs; i += kThreads) hist[i] = 0;
   if (tid == 0) s_bad = 0;
@@ -231,8 +233,7 @@ cudaError_t launch_prepare_meta(const lora_meta &m, cudaStream_t st) {
   const size_t smem = ((size_t)kWarps * (m.num_slots + 1) + 4 * (size_t)m.num_slots) * sizeof(int32_t);
   cudaError_t e = set_max_dynamic_smem((const void *)prepare_meta_kernel, (int)smem);
   if (e != cudaSuccess) return e;
-  prepare_meta_kernel<<<1, kThreads, smem, st>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(prepare_meta_kernel, dim3(1), dim3(kThreads), smem, st, 1u, a);
 }
 
 }  // namespace ra

@@ -25,6 +25,8 @@ struct SlotArgs {
 // destination elements with one vector store.
 template <typename T>
 __global__ void __launch_bounds__(256) slot_write_kernel(SlotArgs a) {
+  pdl_wait();
+  pdl_trigger();
   const int s = blockIdx.y >> 1;
   const bool isB = blockIdx.y & 1;
   if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
@@ -90,11 +92,8 @@ cudaError_t launch_slot_write(const lora_layer_desc &d, int slot, int rank, floa
   if (blocks > 1216) blocks = 1216;  // 8 CTAs per SM x 152 SMs, grid-stride beyond
   if (blocks < 1) blocks = 1;
   dim3 grid((unsigned)blocks, 2 * d.n_slices);
-  if (d.dtype == LORA_BF16)
-    slot_write_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(a);
-  else
-    slot_write_kernel<float><<<grid, 256, 0, st>>>(a);
-  return cudaGetLastError();
+  if (d.dtype == LORA_BF16) return launch_pdl(slot_write_kernel<__nv_bfloat16>, grid, dim3(256), 0, st, 1u, a);
+  return launch_pdl(slot_write_kernel<float>, grid, dim3(256), 0, st, 1u, a);
 }
 
 }  // namespace ra
