@@ -270,6 +270,9 @@ class Replica:
         self.meta.token_slot[:T].copy_(ts_src)
         self.meta.set_num_tokens(T)
         self.buf = torch.zeros(inst.n_slices, T, inst.r_max, dtype=torch.float32, device="cuda")
+        self.ws = ra.workspace(self.table, T, kind)
+        self.ws_ptr = self.ws.data_ptr() if self.ws is not None else 0
+        self.ws_bytes = self.ws.numel() * 4 if self.ws is not None else 0
         self.kind = kind
         self.ydt = ra.LORA_BF16 if self.y.dtype == torch.bfloat16 else ra.LORA_F32
 
@@ -289,12 +292,13 @@ class Replica:
         if path == "fused":
             buf = self.buf.data_ptr() if self.kind != ra.LORA_BGMV else 0
             ra.check(ra.lora_apply(self.table.desc, self.meta.c, self.x.data_ptr(), self.x.stride(0), buf,
-                                   self.y.data_ptr(), self.y.stride(0), self.ydt, self.kind, st), "apply")
+                                   self.y.data_ptr(), self.y.stride(0), self.ydt, self.kind, self.ws_ptr,
+                                   self.ws_bytes, st), "apply")
             if ev is not None:
                 ev[2].record()
             return
         ra.check(ra.lora_shrink(self.table.desc, self.meta.c, self.x.data_ptr(), self.x.stride(0),
-                                self.buf.data_ptr(), self.kind, 0, 0, st), "shrink")
+                                self.buf.data_ptr(), self.kind, self.ws_ptr, self.ws_bytes, st), "shrink")
         if ev is not None:
             ev[2].record()
         ra.check(ra.lora_expand(self.table.desc, self.meta.c, self.buf.data_ptr(), self.y.data_ptr(),

@@ -170,7 +170,12 @@ int lora_prepare_meta(const lora_meta *meta, lora_stream_t stream);
  *   x:   device, [num_tokens, d_in] with row stride ldx elements, desc->dtype
  *   buf: device fp32, [n_slices, num_tokens, r_max] contiguous; rows of
  *        slot-0 tokens are not written
- *   ws:  scratch; may be NULL when lora_workspace_bytes() returns 0
+ *   ws:  device scratch of at least lora_workspace_bytes(desc, num_tokens,
+ *        kind) bytes, 16-byte aligned, caller-owned; may be NULL when that is
+ *        0. The CUDA-core family splits d_in into chunks and keeps each
+ *        chunk's partial rows there; its contents need no initialisation and
+ *        are meaningless between calls. Calls that share a workspace must not
+ *        overlap in time (order them on one stream).
  * bf16 inputs are multiplied exactly and accumulated in fp32 in a fixed
  * order (results do not depend on the batch's other tokens).
  */
@@ -193,24 +198,26 @@ int lora_expand(const lora_layer_desc *desc, const lora_meta *meta, const float 
                 int64_t ldy, int32_t y_dtype, int32_t kind, lora_stream_t stream);
 
 /*
- * Fused shrink + expand: the whole delta for every LoRA token in one pass,
+ * Fused shrink + expand: the whole delta for every LoRA token in one call,
  *   y[t, off_s + n] += sum_k (scale[a] * x[t] . A[s][a])[k] * B[s][a, k, n]
  * with the same arithmetic, rounding and slot-0 rule as lora_shrink followed
  * by lora_expand (results are bitwise equal for segments that run in the
- * BGMV family). In the BGMV family one thread-block cluster per (segment,
- * slice) reduces the rank-r row in distributed shared memory and adds it
- * into y without an fp32 round trip through global memory (the
- * "batched gather" form of the handbook page, section "不合并权重，批量计算").
+ * BGMV family). In the BGMV family the expand forms the rank-r rows
+ * directly from the shrink's chunk partials, so the u buffer is optional
+ * (the "batched gather" form of the handbook page, section "不合并权重，批量计算").
  *   buf: device fp32 [n_slices, num_tokens, r_max] or NULL. When non-NULL it
  *        also receives the shrink result. It must be non-NULL when any
  *        segment runs in the SGMV family (kind LORA_SGMV, or LORA_AUTO on a
  *        bf16 table), which goes through the buffer.
+ *   ws, ws_bytes: scratch as for lora_shrink.
  * Other arguments and errors as lora_shrink / lora_expand.
  */
 int lora_apply(const lora_layer_desc *desc, const lora_meta *meta, const void *x, int64_t ldx, float *buf,
-               void *y, int64_t ldy, int32_t y_dtype, int32_t kind, lora_stream_t stream);
+               void *y, int64_t ldy, int32_t y_dtype, int32_t kind, void *ws, size_t ws_bytes,
+               lora_stream_t stream);
 
-/* Scratch bytes lora_shrink needs for this layer and token bound (0: none). */
+/* Scratch bytes lora_shrink / lora_apply need for this layer and up to
+ * max_tokens tokens (0: none); 0 for an invalid desc. */
 size_t lora_workspace_bytes(const lora_layer_desc *desc, int32_t max_tokens, int32_t kind);
 
 /* Bytes the meta->tiles work-list buffer needs for a table of num_slots slots. */

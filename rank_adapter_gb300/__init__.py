@@ -27,7 +27,7 @@ __all__ = [
     "LayerDesc", "Meta", "LoraError", "lib_path", "exported_symbols",
     "lora_set_slot", "lora_reset_slot", "lora_prepare_meta", "lora_shrink", "lora_expand", "lora_apply",
     "lora_workspace_bytes", "lora_meta_tiles_bytes", "lora_query_status", "lora_strerror",
-    "lora_last_cuda_error", "SlotTable", "TokenMeta", "shrink", "expand", "apply", "check",
+    "lora_last_cuda_error", "SlotTable", "TokenMeta", "shrink", "expand", "apply", "workspace", "check",
 ]
 
 LORA_OK, LORA_EINVAL, LORA_ERANGE, LORA_EALIGN, LORA_EUNSUPPORTED, LORA_ECUDA, LORA_EBADSLOT = range(7)
@@ -85,7 +85,8 @@ _sig = {
     "lora_prepare_meta": (_i32, [_P(Meta), _vp]),
     "lora_shrink": (_i32, [_P(LayerDesc), _P(Meta), _vp, ctypes.c_int64, _vp, _i32, _vp, ctypes.c_size_t, _vp]),
     "lora_expand": (_i32, [_P(LayerDesc), _P(Meta), _vp, _vp, ctypes.c_int64, _i32, _i32, _vp]),
-    "lora_apply": (_i32, [_P(LayerDesc), _P(Meta), _vp, ctypes.c_int64, _vp, _vp, ctypes.c_int64, _i32, _i32, _vp]),
+    "lora_apply": (_i32, [_P(LayerDesc), _P(Meta), _vp, ctypes.c_int64, _vp, _vp, ctypes.c_int64, _i32, _i32, _vp,
+                          ctypes.c_size_t, _vp]),
     "lora_workspace_bytes": (ctypes.c_size_t, [_P(LayerDesc), _i32, _i32]),
     "lora_meta_tiles_bytes": (ctypes.c_size_t, [_i32]),
     "lora_query_status": (_i32, [_P(Meta), _P(_i32), _vp]),
@@ -157,9 +158,9 @@ def lora_expand(desc: LayerDesc, meta: Meta, buf: int, y: int, ldy: int, y_dtype
 
 
 def lora_apply(desc: LayerDesc, meta: Meta, x: int, ldx: int, buf: int, y: int, ldy: int, y_dtype: int,
-               kind: int = LORA_AUTO, stream=None) -> int:
+               kind: int = LORA_AUTO, ws: int = 0, ws_bytes: int = 0, stream=None) -> int:
     return _lib.lora_apply(ctypes.byref(desc), ctypes.byref(meta), x, ldx, buf or None, y, ldy, y_dtype, kind,
-                           _stream(stream))
+                           ws or None, ws_bytes, _stream(stream))
 
 
 def lora_workspace_bytes(desc: LayerDesc, max_tokens: int, kind: int = LORA_AUTO) -> int:
@@ -288,10 +289,27 @@ class TokenMeta:
         return self.scalars[2]
 
 
+def workspace(table: SlotTable, max_tokens: int, kind: int = LORA_AUTO, device="cuda"):
+    """A caller-owned scratch tensor of lora_workspace_bytes() bytes (None when 0)."""
+    import torch
+    nb = lora_workspace_bytes(table.desc, max_tokens, kind)
+    return torch.empty((nb + 15) // 16 * 4, dtype=torch.float32, device=device) if nb else None
+
+
+def _ws_args(table, meta, kind, ws):
+    if ws is None:
+        ws = workspace(table, meta.c.num_tokens, kind)
+    if ws is None:
+        return 0, 0, None
+    return ws.data_ptr(), ws.numel() * ws.element_size(), ws
+
+
 def shrink(table: SlotTable, meta: TokenMeta, x, buf, kind: int = LORA_AUTO, stream=None,
            ws=None) -> None:
-    """buf[s, t, :] = scale * x[t] @ A_s[slot t] for LoRA tokens (see lora_shrink)."""
-    wsp, wsb = (ws.data_ptr(), ws.numel() * ws.element_size()) if ws is not None else (0, 0)
+    """buf[s, t, :] = scale * x[t] @ A_s[slot t] for LoRA tokens (see lora_shrink).
+
+    ws: scratch from workspace(); allocated per call when omitted."""
+    wsp, wsb, _keep = _ws_args(table, meta, kind, ws)
     check(lora_shrink(table.desc, meta.c, x.data_ptr(), x.stride(0), buf.data_ptr(), kind, wsp, wsb, stream),
           "lora_shrink")
 
@@ -304,9 +322,13 @@ def expand(table: SlotTable, meta: TokenMeta, buf, y, kind: int = LORA_AUTO, str
           "lora_expand")
 
 
-def apply(table: SlotTable, meta: TokenMeta, x, y, buf=None, kind: int = LORA_AUTO, stream=None) -> None:
-    """Fused shrink + expand: y[t, off_s:] += (scale * x[t] @ A_s) @ B_s (see lora_apply)."""
+def apply(table: SlotTable, meta: TokenMeta, x, y, buf=None, kind: int = LORA_AUTO, stream=None,
+          ws=None) -> None:
+    """Fused shrink + expand: y[t, off_s:] += (scale * x[t] @ A_s) @ B_s (see lora_apply).
+
+    ws: scratch from workspace(); allocated per call when omitted."""
     import torch
     ydt = LORA_BF16 if y.dtype == torch.bfloat16 else LORA_F32
+    wsp, wsb, _keep = _ws_args(table, meta, kind, ws)
     check(lora_apply(table.desc, meta.c, x.data_ptr(), x.stride(0), buf.data_ptr() if buf is not None else 0,
-                     y.data_ptr(), y.stride(0), ydt, kind, stream), "lora_apply")
+                     y.data_ptr(), y.stride(0), ydt, kind, wsp, wsb, stream), "lora_apply")

@@ -5,21 +5,22 @@
 // Decode is bound by reading each active adapter's A and B once from HBM
 // (page "vLLM 源码完全拆解(十八): 多 LoRA 服务", section "成本与边界": about
 // 2 r (d_in + d_out) extra elements per layer), so the kernels are organised
-// around the weights. A work unit is one (segment, slice) and one CTA owns
-// it whole: no split of d_in, so no cross-CTA reduction, no cluster barrier
-// and no scratch. Its A rows (with the matching x columns of the tile's 4
-// tokens) stream through a three-buffer ring of 16-byte cp.async copies; the
-// first B pass is in flight during the whole shrink and later B passes are
-// double-buffered; the tile's y rows are pulled into L2 at CTA start.
+// around the weights, in small uniform CTAs that keep every SM streaming:
 //
-// Arithmetic: a thread owns one 16-byte vector column of A and a set of
-// row pairs; it widens each weight once and feeds all 4 tokens with packed
-// fp32x2 FMAs (even rows in one lane of the pair, odd rows in the other).
-// Row groups combine by a recursive-halving shuffle reduce-scatter and a
-// fixed-order sum over warps, so results are deterministic. The expand runs
-// the same way over pairs of rank indices and 4 output columns per thread.
-// Shrink + expand (split path) and the fused apply share this arithmetic and
-// give bitwise identical outputs.
+// * shrink: one CTA per (segment, slice, chunk of d_in rows of 32 KB of A).
+//   All of its A rows and the matching x columns of the tile's 4 tokens are
+//   requested at once with 16-byte cp.async copies; a thread widens a
+//   16-byte weight vector once and feeds the 4 tokens with packed fp32x2
+//   FMAs; row groups combine by a recursive-halving shuffle reduce-scatter
+//   and a fixed-order sum over warps. With one chunk the CTA writes the
+//   scaled rank-r rows u = s * x A; with several it writes unscaled partial
+//   rows to a caller-provided workspace.
+// * expand: one CTA per (segment, slice, column chunk of 32 KB of B). It
+//   forms u by summing the chunk partials in chunk order (or reads u), then
+//   adds u B into y with packed FMAs over pairs of rank indices.
+// * reduce: for the split path, turns the partials into the u buffer with
+//   the same arithmetic, so shrink + expand and the fused apply (shrink +
+//   expand-from-partials, two launches) give bitwise identical results.
 #include <utility>
 
 #include "common.cuh"
@@ -30,17 +31,19 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kTT = 4;               // tokens per tile
-constexpr int kAStageBytes = 16384;  // A bytes per ring buffer
-constexpr int kRing = 3;             // A ring buffers
-constexpr int kBPassBytes = 32768;   // B bytes per pass buffer
+constexpr int kAStageBytes = 16384;  // A bytes per stretch
+constexpr int kStretches = 2;        // stretches per shrink CTA (all in flight at once)
+constexpr int kBPassBytes = 32768;   // B bytes per expand CTA
 constexpr int kSmallTable = 256;     // slot tables up to this size: rank / scale copied whole
 
 struct Geo {
   int d_in, r_max;
-  int sc;                 // A rows per ring buffer (multiple of 8)
-  int pw;                 // B columns per pass (multiple of 8)
-  int a_stage, x_stage;   // bytes of the A and x parts of one ring buffer
-  int off_rs, off_ring, off_b0, off_red, off_u, off_rows, smem;
+  int sc;                 // A rows per stretch (multiple of 8)
+  int kchunk, kc_count;   // d_in rows per shrink CTA, and chunks per unit
+  int pw;                 // B columns per expand CTA (multiple of 8)
+  int a_stage, x_stage;   // bytes of the A and x parts of one stretch buffer
+  int off_rs, off_rows, off_u, off_ring, off_red, off_b;
+  int smem_shrink, smem_expand, smem_reduce;
 };
 
 struct BgmvArgs {
@@ -48,14 +51,16 @@ struct BgmvArgs {
   int64_t ldx;
   const void *A[LORA_MAX_SLICES];
   const void *B[LORA_MAX_SLICES];
-  const float *buf_in;  // standalone expand: u rows written by the shrink
-  float *buf;           // shrink / apply: receives u rows (apply: may be null)
+  float *buf;           // shrink: receives u rows (one chunk) ; reduce: receives u rows
+  float *part;          // shrink: receives chunk partials (several chunks)
+  const float *u_in;    // expand / reduce: chunk partials or u rows
+  int u_parts;          // expand: u_in holds chunk partials
   void *y;
   int64_t ldy;
   int out_sizes[LORA_MAX_SLICES];
   int out_off[LORA_MAX_SLICES];
   int slice_order[LORA_MAX_SLICES];      // slices by decreasing width: heavy units launch first
-  int chunk_start[LORA_MAX_SLICES + 1];  // standalone expand: column chunks per slice
+  int chunk_start[LORA_MAX_SLICES + 1];  // expand: column chunks per slice
   int n_slices, max_items;
   MetaView mv;
   int list;  // int offset of the unit-record list inside the work lists
@@ -229,12 +234,12 @@ __device__ __forceinline__ void expand_pass(const TW *Bs, int pw, const float *u
   }
 }
 
-// Shrink (kApply = false) or fused shrink + expand (kApply = true), one CTA
-// per unit. Grid: max_items * n_slices; block -> (slice_order[b / max_items], item b % max_items).
-template <typename TW, typename TY, int NV, bool kApply>
-__global__ void __launch_bounds__(kThreads, 2) bgmv_kernel(BgmvArgs a) {
+// Shrink. Grid: (max_items * n_slices, kc_count); block (b, c) -> unit
+// (slice_order[b / max_items], item b % max_items), rows [c * kchunk, +kchunk).
+template <typename TW, int NV>
+__global__ void __launch_bounds__(kThreads, 3) bgmv_shrink_kernel(BgmvArgs a) {
   constexpr int VEC = Elem<TW>::kVec;
-  constexpr int NRG = kThreads / NV;    // row-pair groups
+  constexpr int NRG = kThreads / NV;    // row groups
   constexpr int NVAL = kTT * VEC;       // accumulators per thread
   constexpr int LPV = 32 / NV;          // lanes sharing one vector column
   constexpr int NKEEP = NVAL / (LPV > NVAL ? NVAL : LPV);
@@ -244,6 +249,7 @@ __global__ void __launch_bounds__(kThreads, 2) bgmv_kernel(BgmvArgs a) {
   const Geo &g = a.g;
   const int item = (int)blockIdx.x % a.max_items;
   const int slice = a.slice_order[blockIdx.x / a.max_items];
+  const int kc = blockIdx.y;
   int *rows = reinterpret_cast<int *>(smem + g.off_rows);
   Unit u;
   if (!load_unit(a, item, u, smem, rows)) return;
@@ -251,50 +257,16 @@ __global__ void __launch_bounds__(kThreads, 2) bgmv_kernel(BgmvArgs a) {
   const int v = tid % NV, rq = tid / NV;
   const int r_max = g.r_max;
   const int nva = (u.r_a + VEC - 1) / VEC;
-  const int ns = (g.d_in + g.sc - 1) / g.sc;  // A stretches
-  const TW *Aslot = static_cast<const TW *>(a.A[slice]) + (int64_t)u.slot * g.d_in * r_max;
+  const int k0 = kc * g.kchunk;
+  const int klen = min(g.kchunk, g.d_in - k0);
+  const int nst = (klen + g.sc - 1) / g.sc;  // stretches of this chunk (<= kStretches)
+  const TW *Aslot = static_cast<const TW *>(a.A[slice]) + ((int64_t)u.slot * g.d_in + k0) * r_max;
   const TW *x = static_cast<const TW *>(a.x);
-  TY *y = static_cast<TY *>(a.y);
-  const int out_s = a.out_sizes[slice];
-  const TW *Bslot = static_cast<const TW *>(a.B[slice]) + (int64_t)u.slot * r_max * out_s;
-  const int r_pad = (u.r_a + 1) & ~1;
-  const int npass = (out_s + g.pw - 1) / g.pw;
   float *wred = reinterpret_cast<float *>(smem + g.off_red);  // [kWarps][kTT][r_max]
-  float *us = reinterpret_cast<float *>(smem + g.off_u);      // [kTT][r_max]
-  auto ringA = [&](int b) { return reinterpret_cast<TW *>(smem + g.off_ring + b * (g.a_stage + g.x_stage)); };
-  auto ringX = [&](int b) {
+  auto stA = [&](int b) { return reinterpret_cast<TW *>(smem + g.off_ring + b * (g.a_stage + g.x_stage)); };
+  auto stX = [&](int b) {
     return reinterpret_cast<TW *>(smem + g.off_ring + b * (g.a_stage + g.x_stage) + g.a_stage);
   };
-  // B pass p lives in b0 (even p) or at the start of the A ring (odd p; the ring is idle by then).
-  auto bufB = [&](int p) { return reinterpret_cast<TW *>(smem + ((p & 1) ? g.off_ring : g.off_b0)); };
-
-  int committed = 0;
-  auto commit = [&]() {
-    cp_async_commit();
-    return committed++;
-  };
-  // A rows [s * sc, +nr) and the matching x columns of tokens [0, nt) into ring buffer b.
-  auto issue_stretch = [&](int s, int b, int nt) {
-    const int r0 = s * g.sc, nr = min(g.sc, g.d_in - r0);
-    const uint4 *src = reinterpret_cast<const uint4 *>(Aslot + (int64_t)r0 * r_max);
-    uint4 *dst = reinterpret_cast<uint4 *>(ringA(b));
-    for (int i = tid; i < nr * NV; i += kThreads)
-      if ((i & (NV - 1)) < nva) cp_async16(dst + i, src + i);
-    const int upr = nr / VEC;
-    TW *xs = ringX(b);
-    for (int t = warp; t < nt; t += kWarps) {
-      const TW *xsrc = x + (int64_t)rows[t] * a.ldx + r0;
-      for (int c = tid & 31; c < upr; c += 32) cp_async16(xs + t * g.sc + c * VEC, xsrc + c * VEC);
-    }
-  };
-  auto issue_pass = [&](int p) {
-    const int pc0 = p * g.pw;
-    TW *Bs = bufB(p);
-    issue_b<TW>(Bs, g.pw, Bslot, out_s, u.r_a, pc0, min(g.pw, out_s - pc0));
-    if (r_pad > u.r_a)  // odd rank: the partner row of the last pair is zero
-      for (int c = tid; c < g.pw; c += kThreads) Bs[u.r_a * g.pw + c] = Elem<TW>::from_f(0.f);
-  };
-
   const int ntiles = (u.cnt + kTT - 1) / kTT;
   for (int tile = 0; tile < ntiles; ++tile) {
     const int nt = min(kTT, u.cnt - tile * kTT);
@@ -303,53 +275,54 @@ __global__ void __launch_bounds__(kThreads, 2) bgmv_kernel(BgmvArgs a) {
       if (tid < nt) rows[tid] = a.mv.sorted_rows[u.start + tile * kTT + tid];
       __syncthreads();
     }
-    // Prologue: up to kRing A stretches, then (fused) the first B pass, and the y rows into L2.
-    int gs0 = -1, gs1 = -1, gs2 = -1;
-    if (ns > 0) { issue_stretch(0, 0, nt); gs0 = commit(); }
-    if (ns > 1) { issue_stretch(1, 1, nt); gs1 = commit(); }
-    if (ns > 2) { issue_stretch(2, 2, nt); gs2 = commit(); }
-    if constexpr (kApply) {
-      if (tile == 0 || npass > 1) { issue_pass(0); commit(); }
-      if (tid < nt) prefetch_l2(y + (int64_t)rows[tid] * a.ldy + a.out_off[slice], (uint32_t)(out_s * sizeof(TY)));
+    // Every stretch of the chunk in flight at once (one commit group each).
+    for (int s = 0; s < nst; ++s) {
+      const int r0 = s * g.sc, nr = min(g.sc, klen - r0);
+      const uint4 *src = reinterpret_cast<const uint4 *>(Aslot + (int64_t)r0 * r_max);
+      uint4 *dst = reinterpret_cast<uint4 *>(stA(s));
+      for (int i = tid; i < nr * NV; i += kThreads)
+        if ((i & (NV - 1)) < nva) cp_async16(dst + i, src + i);
+      const int upr = nr / VEC;
+      TW *xs = stX(s);
+      for (int t = warp; t < nt; t += kWarps) {
+        const TW *xsrc = x + (int64_t)rows[t] * a.ldx + k0 + r0;
+        for (int c = tid & 31; c < upr; c += 32) cp_async16(xs + t * g.sc + c * VEC, xsrc + c * VEC);
+      }
+      cp_async_commit();
     }
-
-    float2 acc2[NVAL];
+    float2 acc2[NVAL / 2];  // (acc[t][2p], acc[t][2p + 1]) at t * VEC / 2 + p
 #pragma unroll
-    for (int i = 0; i < NVAL; ++i) acc2[i] = make_float2(0.f, 0.f);
-    for (int s = 0; s < ns; ++s) {
-      const int b = s % kRing;
-      cp_async_wait_upto(committed - 1 - (b == 0 ? gs0 : b == 1 ? gs1 : gs2));
+    for (int i = 0; i < NVAL / 2; ++i) acc2[i] = make_float2(0.f, 0.f);
+    for (int s = 0; s < nst; ++s) {
+      cp_async_wait_upto(nst - 1 - s);
       __syncthreads();
       if (v < nva) {
-        const int nr = min(g.sc, g.d_in - s * g.sc);
-        const TW *As = ringA(b) + v * VEC;
-        const TW *xs = ringX(b);
-#pragma unroll 2
-        for (int j = 2 * rq; j < nr; j += 2 * NRG) {
-          float a0[VEC], a1[VEC];
-          widen16<TW>(*reinterpret_cast<const uint4 *>(As + j * r_max), a0);
-          widen16<TW>(*reinterpret_cast<const uint4 *>(As + (j + 1) * r_max), a1);
+        const int nr = min(g.sc, klen - s * g.sc);
+        const TW *As = stA(s) + v * VEC;
+        const TW *xs = stX(s);
+#pragma unroll 4
+        for (int j = rq; j < nr; j += NRG) {
+          float w[VEC];
+          widen16<TW>(*reinterpret_cast<const uint4 *>(As + j * r_max), w);
 #pragma unroll
           for (int t = 0; t < kTT; ++t) {
-            const float2 x2 = load2(xs + t * g.sc + j);
+            const float xt = Elem<TW>::to_f(xs[t * g.sc + j]);
+            const float2 xx = make_float2(xt, xt);
 #pragma unroll
-            for (int e = 0; e < VEC; ++e)
-              acc2[t * VEC + e] = __ffma2_rn(x2, make_float2(a0[e], a1[e]), acc2[t * VEC + e]);
+            for (int p = 0; p < VEC / 2; ++p)
+              acc2[t * (VEC / 2) + p] = __ffma2_rn(xx, make_float2(w[2 * p], w[2 * p + 1]), acc2[t * (VEC / 2) + p]);
           }
         }
       }
-      if (s + kRing < ns) {
-        __syncthreads();  // buffer b is free again
-        issue_stretch(s + kRing, b, nt);
-        const int gnew = commit();
-        if (b == 0) gs0 = gnew; else if (b == 1) gs1 = gnew; else gs2 = gnew;
-      }
     }
-    // Even + odd rows, then row groups (in-warp), then warps in order. Entries
-    // of absent tokens (t >= nt) carry garbage and are masked below.
+    // Row groups (in-warp), then warps in order. Entries of absent tokens
+    // (t >= nt) carry garbage and are never written out.
     float acc[NVAL];
 #pragma unroll
-    for (int i = 0; i < NVAL; ++i) acc[i] = acc2[i].x + acc2[i].y;
+    for (int i = 0; i < NVAL / 2; ++i) {
+      acc[2 * i] = acc2[i].x;
+      acc[2 * i + 1] = acc2[i].y;
+    }
     const int off = reduce_scatter<NVAL, NV>(acc);
 #pragma unroll
     for (int i = 0; i < NKEEP; ++i) {
@@ -357,37 +330,51 @@ __global__ void __launch_bounds__(kThreads, 2) bgmv_kernel(BgmvArgs a) {
       wred[(warp * kTT + t) * r_max + v * VEC + e] = acc[i];
     }
     __syncthreads();
-    for (int i = tid; i < kTT * r_max; i += kThreads) {
+    for (int i = tid; i < nt * r_max; i += kThreads) {
       const int t = i / r_max, k = i - t * r_max;
       float sum = 0.f;
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) sum += wred[w * kTT * r_max + i];
-      const float val = (k < u.r_a && t < nt) ? u.scale * sum : 0.f;
-      us[i] = val;
-      if (t < nt && a.buf != nullptr) a.buf[((int64_t)slice * a.mv.num_tokens + rows[t]) * r_max + k] = val;
-    }
-    if constexpr (kApply) {
-      for (int p = 0; p < npass; ++p) {
-        if (p + 1 < npass) {
-          __syncthreads();  // the buffer of pass p + 1 is no longer read
-          issue_pass(p + 1);
-          commit();
-          cp_async_wait_upto(1);  // everything but pass p + 1 has landed
-        } else {
-          cp_async_wait_upto(0);
-        }
-        __syncthreads();
-        expand_pass<TW, TY>(bufB(p), g.pw, us, r_max, r_pad, rows, nt, y, a.ldy, a.out_off[slice] + p * g.pw,
-                            min(g.pw, out_s - p * g.pw));
+      for (int w2 = 0; w2 < kWarps; ++w2) sum += wred[w2 * kTT * r_max + i];
+      if (g.kc_count == 1) {
+        a.buf[((int64_t)slice * a.mv.num_tokens + rows[t]) * r_max + k] = k < u.r_a ? u.scale * sum : 0.f;
+      } else {
+        const int64_t pos = (int64_t)slice * a.mv.num_tokens + u.start + tile * kTT + t;
+        a.part[(pos * g.kc_count + kc) * r_max + k] = sum;
       }
     }
-    __syncthreads();  // rows / us / ring / B buffers are reused by the next tile
+    __syncthreads();  // rows / wred / ring are reused by the next tile
   }
-  cp_async_wait_upto(0);
 }
 
-// Standalone expand: one CTA per (segment, slice, column chunk of pw).
-// Grid: (chunks over all slices, max_items).
+// u[t][k] of token `pos` (sorted position) from the chunk partials, summed in chunk order.
+__device__ __forceinline__ float u_from_partials(const BgmvArgs &a, int slice, int pos, int k, const Unit &u) {
+  if (k >= u.r_a) return 0.f;
+  const float *p = a.u_in + (((int64_t)slice * a.mv.num_tokens + pos) * a.g.kc_count) * a.g.r_max + k;
+  float sum = 0.f;
+  for (int c = 0; c < a.g.kc_count; ++c) sum += p[c * a.g.r_max];
+  return u.scale * sum;
+}
+
+// Split path: u rows of every token of a unit from its chunk partials. Grid: max_items * n_slices.
+__global__ void __launch_bounds__(kThreads) bgmv_reduce_kernel(BgmvArgs a) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  pdl_wait();
+  pdl_trigger();
+  const int item = (int)blockIdx.x % a.max_items;
+  const int slice = a.slice_order[blockIdx.x / a.max_items];
+  int *rows = reinterpret_cast<int *>(smem + a.g.off_rows);
+  Unit u;
+  if (!load_unit(a, item, u, smem, rows)) return;
+  const int r_max = a.g.r_max;
+  for (int i = threadIdx.x; i < u.cnt * r_max; i += kThreads) {
+    const int t = i / r_max, k = i - t * r_max;
+    const int row = a.mv.sorted_rows[u.start + t];
+    a.buf[((int64_t)slice * a.mv.num_tokens + row) * r_max + k] = u_from_partials(a, slice, u.start + t, k, u);
+  }
+}
+
+// Expand: one CTA per (segment, slice, column chunk of pw). Grid: (chunks over all slices, max_items).
+// u comes from the chunk partials (u_parts) or from the u buffer.
 template <typename TW, typename TY>
 __global__ void __launch_bounds__(kThreads, 4) bgmv_expand_kernel(BgmvArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
@@ -404,15 +391,14 @@ __global__ void __launch_bounds__(kThreads, 4) bgmv_expand_kernel(BgmvArgs a) {
   const int pcn = min(g.pw, out_s - pc0);
   const int r_max = g.r_max;
   const int r_pad = (u.r_a + 1) & ~1;
-  TW *Bs = reinterpret_cast<TW *>(smem + g.off_b0);
+  TW *Bs = reinterpret_cast<TW *>(smem + g.off_b);
   float *us = reinterpret_cast<float *>(smem + g.off_u);
   const TW *Bslot = static_cast<const TW *>(a.B[s]) + (int64_t)u.slot * r_max * out_s;
-  const float *bufs = a.buf_in + (int64_t)s * a.mv.num_tokens * r_max;
   TY *y = static_cast<TY *>(a.y);
   const int col_base = a.out_off[s] + pc0;
   issue_b<TW>(Bs, g.pw, Bslot, out_s, u.r_a, pc0, pcn);
   cp_async_commit();
-  if (r_pad > u.r_a)
+  if (r_pad > u.r_a)  // odd rank: the partner row of the last pair is zero
     for (int c = threadIdx.x; c < g.pw; c += kThreads) Bs[u.r_a * g.pw + c] = Elem<TW>::from_f(0.f);
   const int ntiles = (u.cnt + kTT - 1) / kTT;
   for (int tile = 0; tile < ntiles; ++tile) {
@@ -425,7 +411,12 @@ __global__ void __launch_bounds__(kThreads, 4) bgmv_expand_kernel(BgmvArgs a) {
     if (threadIdx.x < nt) prefetch_l2(y + (int64_t)rows[threadIdx.x] * a.ldy + col_base, (uint32_t)(pcn * sizeof(TY)));
     for (int i = threadIdx.x; i < kTT * r_max; i += kThreads) {
       const int t = i / r_max, k = i - t * r_max;
-      us[i] = (t < nt && k < u.r_a) ? bufs[(int64_t)rows[t] * r_max + k] : 0.f;
+      float val = 0.f;
+      if (t < nt) {
+        if (a.u_parts) val = u_from_partials(a, s, u.start + tile * kTT + t, k, u);
+        else if (k < u.r_a) val = a.u_in[((int64_t)s * a.mv.num_tokens + rows[t]) * r_max + k];
+      }
+      us[i] = val;
     }
     cp_async_wait_upto(0);
     __syncthreads();
@@ -435,8 +426,8 @@ __global__ void __launch_bounds__(kThreads, 4) bgmv_expand_kernel(BgmvArgs a) {
 
 int align16(int v) { return (v + 15) & ~15; }
 
-// Shared-memory geometry. mode: 0 shrink, 1 standalone expand, 2 fused apply.
-Geo make_geo(const lora_layer_desc &d, int mode) {
+// Geometry of the shrink and expand CTAs for a layer.
+Geo make_geo(const lora_layer_desc &d) {
   Geo g{};
   const int es = d.dtype == LORA_BF16 ? 2 : 4;
   g.d_in = d.d_in;
@@ -446,6 +437,8 @@ Geo make_geo(const lora_layer_desc &d, int mode) {
   if (sc < 8) sc = 8;
   if (sc > d.d_in) sc = d.d_in;
   g.sc = sc;
+  g.kchunk = kStretches * sc;
+  g.kc_count = (d.d_in + g.kchunk - 1) / g.kchunk;
   int pw = (kBPassBytes / row_bytes) & ~7;
   if (pw < 8) pw = 8;
   int max_out = 0;
@@ -454,27 +447,28 @@ Geo make_geo(const lora_layer_desc &d, int mode) {
   g.pw = pw;
   g.a_stage = align16(sc * row_bytes);
   g.x_stage = align16(kTT * sc * es);
-  const int b_stage = align16((d.r_max + 1) * pw * es);  // + the zero partner row of an odd rank
   int off = 0;
   g.off_rs = off;
   off += align16(2 * kSmallTable * 4);
-  g.off_ring = off;
-  int ring = mode == 1 ? 0 : kRing * (g.a_stage + g.x_stage);
-  if (mode == 2 && ring < b_stage) ring = b_stage;  // the odd B passes reuse the ring
-  off += ring;
-  g.off_b0 = off;
-  off += mode == 0 ? 0 : b_stage;
-  g.off_red = off;
-  off += mode == 1 ? 0 : align16(kWarps * kTT * d.r_max * 4);
-  g.off_u = off;
-  off += align16(kTT * d.r_max * 4);
   g.off_rows = off;
   off += align16(kTT * 4);
-  g.smem = off;
+  g.off_u = off;
+  off += align16(kTT * d.r_max * 4);
+  const int common = off;
+  // shrink: ring + reduction buffer
+  g.off_ring = off;
+  off += kStretches * (g.a_stage + g.x_stage);
+  g.off_red = off;
+  off += align16(kWarps * kTT * d.r_max * 4);
+  g.smem_shrink = off;
+  // expand: one B chunk (+ the zero partner row of an odd rank)
+  g.off_b = common;
+  g.smem_expand = common + align16((d.r_max + 1) * pw * es);
+  g.smem_reduce = common;
   return g;
 }
 
-void fill_common(BgmvArgs &a, const lora_layer_desc &d, const MetaView &mv, ListSel sel, int mode) {
+void fill_common(BgmvArgs &a, const lora_layer_desc &d, const MetaView &mv, ListSel sel) {
   a.list = WorkLists::list(mv.num_slots, sel);
   a.n_slices = d.n_slices;
   a.max_items = std::min(mv.num_slots - 1, mv.num_tokens);
@@ -493,93 +487,118 @@ void fill_common(BgmvArgs &a, const lora_layer_desc &d, const MetaView &mv, List
       std::swap(a.slice_order[j], a.slice_order[j - 1]);
   a.slot_rank = d.slot_rank;
   a.slot_scale = d.slot_scale;
-  a.g = make_geo(d, mode);
-}
-
-template <typename TW, typename TY, bool kApply, int NV>
-cudaError_t launch_nv(const BgmvArgs &a, cudaStream_t st) {
-  auto k = bgmv_kernel<TW, TY, NV, kApply>;
-  cudaError_t e = set_max_dynamic_smem((const void *)k, a.g.smem);
-  if (e != cudaSuccess) return e;
-  return launch_pdl(k, dim3((unsigned)(a.max_items * a.n_slices)), dim3(kThreads), (size_t)a.g.smem, st, 1u, a);
-}
-
-template <typename TW, typename TY, bool kApply>
-cudaError_t dispatch_nv(const BgmvArgs &a, int r_max, cudaStream_t st) {
-  const int nv = r_max / Elem<TW>::kVec;
-  if constexpr (sizeof(TW) == 2) {
-    switch (nv) {
-      case 1: return launch_nv<TW, TY, kApply, 1>(a, st);
-      case 2: return launch_nv<TW, TY, kApply, 2>(a, st);
-      case 4: return launch_nv<TW, TY, kApply, 4>(a, st);
-      case 8: return launch_nv<TW, TY, kApply, 8>(a, st);
-      case 16: return launch_nv<TW, TY, kApply, 16>(a, st);
-    }
-  } else {
-    switch (nv) {
-      case 2: return launch_nv<TW, TY, kApply, 2>(a, st);
-      case 4: return launch_nv<TW, TY, kApply, 4>(a, st);
-      case 8: return launch_nv<TW, TY, kApply, 8>(a, st);
-      case 16: return launch_nv<TW, TY, kApply, 16>(a, st);
-      case 32: return launch_nv<TW, TY, kApply, 32>(a, st);
-    }
-  }
-  return cudaErrorInvalidValue;
-}
-
-}  // namespace
-
-cudaError_t launch_bgmv_shrink(const lora_layer_desc &d, const MetaView &mv, ListSel sel,
-                               const void *x, int64_t ldx, float *buf, cudaStream_t st) {
-  if (std::min(mv.num_slots - 1, mv.num_tokens) <= 0) return cudaSuccess;
-  BgmvArgs a{};
-  fill_common(a, d, mv, sel, 0);
-  a.x = x;
-  a.ldx = ldx;
-  a.buf = buf;
-  if (d.dtype == LORA_BF16) return dispatch_nv<__nv_bfloat16, float, false>(a, d.r_max, st);
-  return dispatch_nv<float, float, false>(a, d.r_max, st);
-}
-
-cudaError_t launch_bgmv_apply(const lora_layer_desc &d, const MetaView &mv, ListSel sel, const void *x,
-                              int64_t ldx, float *buf, void *y, int64_t ldy, int y_dtype, cudaStream_t st) {
-  if (std::min(mv.num_slots - 1, mv.num_tokens) <= 0) return cudaSuccess;
-  BgmvArgs a{};
-  fill_common(a, d, mv, sel, 2);
-  a.x = x;
-  a.ldx = ldx;
-  a.buf = buf;
-  a.y = y;
-  a.ldy = ldy;
-  if (d.dtype == LORA_BF16) {
-    if (y_dtype == LORA_BF16) return dispatch_nv<__nv_bfloat16, __nv_bfloat16, true>(a, d.r_max, st);
-    return dispatch_nv<__nv_bfloat16, float, true>(a, d.r_max, st);
-  }
-  return dispatch_nv<float, float, true>(a, d.r_max, st);
-}
-
-cudaError_t launch_bgmv_expand(const lora_layer_desc &d, const MetaView &mv, ListSel sel,
-                               const float *buf, void *y, int64_t ldy, int y_dtype, cudaStream_t st) {
-  if (std::min(mv.num_slots - 1, mv.num_tokens) <= 0) return cudaSuccess;
-  BgmvArgs a{};
-  fill_common(a, d, mv, sel, 1);
-  a.buf_in = buf;
-  a.y = y;
-  a.ldy = ldy;
+  a.g = make_geo(d);
   int chunks = 0;
   for (int s = 0; s < d.n_slices; ++s) {
     a.chunk_start[s] = chunks;
     chunks += (d.out_sizes[s] + a.g.pw - 1) / a.g.pw;
   }
   a.chunk_start[d.n_slices] = chunks;
-  dim3 grid((unsigned)chunks, (unsigned)a.max_items);
-  void (*k)(BgmvArgs);
-  if (d.dtype == LORA_BF16 && y_dtype == LORA_BF16) k = bgmv_expand_kernel<__nv_bfloat16, __nv_bfloat16>;
-  else if (d.dtype == LORA_BF16) k = bgmv_expand_kernel<__nv_bfloat16, float>;
-  else k = bgmv_expand_kernel<float, float>;
-  cudaError_t e = set_max_dynamic_smem((const void *)k, a.g.smem);
+}
+
+template <typename TW, int NV>
+cudaError_t launch_shrink_nv(const BgmvArgs &a, cudaStream_t st) {
+  auto k = bgmv_shrink_kernel<TW, NV>;
+  cudaError_t e = set_max_dynamic_smem((const void *)k, a.g.smem_shrink);
   if (e != cudaSuccess) return e;
-  return launch_pdl(k, grid, dim3(kThreads), (size_t)a.g.smem, st, 1u, a);
+  return launch_pdl(k, dim3((unsigned)(a.max_items * a.n_slices), (unsigned)a.g.kc_count), dim3(kThreads),
+                    (size_t)a.g.smem_shrink, st, 1u, a);
+}
+
+template <typename TW>
+cudaError_t dispatch_shrink(const BgmvArgs &a, cudaStream_t st) {
+  const int nv = a.g.r_max / Elem<TW>::kVec;
+  if constexpr (sizeof(TW) == 2) {
+    switch (nv) {
+      case 1: return launch_shrink_nv<TW, 1>(a, st);
+      case 2: return launch_shrink_nv<TW, 2>(a, st);
+      case 4: return launch_shrink_nv<TW, 4>(a, st);
+      case 8: return launch_shrink_nv<TW, 8>(a, st);
+      case 16: return launch_shrink_nv<TW, 16>(a, st);
+    }
+  } else {
+    switch (nv) {
+      case 2: return launch_shrink_nv<TW, 2>(a, st);
+      case 4: return launch_shrink_nv<TW, 4>(a, st);
+      case 8: return launch_shrink_nv<TW, 8>(a, st);
+      case 16: return launch_shrink_nv<TW, 16>(a, st);
+      case 32: return launch_shrink_nv<TW, 32>(a, st);
+    }
+  }
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_expand(const BgmvArgs &a, int dtype, int y_dtype, cudaStream_t st) {
+  void (*k)(BgmvArgs);
+  if (dtype == LORA_BF16 && y_dtype == LORA_BF16) k = bgmv_expand_kernel<__nv_bfloat16, __nv_bfloat16>;
+  else if (dtype == LORA_BF16) k = bgmv_expand_kernel<__nv_bfloat16, float>;
+  else k = bgmv_expand_kernel<float, float>;
+  cudaError_t e = set_max_dynamic_smem((const void *)k, a.g.smem_expand);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(k, dim3((unsigned)a.chunk_start[a.n_slices], (unsigned)a.max_items), dim3(kThreads),
+                    (size_t)a.g.smem_expand, st, 1u, a);
+}
+
+}  // namespace
+
+size_t bgmv_workspace_bytes(const lora_layer_desc &d, int max_tokens) {
+  const Geo g = make_geo(d);
+  if (g.kc_count <= 1 || max_tokens <= 0) return 0;
+  return (size_t)d.n_slices * max_tokens * g.kc_count * d.r_max * sizeof(float);
+}
+
+cudaError_t launch_bgmv_shrink(const lora_layer_desc &d, const MetaView &mv, ListSel sel, const void *x,
+                               int64_t ldx, float *buf, float *ws, cudaStream_t st) {
+  if (std::min(mv.num_slots - 1, mv.num_tokens) <= 0) return cudaSuccess;
+  BgmvArgs a{};
+  fill_common(a, d, mv, sel);
+  a.x = x;
+  a.ldx = ldx;
+  a.buf = buf;
+  a.part = ws;
+  cudaError_t e = d.dtype == LORA_BF16 ? dispatch_shrink<__nv_bfloat16>(a, st) : dispatch_shrink<float>(a, st);
+  if (e != cudaSuccess || a.g.kc_count == 1) return e;
+  a.u_in = ws;
+  return launch_pdl(bgmv_reduce_kernel, dim3((unsigned)(a.max_items * a.n_slices)), dim3(kThreads),
+                    (size_t)a.g.smem_reduce, st, 1u, a);
+}
+
+cudaError_t launch_bgmv_apply(const lora_layer_desc &d, const MetaView &mv, ListSel sel, const void *x,
+                              int64_t ldx, float *buf, float *ws, void *y, int64_t ldy, int y_dtype,
+                              cudaStream_t st) {
+  if (std::min(mv.num_slots - 1, mv.num_tokens) <= 0) return cudaSuccess;
+  BgmvArgs a{};
+  fill_common(a, d, mv, sel);
+  a.x = x;
+  a.ldx = ldx;
+  a.part = ws;
+  a.buf = buf;
+  const bool parts = a.g.kc_count > 1;
+  cudaError_t e = d.dtype == LORA_BF16 ? dispatch_shrink<__nv_bfloat16>(a, st) : dispatch_shrink<float>(a, st);
+  if (e != cudaSuccess) return e;
+  if (parts && buf != nullptr) {  // the caller also wants the u rows
+    a.u_in = ws;
+    e = launch_pdl(bgmv_reduce_kernel, dim3((unsigned)(a.max_items * a.n_slices)), dim3(kThreads),
+                   (size_t)a.g.smem_reduce, st, 1u, a);
+    if (e != cudaSuccess) return e;
+  }
+  a.u_in = parts ? ws : buf;
+  a.u_parts = parts ? 1 : 0;
+  a.y = y;
+  a.ldy = ldy;
+  return launch_expand(a, d.dtype, y_dtype, st);
+}
+
+cudaError_t launch_bgmv_expand(const lora_layer_desc &d, const MetaView &mv, ListSel sel, const float *buf,
+                               void *y, int64_t ldy, int y_dtype, cudaStream_t st) {
+  if (std::min(mv.num_slots - 1, mv.num_tokens) <= 0) return cudaSuccess;
+  BgmvArgs a{};
+  fill_common(a, d, mv, sel);
+  a.u_in = buf;
+  a.u_parts = 0;
+  a.y = y;
+  a.ldy = ldy;
+  return launch_expand(a, d.dtype, y_dtype, st);
 }
 
 }  // namespace ra

@@ -76,6 +76,15 @@ int check_meta(const lora_meta *m) {
   return LORA_OK;
 }
 
+// The BGMV shrink keeps per-chunk partial rows in caller-provided scratch.
+int check_ws(const lora_layer_desc *d, const lora_meta *m, const void *ws, size_t ws_bytes) {
+  const size_t need = ra::bgmv_workspace_bytes(*d, m->num_tokens);
+  if (need == 0) return LORA_OK;
+  if (ws == nullptr || ws_bytes < need) return LORA_EINVAL;
+  if (!aligned16(ws)) return LORA_EALIGN;
+  return LORA_OK;
+}
+
 ra::MetaView view_of(const lora_meta *m) {
   ra::MetaView v;
   v.sorted_rows = m->sorted_rows;
@@ -116,10 +125,9 @@ size_t lora_meta_tiles_bytes(int32_t num_slots) {
 }
 
 size_t lora_workspace_bytes(const lora_layer_desc *desc, int32_t max_tokens, int32_t kind) {
-  (void)desc;
-  (void)max_tokens;
-  (void)kind;
-  return 0;  // split-K partials are reduced in distributed shared memory
+  (void)kind;  // every kind may route segments through the BGMV family
+  if (check_desc(desc) != LORA_OK || max_tokens <= 0) return 0;
+  return ra::bgmv_workspace_bytes(*desc, max_tokens);
 }
 
 int lora_set_slot(const lora_layer_desc *desc, int32_t slot, int32_t rank, float scale,
@@ -156,8 +164,6 @@ int lora_prepare_meta(const lora_meta *meta, lora_stream_t stream) {
 int lora_shrink(const lora_layer_desc *desc, const lora_meta *meta, const void *x, int64_t ldx,
                 float *buf, int32_t kind, void *ws, size_t ws_bytes, lora_stream_t stream) {
   clear_stale_error();
-  (void)ws;
-  (void)ws_bytes;
   int st = check_desc(desc);
   if (st != LORA_OK) return st;
   st = check_meta(meta);
@@ -169,13 +175,18 @@ int lora_shrink(const lora_layer_desc *desc, const lora_meta *meta, const void *
   if (x == nullptr || buf == nullptr) return LORA_EINVAL;
   if (ldx < desc->d_in) return LORA_EINVAL;
   if (!aligned16(x) || !aligned16(buf) || (ldx * (int64_t)elem_size(desc->dtype)) % 16 != 0) return LORA_EALIGN;
+  if (kind != LORA_SGMV) {
+    st = check_ws(desc, meta, ws, ws_bytes);
+    if (st != LORA_OK) return st;
+  }
   const ra::MetaView mv = view_of(meta);
   cudaStream_t s = (cudaStream_t)stream;
+  float *wsf = static_cast<float *>(ws);
   if (kind == LORA_BGMV || (kind == LORA_AUTO && !sgmv_available(desc)))
-    return cuda_status(ra::launch_bgmv_shrink(*desc, mv, ra::kListAll, x, ldx, buf, s));
+    return cuda_status(ra::launch_bgmv_shrink(*desc, mv, ra::kListAll, x, ldx, buf, wsf, s));
   if (kind == LORA_SGMV)
     return cuda_status(ra::launch_sgmv_shrink(*desc, mv, ra::kListAll, x, ldx, buf, s));
-  st = cuda_status(ra::launch_bgmv_shrink(*desc, mv, ra::kListSmall, x, ldx, buf, s));
+  st = cuda_status(ra::launch_bgmv_shrink(*desc, mv, ra::kListSmall, x, ldx, buf, wsf, s));
   if (st != LORA_OK) return st;
   return cuda_status(ra::launch_sgmv_shrink(*desc, mv, ra::kListLarge, x, ldx, buf, s));
 }
@@ -210,7 +221,8 @@ int lora_expand(const lora_layer_desc *desc, const lora_meta *meta, const float 
 }
 
 int lora_apply(const lora_layer_desc *desc, const lora_meta *meta, const void *x, int64_t ldx, float *buf,
-               void *y, int64_t ldy, int32_t y_dtype, int32_t kind, lora_stream_t stream) {
+               void *y, int64_t ldy, int32_t y_dtype, int32_t kind, void *ws, size_t ws_bytes,
+               lora_stream_t stream) {
   clear_stale_error();
   int st = check_desc(desc);
   if (st != LORA_OK) return st;
@@ -230,16 +242,21 @@ int lora_apply(const lora_layer_desc *desc, const lora_meta *meta, const void *x
   if (!aligned16(x) || !aligned16(y) || (buf != nullptr && !aligned16(buf)) ||
       (ldx * (int64_t)elem_size(desc->dtype)) % 16 != 0 || (ldy * (int64_t)elem_size(y_dtype)) % 16 != 0)
     return LORA_EALIGN;
+  if (kind != LORA_SGMV) {
+    st = check_ws(desc, meta, ws, ws_bytes);
+    if (st != LORA_OK) return st;
+  }
   const ra::MetaView mv = view_of(meta);
   cudaStream_t s = (cudaStream_t)stream;
+  float *wsf = static_cast<float *>(ws);
   if (!uses_sgmv)
-    return cuda_status(ra::launch_bgmv_apply(*desc, mv, ra::kListAll, x, ldx, buf, y, ldy, y_dtype, s));
+    return cuda_status(ra::launch_bgmv_apply(*desc, mv, ra::kListAll, x, ldx, buf, wsf, y, ldy, y_dtype, s));
   if (kind == LORA_SGMV) {
     st = cuda_status(ra::launch_sgmv_shrink(*desc, mv, ra::kListAll, x, ldx, buf, s));
     if (st != LORA_OK) return st;
     return cuda_status(ra::launch_sgmv_expand(*desc, mv, ra::kListAll, buf, y, ldy, y_dtype, s));
   }
-  st = cuda_status(ra::launch_bgmv_apply(*desc, mv, ra::kListSmall, x, ldx, buf, y, ldy, y_dtype, s));
+  st = cuda_status(ra::launch_bgmv_apply(*desc, mv, ra::kListSmall, x, ldx, buf, wsf, y, ldy, y_dtype, s));
   if (st != LORA_OK) return st;
   st = cuda_status(ra::launch_sgmv_shrink(*desc, mv, ra::kListLarge, x, ldx, buf, s));
   if (st != LORA_OK) return st;

@@ -128,7 +128,16 @@ def test_shrink_expand_validation(ra):
     m0 = _meta(ra, T=0)
     assert ra.lora_shrink(d, m0, 0, 64, 0, 1, 0, 0, 0) == ra.LORA_OK                   # T = 0: no-op
     assert ra.lora_expand(d, m0, 0, 0, 64, ra.LORA_BF16, 1, 0) == ra.LORA_OK
-    assert ra.lora_workspace_bytes(d, 1024, 0) == 0
+    assert ra.lora_workspace_bytes(d, 1024, 0) == 0        # d_in = 64: one chunk, no partials
+    big = _desc(ra, d_in=4096, n_slices=3)
+    nb = ra.lora_workspace_bytes(big, 256, 0)
+    assert nb > 0 and nb % 16 == 0
+    assert ra.lora_workspace_bytes(_desc(ra, r_max=12), 256, 0) == 0  # invalid desc
+    mb = _meta(ra, T=256, S=4)
+    assert ra.lora_shrink(big, mb, 0x5000, 4096, 0x6000, 1, 0, 0, 0) == ra.LORA_EINVAL        # no scratch
+    assert ra.lora_shrink(big, mb, 0x5000, 4096, 0x6000, 1, 0x7000, nb - 16, 0) == ra.LORA_EINVAL
+    assert ra.lora_shrink(big, mb, 0x5000, 4096, 0x6000, 1, 0x7008, nb, 0) == ra.LORA_EALIGN
+    assert ra.lora_apply(big, mb, 0x5000, 4096, 0, 0x8000, 16 * 4 * 3, ra.LORA_BF16, 1, 0, 0, 0) == ra.LORA_EINVAL
 
 
 def test_product_path_has_no_oracle_import():
