@@ -171,11 +171,11 @@ int lora_prepare_meta(const lora_meta *meta, lora_stream_t stream);
  *   buf: device fp32, [n_slices, num_tokens, r_max] contiguous; rows of
  *        slot-0 tokens are not written
  *   ws:  device scratch of at least lora_workspace_bytes(desc, num_tokens,
- *        kind) bytes, 16-byte aligned, caller-owned; may be NULL when that is
- *        0. The CUDA-core family splits d_in into chunks and keeps each
- *        chunk's partial rows there; its contents need no initialisation and
- *        are meaningless between calls. Calls that share a workspace must not
- *        overlap in time (order them on one stream).
+ *        kind) bytes, 16-byte aligned, caller-owned. The CUDA-core family
+ *        splits d_in into chunks and keeps each chunk's partial rows there;
+ *        its contents need no initialisation and are meaningless between
+ *        calls. Calls that share a workspace must not overlap in time (order
+ *        them on one stream).
  * bf16 inputs are multiplied exactly and accumulated in fp32 in a fixed
  * order (results do not depend on the batch's other tokens).
  */

@@ -12,9 +12,9 @@
 //   requested at once with 16-byte cp.async copies; a thread widens a
 //   16-byte weight vector once and feeds the 4 tokens with packed fp32x2
 //   FMAs; row groups combine by a recursive-halving shuffle reduce-scatter
-//   and a fixed-order sum over warps. With one chunk the CTA writes the
-//   scaled rank-r rows u = s * x A; with several it writes unscaled partial
-//   rows to a caller-provided workspace.
+//   and a fixed-order sum over warps. It writes unscaled partial rows to a
+//   caller-provided workspace (or, for lora_shrink with a single chunk, the
+//   scaled rank-r rows u = s * x A directly).
 // * expand: one CTA per (segment, slice, column chunk of 32 KB of B). It
 //   forms u by summing the chunk partials in chunk order (or reads u), then
 //   adds u B into y with packed FMAs over pairs of rank indices.
@@ -51,8 +51,9 @@ struct BgmvArgs {
   int64_t ldx;
   const void *A[LORA_MAX_SLICES];
   const void *B[LORA_MAX_SLICES];
-  float *buf;           // shrink: receives u rows (one chunk) ; reduce: receives u rows
-  float *part;          // shrink: receives chunk partials (several chunks)
+  float *buf;           // shrink (to_parts == 0) and reduce: receives u rows
+  float *part;          // shrink (to_parts == 1): receives chunk partials
+  int to_parts;
   const float *u_in;    // expand / reduce: chunk partials or u rows
   int u_parts;          // expand: u_in holds chunk partials
   void *y;
@@ -335,7 +336,7 @@ __global__ void __launch_bounds__(kThreads, 3) bgmv_shrink_kernel(BgmvArgs a) {
       float sum = 0.f;
 #pragma unroll
       for (int w2 = 0; w2 < kWarps; ++w2) sum += wred[w2 * kTT * r_max + i];
-      if (g.kc_count == 1) {
+      if (!a.to_parts) {
         a.buf[((int64_t)slice * a.mv.num_tokens + rows[t]) * r_max + k] = k < u.r_a ? u.scale * sum : 0.f;
       } else {
         const int64_t pos = (int64_t)slice * a.mv.num_tokens + u.start + tile * kTT + t;
@@ -543,7 +544,7 @@ cudaError_t launch_expand(const BgmvArgs &a, int dtype, int y_dtype, cudaStream_
 
 size_t bgmv_workspace_bytes(const lora_layer_desc &d, int max_tokens) {
   const Geo g = make_geo(d);
-  if (g.kc_count <= 1 || max_tokens <= 0) return 0;
+  if (max_tokens <= 0) return 0;
   return (size_t)d.n_slices * max_tokens * g.kc_count * d.r_max * sizeof(float);
 }
 
@@ -556,8 +557,9 @@ cudaError_t launch_bgmv_shrink(const lora_layer_desc &d, const MetaView &mv, Lis
   a.ldx = ldx;
   a.buf = buf;
   a.part = ws;
+  a.to_parts = a.g.kc_count > 1;  // one chunk: the CTA writes u rows itself
   cudaError_t e = d.dtype == LORA_BF16 ? dispatch_shrink<__nv_bfloat16>(a, st) : dispatch_shrink<float>(a, st);
-  if (e != cudaSuccess || a.g.kc_count == 1) return e;
+  if (e != cudaSuccess || !a.to_parts) return e;
   a.u_in = ws;
   return launch_pdl(bgmv_reduce_kernel, dim3((unsigned)(a.max_items * a.n_slices)), dim3(kThreads),
                     (size_t)a.g.smem_reduce, st, 1u, a);
@@ -573,17 +575,16 @@ cudaError_t launch_bgmv_apply(const lora_layer_desc &d, const MetaView &mv, List
   a.ldx = ldx;
   a.part = ws;
   a.buf = buf;
-  const bool parts = a.g.kc_count > 1;
+  a.to_parts = 1;  // the expand forms u from the partials; buf is optional
   cudaError_t e = d.dtype == LORA_BF16 ? dispatch_shrink<__nv_bfloat16>(a, st) : dispatch_shrink<float>(a, st);
   if (e != cudaSuccess) return e;
-  if (parts && buf != nullptr) {  // the caller also wants the u rows
-    a.u_in = ws;
+  a.u_in = ws;
+  if (buf != nullptr) {  // the caller also wants the u rows
     e = launch_pdl(bgmv_reduce_kernel, dim3((unsigned)(a.max_items * a.n_slices)), dim3(kThreads),
                    (size_t)a.g.smem_reduce, st, 1u, a);
     if (e != cudaSuccess) return e;
   }
-  a.u_in = parts ? ws : buf;
-  a.u_parts = parts ? 1 : 0;
+  a.u_parts = 1;
   a.y = y;
   a.ldy = ldy;
   return launch_expand(a, d.dtype, y_dtype, st);

@@ -76,7 +76,7 @@ int check_meta(const lora_meta *m) {
   return LORA_OK;
 }
 
-// The BGMV shrink keeps per-chunk partial rows in caller-provided scratch.
+// The BGMV family keeps per-chunk partial rows in caller-provided scratch.
 int check_ws(const lora_layer_desc *d, const lora_meta *m, const void *ws, size_t ws_bytes) {
   const size_t need = ra::bgmv_workspace_bytes(*d, m->num_tokens);
   if (need == 0) return LORA_OK;

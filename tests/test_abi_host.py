@@ -118,6 +118,7 @@ def test_shrink_expand_validation(ra):
     assert ra.lora_shrink(d, m, 0x5000, 60, 0x6000, 1, 0, 0, 0) == ra.LORA_EINVAL       # ldx < d_in
     assert ra.lora_shrink(d, m, 0x5008, 64, 0x6000, 1, 0, 0, 0) == ra.LORA_EALIGN
     assert ra.lora_shrink(d, m, 0x5000, 68, 0x6000, 1, 0, 0, 0) == ra.LORA_EALIGN       # ldx*2 % 16
+    assert ra.lora_shrink(d, m, 0x5000, 64, 0x6000, 1, 0, 0, 0) == ra.LORA_EINVAL       # no scratch
     m2 = _meta(ra, S=5)
     assert ra.lora_shrink(d, m2, 0x5000, 64, 0x6000, 1, 0, 0, 0) == ra.LORA_EINVAL      # slot count mismatch
     f = _desc(ra, dtype=ra.LORA_F32)
@@ -128,7 +129,8 @@ def test_shrink_expand_validation(ra):
     m0 = _meta(ra, T=0)
     assert ra.lora_shrink(d, m0, 0, 64, 0, 1, 0, 0, 0) == ra.LORA_OK                   # T = 0: no-op
     assert ra.lora_expand(d, m0, 0, 0, 64, ra.LORA_BF16, 1, 0) == ra.LORA_OK
-    assert ra.lora_workspace_bytes(d, 1024, 0) == 0        # d_in = 64: one chunk, no partials
+    assert ra.lora_workspace_bytes(d, 1024, 0) == 2 * 1024 * 1 * 16 * 4   # d_in = 64: one chunk
+    assert ra.lora_workspace_bytes(d, 0, 0) == 0
     big = _desc(ra, d_in=4096, n_slices=3)
     nb = ra.lora_workspace_bytes(big, 256, 0)
     assert nb > 0 and nb % 16 == 0
