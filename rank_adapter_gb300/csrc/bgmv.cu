@@ -64,7 +64,10 @@ struct BgmvArgs {
   int chunk_start[LORA_MAX_SLICES + 1];  // expand: column chunks per slice
   int n_slices, max_items;
   MetaView mv;
-  int list;  // int offset of the unit-record list inside the work lists
+  int list;      // int offset of the unit-record list inside the work lists
+  int slot_rec;  // int offset of that list's slot -> record index
+  int by_slot;   // shrink: grid rows are slots 1..S-1 (A prefetched before the wait)
+  int pre;       // expand: runs right behind this library's shrink / reduce
   const int32_t *slot_rank;
   const float *slot_scale;
   Geo g;
@@ -103,6 +106,18 @@ __device__ __forceinline__ bool load_unit(const BgmvArgs &a, int item, Unit &u, 
   u.r_a = min(max(rk, 0), a.g.r_max);
   u.scale = small_table ? scale_s[u.slot] : a.slot_scale[u.slot];
   return true;
+}
+
+// Record `idx` of the list (count, start, first rows -> rows[]) for a slot
+// whose rank and scale are already known.
+__device__ __forceinline__ void read_record(const BgmvArgs &a, int idx, Unit &u, int *rows) {
+  const int4 *rec = reinterpret_cast<const int4 *>(a.mv.work + a.list + idx * WorkLists::kRec);
+  const int4 h = rec[0], r = rec[1];
+  u.cnt = h.z;
+  u.start = h.w;
+  if (threadIdx.x < kTT)
+    rows[threadIdx.x] = threadIdx.x == 0 ? r.x : threadIdx.x == 1 ? r.y : threadIdx.x == 2 ? r.z : r.w;
+  __syncthreads();
 }
 
 // Widen bf16 / fp32 weights to fp32.
@@ -245,29 +260,59 @@ __global__ void __launch_bounds__(kThreads, 3) bgmv_shrink_kernel(BgmvArgs a) {
   constexpr int LPV = 32 / NV;          // lanes sharing one vector column
   constexpr int NKEEP = NVAL / (LPV > NVAL ? NVAL : LPV);
   extern __shared__ __align__(16) unsigned char smem[];
-  pdl_wait();
-  pdl_trigger();
   const Geo &g = a.g;
-  const int item = (int)blockIdx.x % a.max_items;
-  const int slice = a.slice_order[blockIdx.x / a.max_items];
   const int kc = blockIdx.y;
+  const int rows_per = a.by_slot ? a.mv.num_slots - 1 : a.max_items;
+  const int slice = a.slice_order[blockIdx.x / rows_per];
   int *rows = reinterpret_cast<int *>(smem + g.off_rows);
-  Unit u;
-  if (!load_unit(a, item, u, smem, rows)) return;
   const int tid = threadIdx.x, warp = tid >> 5;
   const int v = tid % NV, rq = tid / NV;
   const int r_max = g.r_max;
-  const int nva = (u.r_a + VEC - 1) / VEC;
   const int k0 = kc * g.kchunk;
   const int klen = min(g.kchunk, g.d_in - k0);
   const int nst = (klen + g.sc - 1) / g.sc;  // stretches of this chunk (<= kStretches)
-  const TW *Aslot = static_cast<const TW *>(a.A[slice]) + ((int64_t)u.slot * g.d_in + k0) * r_max;
   const TW *x = static_cast<const TW *>(a.x);
   float *wred = reinterpret_cast<float *>(smem + g.off_red);  // [kWarps][kTT][r_max]
   auto stA = [&](int b) { return reinterpret_cast<TW *>(smem + g.off_ring + b * (g.a_stage + g.x_stage)); };
   auto stX = [&](int b) {
     return reinterpret_cast<TW *>(smem + g.off_ring + b * (g.a_stage + g.x_stage) + g.a_stage);
   };
+  // All A stretches of this chunk in flight at once, rank tail skipped.
+  auto issue_a = [&](int slot, int nva) {
+    const TW *Aslot = static_cast<const TW *>(a.A[slice]) + ((int64_t)slot * g.d_in + k0) * r_max;
+    for (int s = 0; s < nst; ++s) {
+      const int r0 = s * g.sc, nr = min(g.sc, klen - r0);
+      const uint4 *src = reinterpret_cast<const uint4 *>(Aslot + (int64_t)r0 * r_max);
+      uint4 *dst = reinterpret_cast<uint4 *>(stA(s));
+      for (int i = tid; i < nr * NV; i += kThreads)
+        if ((i & (NV - 1)) < nva) cp_async16(dst + i, src + i);
+    }
+    cp_async_commit();
+  };
+  Unit u;
+  if (a.by_slot) {
+    // The slot table is complete before any kernel of this library starts
+    // (see pdl_wait), so this slot's A chunk streams in while the metadata
+    // kernel may still be running.
+    u.slot = 1 + (int)blockIdx.x % rows_per;
+    u.r_a = min(max(a.slot_rank[u.slot], 0), r_max);
+    u.scale = a.slot_scale[u.slot];
+    issue_a(u.slot, (u.r_a + VEC - 1) / VEC);
+    pdl_wait();
+    pdl_trigger();
+    const int ri = a.mv.work[a.slot_rec + u.slot];
+    if (ri < 0) {  // the slot has no tokens in this batch
+      cp_async_wait_upto(0);
+      return;
+    }
+    read_record(a, ri, u, rows);
+  } else {
+    pdl_wait();
+    pdl_trigger();
+    if (!load_unit(a, (int)blockIdx.x % rows_per, u, smem, rows)) return;
+    issue_a(u.slot, (u.r_a + VEC - 1) / VEC);
+  }
+  const int nva = (u.r_a + VEC - 1) / VEC;
   const int ntiles = (u.cnt + kTT - 1) / kTT;
   for (int tile = 0; tile < ntiles; ++tile) {
     const int nt = min(kTT, u.cnt - tile * kTT);
@@ -276,27 +321,23 @@ __global__ void __launch_bounds__(kThreads, 3) bgmv_shrink_kernel(BgmvArgs a) {
       if (tid < nt) rows[tid] = a.mv.sorted_rows[u.start + tile * kTT + tid];
       __syncthreads();
     }
-    // Every stretch of the chunk in flight at once (one commit group each).
+    // This tile's x columns for every stretch (the A chunk stays resident across tiles).
     for (int s = 0; s < nst; ++s) {
       const int r0 = s * g.sc, nr = min(g.sc, klen - r0);
-      const uint4 *src = reinterpret_cast<const uint4 *>(Aslot + (int64_t)r0 * r_max);
-      uint4 *dst = reinterpret_cast<uint4 *>(stA(s));
-      for (int i = tid; i < nr * NV; i += kThreads)
-        if ((i & (NV - 1)) < nva) cp_async16(dst + i, src + i);
       const int upr = nr / VEC;
       TW *xs = stX(s);
       for (int t = warp; t < nt; t += kWarps) {
         const TW *xsrc = x + (int64_t)rows[t] * a.ldx + k0 + r0;
         for (int c = tid & 31; c < upr; c += 32) cp_async16(xs + t * g.sc + c * VEC, xsrc + c * VEC);
       }
-      cp_async_commit();
     }
+    cp_async_commit();
+    cp_async_wait_upto(0);
+    __syncthreads();
     float2 acc2[NVAL / 2];  // (acc[t][2p], acc[t][2p + 1]) at t * VEC / 2 + p
 #pragma unroll
     for (int i = 0; i < NVAL / 2; ++i) acc2[i] = make_float2(0.f, 0.f);
     for (int s = 0; s < nst; ++s) {
-      cp_async_wait_upto(nst - 1 - s);
-      __syncthreads();
       if (v < nva) {
         const int nr = min(g.sc, klen - s * g.sc);
         const TW *As = stA(s) + v * VEC;
@@ -379,14 +420,22 @@ __global__ void __launch_bounds__(kThreads) bgmv_reduce_kernel(BgmvArgs a) {
 template <typename TW, typename TY>
 __global__ void __launch_bounds__(kThreads, 4) bgmv_expand_kernel(BgmvArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
-  pdl_wait();
-  pdl_trigger();
+  // Behind this library's shrink (or reduce), the metadata and the slot
+  // table are complete (see pdl_wait): the record, the B chunk and the y
+  // prefetch go out before the wait and overlap the shrink's tail.
+  if (!a.pre) {
+    pdl_wait();
+    pdl_trigger();
+  }
   const Geo &g = a.g;
   int s = 0;
   while (s + 1 < a.n_slices && (int)blockIdx.x >= a.chunk_start[s + 1]) ++s;
   int *rows = reinterpret_cast<int *>(smem + g.off_rows);
   Unit u;
-  if (!load_unit(a, blockIdx.y, u, smem, rows)) return;
+  if (!load_unit(a, blockIdx.y, u, smem, rows)) {
+    if (a.pre) pdl_wait();
+    return;
+  }
   const int out_s = a.out_sizes[s];
   const int pc0 = ((int)blockIdx.x - a.chunk_start[s]) * g.pw;
   const int pcn = min(g.pw, out_s - pc0);
@@ -401,6 +450,12 @@ __global__ void __launch_bounds__(kThreads, 4) bgmv_expand_kernel(BgmvArgs a) {
   cp_async_commit();
   if (r_pad > u.r_a)  // odd rank: the partner row of the last pair is zero
     for (int c = threadIdx.x; c < g.pw; c += kThreads) Bs[u.r_a * g.pw + c] = Elem<TW>::from_f(0.f);
+  if (a.pre) {
+    if (threadIdx.x < min(kTT, u.cnt))
+      prefetch_l2(y + (int64_t)rows[threadIdx.x] * a.ldy + col_base, (uint32_t)(pcn * sizeof(TY)));
+    pdl_wait();
+    pdl_trigger();
+  }
   const int ntiles = (u.cnt + kTT - 1) / kTT;
   for (int tile = 0; tile < ntiles; ++tile) {
     const int nt = min(kTT, u.cnt - tile * kTT);
@@ -471,6 +526,9 @@ Geo make_geo(const lora_layer_desc &d) {
 
 void fill_common(BgmvArgs &a, const lora_layer_desc &d, const MetaView &mv, ListSel sel) {
   a.list = WorkLists::list(mv.num_slots, sel);
+  a.slot_rec = WorkLists::slot_rec(mv.num_slots, sel);
+  // Slot-indexed shrink CTAs when most slots are likely live in this batch.
+  a.by_slot = mv.num_tokens >= mv.num_slots - 1 ? 1 : 0;
   a.n_slices = d.n_slices;
   a.max_items = std::min(mv.num_slots - 1, mv.num_tokens);
   a.mv = mv;
@@ -502,7 +560,8 @@ cudaError_t launch_shrink_nv(const BgmvArgs &a, cudaStream_t st) {
   auto k = bgmv_shrink_kernel<TW, NV>;
   cudaError_t e = set_max_dynamic_smem((const void *)k, a.g.smem_shrink);
   if (e != cudaSuccess) return e;
-  return launch_pdl(k, dim3((unsigned)(a.max_items * a.n_slices), (unsigned)a.g.kc_count), dim3(kThreads),
+  const int rows_per = a.by_slot ? a.mv.num_slots - 1 : a.max_items;
+  return launch_pdl(k, dim3((unsigned)(rows_per * a.n_slices), (unsigned)a.g.kc_count), dim3(kThreads),
                     (size_t)a.g.smem_shrink, st, 1u, a);
 }
 
@@ -585,6 +644,7 @@ cudaError_t launch_bgmv_apply(const lora_layer_desc &d, const MetaView &mv, List
     if (e != cudaSuccess) return e;
   }
   a.u_parts = 1;
+  a.pre = 1;
   a.y = y;
   a.ldy = ldy;
   return launch_expand(a, d.dtype, y_dtype, st);

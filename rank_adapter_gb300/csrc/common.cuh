@@ -134,14 +134,18 @@ __device__ __forceinline__ void cp_async_wait_upto(int n) {
 //   then three lists of S = num_slots unit records (all, small, large), each
 //   record 8 ints: {segment, slot, count, first sorted row, first 4 token rows}
 //   (rows past the count are -1; unused records are all -1),
-//   then all_tile_start[S+1] and large_tile_start[S+1] (cumulative tile counts).
+//   then all_tile_start[S+1] and large_tile_start[S+1] (cumulative tile counts),
+//   then for each list, slot_rec[S]: the index of slot s's record in that list, or -1.
 struct WorkLists {
   static constexpr int kHeader = 8;
   static constexpr int kRec = 8;
-  __host__ __device__ static inline size_t ints(int S) { return kHeader + 3 * (size_t)kRec * S + 2 * ((size_t)S + 1); }
+  __host__ __device__ static inline size_t ints(int S) {
+    return kHeader + 3 * (size_t)kRec * S + 2 * ((size_t)S + 1) + 3 * (size_t)S;
+  }
   __host__ __device__ static inline int list(int S, int which) { return kHeader + which * kRec * S; }
   __host__ __device__ static inline int all_tile_start(int S) { return kHeader + 3 * kRec * S; }
   __host__ __device__ static inline int large_tile_start(int S) { return kHeader + 3 * kRec * S + S + 1; }
+  __host__ __device__ static inline int slot_rec(int S, int which) { return kHeader + 3 * kRec * S + 2 * (S + 1) + which * S; }
 };
 
 enum ListSel { kListAll = 0, kListSmall = 1, kListLarge = 2 };
@@ -161,9 +165,16 @@ struct MetaView {
 // Every kernel of this library is launched with programmatic stream
 // serialization, so it may be scheduled while its predecessor on the stream
 // drains. Each kernel therefore waits for the predecessor's completion (and
-// memory flush) before its first global-memory access of any kind, and lets
-// its own successor be scheduled right away; only launch latency overlaps,
-// never data.
+// memory flush) before it touches data a predecessor may still be writing.
+// Protocol:
+// * the slot-write kernel never lets a successor start early, so the slot
+//   table (A, B, ranks, scales) is complete whenever a later kernel starts;
+// * other kernels trigger their successor only after their own wait, so when
+//   a kernel starts, everything older than its immediate predecessor is
+//   complete;
+// * a kernel reads before its wait only the slot table, and (the expand when
+//   launched right behind its own shrink) the metadata that is two launches
+//   old.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 

@@ -135,6 +135,9 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_meta_kernel(MetaArgs a) {
 
   int32_t *W = a.work;
   if (tid < S) {
+    W[WorkLists::slot_rec(S, kListAll) + tid] = lora ? ex[2] : -1;
+    W[WorkLists::slot_rec(S, kListSmall) + tid] = small ? ex[3] : -1;
+    W[WorkLists::slot_rec(S, kListLarge) + tid] = large ? ex[4] : -1;
     base_s[tid] = base;
     rec_a[tid] = lora ? WorkLists::list(S, kListAll) + ex[2] * R : -1;
     rec_k[tid] = small ? WorkLists::list(S, kListSmall) + ex[3] * R

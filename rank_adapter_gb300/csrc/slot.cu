@@ -25,8 +25,7 @@ struct SlotArgs {
 // destination elements with one vector store.
 template <typename T>
 __global__ void __launch_bounds__(256) slot_write_kernel(SlotArgs a) {
-  pdl_wait();
-  pdl_trigger();
+  pdl_wait();  // no early trigger: successors start only once the table is complete
   const int s = blockIdx.y >> 1;
   const bool isB = blockIdx.y & 1;
   if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {

@@ -37,7 +37,8 @@ def _work_lists(ref, S):
     """The work lists by their definition: LoRA segments (slot != 0), split at
     LORA_SGMV_MIN_ROWS, as 8-int records {segment, slot, count, start, first 4
     rows (-1 past the count)}, unused records all -1, then cumulative counts of
-    128-row tiles over all LoRA segments and over the large ones."""
+    128-row tiles over all LoRA segments and over the large ones, then per
+    list the record index of every slot (-1 when absent)."""
     import rank_adapter_gb300 as ra
     n = ref["num_segs"]
     slot, cnt, start, rows = ref["seg_slot"], ref["seg_count"], ref["seg_start"], ref["sorted_rows"]
@@ -60,8 +61,15 @@ def _work_lists(ref, S):
             c.append(c[-1] + (int(cnt[i]) + ra.LORA_SGMV_TILE_M - 1) // ra.LORA_SGMV_TILE_M)
         return c + [c[-1]] * (S + 1 - len(c))
 
+    def slot_index(L):
+        idx = [-1] * S
+        for j, i in enumerate(L):
+            idx[slot[i]] = j
+        return idx
+
     ca, cl = cum(segs), cum(large)
     w = [len(segs), len(small), len(large), ca[-1], cl[-1], 0, 0, 0] + lst(segs) + lst(small) + lst(large) + ca + cl
+    w += slot_index(segs) + slot_index(small) + slot_index(large)
     return np.asarray(w, np.int32)
 
 
