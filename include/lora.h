@@ -229,6 +229,34 @@ size_t lora_meta_tiles_bytes(int32_t num_slots);
  */
 int lora_query_status(const lora_meta *meta, int32_t *out, lora_stream_t stream);
 
+/*
+ * Allocation-free shrink. The multi-LoRA pages have no counterpart to this
+ * call; it exists for callers that cannot allocate device memory where they
+ * run the shrink (inside another framework's memory pool, under an allocator
+ * that forbids new device allocations, or on a serving path that must not
+ * call an allocator at all).
+ * Computes exactly what lora_shrink computes with kind LORA_BGMV (same
+ * arguments, same results), but keeps the per-chunk partial rows in a fixed
+ * 8 MiB array inside the library's device image instead of a caller
+ * workspace; the caller still owns x and buf. Every GPU that loads the
+ * library holds that array until the process exits.
+ * - The first call on a device looks up the array's device address (with
+ *   that device current) and caches it; make that first call before any
+ *   stream capture.
+ * - All calls share the one array and it keeps the last call's contents.
+ *   Nothing in it needs to start at zero. Calls whose kernels overlap on the
+ *   GPU (on different streams, or from different threads without ordering)
+ *   race on it: order them.
+ * - A layer and token count whose partial rows exceed
+ *   lora_noalloc_scratch_bytes() return LORA_ERANGE and launch nothing.
+ * - It never calls cudaMalloc, cudaFree or any allocating routine.
+ */
+int lora_shrink_noalloc(const lora_layer_desc *desc, const lora_meta *meta, const void *x, int64_t ldx,
+                        float *buf, lora_stream_t stream);
+
+/* Size in bytes of the fixed scratch array lora_shrink_noalloc uses. */
+size_t lora_noalloc_scratch_bytes(void);
+
 /* Static description of a lora_status value. */
 const char *lora_strerror(int status);
 

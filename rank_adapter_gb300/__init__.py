@@ -26,6 +26,7 @@ __all__ = [
     "LORA_MAX_SLICES", "LORA_MAX_NUM_SLOTS", "LORA_MAX_RANK", "LORA_SGMV_MIN_ROWS", "LORA_SGMV_TILE_M",
     "LayerDesc", "Meta", "LoraError", "lib_path", "exported_symbols",
     "lora_set_slot", "lora_reset_slot", "lora_prepare_meta", "lora_shrink", "lora_expand", "lora_apply",
+    "lora_shrink_noalloc", "lora_noalloc_scratch_bytes",
     "lora_workspace_bytes", "lora_meta_tiles_bytes", "lora_query_status", "lora_strerror",
     "lora_last_cuda_error", "SlotTable", "TokenMeta", "shrink", "expand", "apply", "workspace", "check",
 ]
@@ -87,6 +88,8 @@ _sig = {
     "lora_expand": (_i32, [_P(LayerDesc), _P(Meta), _vp, _vp, ctypes.c_int64, _i32, _i32, _vp]),
     "lora_apply": (_i32, [_P(LayerDesc), _P(Meta), _vp, ctypes.c_int64, _vp, _vp, ctypes.c_int64, _i32, _i32, _vp,
                           ctypes.c_size_t, _vp]),
+    "lora_shrink_noalloc": (_i32, [_P(LayerDesc), _P(Meta), _vp, ctypes.c_int64, _vp, _vp]),
+    "lora_noalloc_scratch_bytes": (ctypes.c_size_t, []),
     "lora_workspace_bytes": (ctypes.c_size_t, [_P(LayerDesc), _i32, _i32]),
     "lora_meta_tiles_bytes": (ctypes.c_size_t, [_i32]),
     "lora_query_status": (_i32, [_P(Meta), _P(_i32), _vp]),
@@ -161,6 +164,15 @@ def lora_apply(desc: LayerDesc, meta: Meta, x: int, ldx: int, buf: int, y: int, 
                kind: int = LORA_AUTO, ws: int = 0, ws_bytes: int = 0, stream=None) -> int:
     return _lib.lora_apply(ctypes.byref(desc), ctypes.byref(meta), x, ldx, buf or None, y, ldy, y_dtype, kind,
                            ws or None, ws_bytes, _stream(stream))
+
+
+def lora_shrink_noalloc(desc: LayerDesc, meta: Meta, x: int, ldx: int, buf: int, stream=None) -> int:
+    """lora_shrink (BGMV family) with its scratch in the library's fixed device array; allocates nothing."""
+    return _lib.lora_shrink_noalloc(ctypes.byref(desc), ctypes.byref(meta), x, ldx, buf, _stream(stream))
+
+
+def lora_noalloc_scratch_bytes() -> int:
+    return int(_lib.lora_noalloc_scratch_bytes())
 
 
 def lora_workspace_bytes(desc: LayerDesc, max_tokens: int, kind: int = LORA_AUTO) -> int:

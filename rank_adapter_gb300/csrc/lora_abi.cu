@@ -274,3 +274,69 @@ int lora_query_status(const lora_meta *meta, int32_t *out, lora_stream_t stream)
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free shrink.
+//
+// Some callers cannot allocate device memory at the point where they run the
+// shrink: code that executes inside another framework's memory pool or under
+// an allocator that forbids new device allocations, or latency-critical
+// serving paths that must not call into an allocator at all. For them this
+// entry point keeps the shrink's per-chunk partial rows in a fixed array
+// that is part of the library's device image instead of a caller-provided
+// workspace. Every GPU that loads the library holds this array (8 MiB) until
+// the process exits.
+
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = 8u << 20;  // 8 MiB of partial rows
+static __device__ __align__(256) float g_noalloc_scratch[kNoAllocScratchBytes / sizeof(float)];
+
+// Device address of g_noalloc_scratch on the current device. In host code the
+// array's name only stands in for the symbol, so the address is looked up
+// (once per device, with that device current) and cached.
+cudaError_t noalloc_scratch(float **out) {
+  static std::mutex mu;
+  static std::map<int, float *> addr;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = addr.find(dev);
+  if (it == addr.end()) {
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    it = addr.emplace(dev, static_cast<float *>(p)).first;
+  }
+  *out = it->second;
+  return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t lora_noalloc_scratch_bytes(void) { return kNoAllocScratchBytes; }
+
+int lora_shrink_noalloc(const lora_layer_desc *desc, const lora_meta *meta, const void *x, int64_t ldx, float *buf,
+                        lora_stream_t stream) {
+  clear_stale_error();
+  int st = check_desc(desc);
+  if (st != LORA_OK) return st;
+  st = check_meta(meta);
+  if (st != LORA_OK) return st;
+  if (meta->num_slots != desc->num_slots) return LORA_EINVAL;
+  if (meta->num_tokens == 0) return LORA_OK;
+  if (x == nullptr || buf == nullptr) return LORA_EINVAL;
+  if (ldx < desc->d_in) return LORA_EINVAL;
+  if (!aligned16(x) || !aligned16(buf) || (ldx * (int64_t)elem_size(desc->dtype)) % 16 != 0) return LORA_EALIGN;
+  if (ra::bgmv_workspace_bytes(*desc, meta->num_tokens) > kNoAllocScratchBytes) return LORA_ERANGE;
+  float *scratch = nullptr;
+  cudaError_t e = noalloc_scratch(&scratch);
+  if (e != cudaSuccess) return cuda_status(e);
+  return cuda_status(
+      ra::launch_bgmv_shrink(*desc, view_of(meta), ra::kListAll, x, ldx, buf, scratch, (cudaStream_t)stream));
+}
+
+}  // extern "C"
