@@ -290,8 +290,8 @@ class Replica:
         if ev is not None:
             ev[1].record()
         if path == "fused":
-            buf = self.buf.data_ptr() if self.kind != ra.LORA_BGMV else 0
-            ra.check(ra.lora_apply(self.table.desc, self.meta.c, self.x.data_ptr(), self.x.stride(0), buf,
+            # The fused step keeps the rank-r intermediate in the workspace; no buf output is asked for.
+            ra.check(ra.lora_apply(self.table.desc, self.meta.c, self.x.data_ptr(), self.x.stride(0), 0,
                                    self.y.data_ptr(), self.y.stride(0), self.ydt, self.kind, self.ws_ptr,
                                    self.ws_bytes, st), "apply")
             if ev is not None:

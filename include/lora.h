@@ -27,6 +27,13 @@
  * - Device-side conditions never trap or hang: a token slot id outside
  *   [0, num_slots) is treated as slot 0 and counted in meta->status
  *   (read it with lora_query_status).
+ * - Kernels are launched with programmatic dependent launch: a kernel may
+ *   start while the previous kernel on the stream drains, and reads the slot
+ *   table (A, B, slot_rank, slot_scale) before waiting for it. Write the
+ *   table through lora_set_slot / lora_reset_slot (they end with a launch
+ *   that waits for the write to be visible); a table written any other way
+ *   needs one more kernel, an event wait or a copy between the write and the
+ *   next call of this library.
  * - Grid sizes depend only on host-known bounds (num_tokens, num_slots,
  *   shapes), never on device data, so a sequence of calls can be captured in
  *   a CUDA graph once it has run eagerly once.

@@ -167,8 +167,9 @@ struct MetaView {
 // drains. Each kernel therefore waits for the predecessor's completion (and
 // memory flush) before it touches data a predecessor may still be writing.
 // Protocol:
-// * the slot-write kernel never lets a successor start early, so the slot
-//   table (A, B, ranks, scales) is complete whenever a later kernel starts;
+// * every slot write is followed by a fence kernel that waits for it and
+//   never triggers early, so the slot table (A, B, ranks, scales) is complete
+//   and visible whenever a later kernel starts;
 // * other kernels trigger their successor only after their own wait, so when
 //   a kernel starts, everything older than its immediate predecessor is
 //   complete;

@@ -62,6 +62,13 @@ __global__ void __launch_bounds__(256) slot_write_kernel(SlotArgs a) {
   }
 }
 
+// Launched right after every slot write. Kernels of this library may start
+// while their predecessor on the stream drains and read the slot table before
+// their own dependency wait; this kernel waits for the slot write to complete
+// and flush, and triggers nothing, so the next kernel starts only after the
+// table is visible.
+__global__ void slot_fence_kernel() { pdl_wait(); }
+
 }  // namespace
 
 cudaError_t launch_slot_write(const lora_layer_desc &d, int slot, int rank, float scale,
@@ -91,8 +98,10 @@ cudaError_t launch_slot_write(const lora_layer_desc &d, int slot, int rank, floa
   if (blocks > 1216) blocks = 1216;  // 8 CTAs per SM x 152 SMs, grid-stride beyond
   if (blocks < 1) blocks = 1;
   dim3 grid((unsigned)blocks, 2 * d.n_slices);
-  if (d.dtype == LORA_BF16) return launch_pdl(slot_write_kernel<__nv_bfloat16>, grid, dim3(256), 0, st, 1u, a);
-  return launch_pdl(slot_write_kernel<float>, grid, dim3(256), 0, st, 1u, a);
+  cudaError_t e = d.dtype == LORA_BF16 ? launch_pdl(slot_write_kernel<__nv_bfloat16>, grid, dim3(256), 0, st, 1u, a)
+                                      : launch_pdl(slot_write_kernel<float>, grid, dim3(256), 0, st, 1u, a);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(slot_fence_kernel, dim3(1), dim3(32), 0, st, 1u);
 }
 
 }  // namespace ra
