@@ -58,16 +58,22 @@ typedef enum {
   LORA_EALIGN = 3,        /* a pointer or leading dimension is not 16-byte aligned */
   LORA_EUNSUPPORTED = 4,  /* valid but not implemented (e.g. SGMV on fp32 tables) */
   LORA_ECUDA = 5,         /* a CUDA launch or copy failed; see lora_last_cuda_error() */
-  LORA_EBADSLOT = 6       /* lora_query_status: some token slot ids were out of range */
+  LORA_EBADSLOT = 6,      /* lora_query_status: some token slot ids were out of range */
+  LORA_EDEVICE = 7        /* lora_query_status: a kernel gave up waiting on its own pipeline
+                             (a fault it avoided); outputs since lora_prepare_meta are invalid */
 } lora_status;
 
 typedef enum { LORA_F32 = 0, LORA_BF16 = 1 } lora_dtype;
 
 /* Which kernel family runs a shrink / expand.
  * BGMV: per-segment streaming of each adapter's A/B on CUDA cores (decode).
- * SGMV: tensor-core (tcgen05) tiles over same-adapter segments (prefill), bf16 only.
- * AUTO: segments with fewer than LORA_SGMV_MIN_ROWS tokens go to BGMV, the
- *       others to SGMV (fp32 tables: all BGMV). */
+ * SGMV: tensor-core (tcgen05) tiles of 128 rows over same-adapter segments
+ *       (prefill); bf16 tables with r_max >= 16 only (else LORA_EUNSUPPORTED).
+ * AUTO: in a batch of at least LORA_AUTO_SGMV_MIN_TOKENS tokens, segments
+ *       with at least LORA_SGMV_MIN_ROWS tokens go to SGMV and the others to
+ *       BGMV; smaller batches, and tables SGMV does not take, run all on BGMV.
+ *       The choice depends only on num_tokens, the table and the metadata,
+ *       so lora_shrink and lora_expand of one batch agree on it. */
 typedef enum { LORA_AUTO = 0, LORA_BGMV = 1, LORA_SGMV = 2 } lora_kind;
 
 #define LORA_MAX_SLICES 4
@@ -76,6 +82,7 @@ typedef enum { LORA_AUTO = 0, LORA_BGMV = 1, LORA_SGMV = 2 } lora_kind;
 #define LORA_MAX_TOKENS (1 << 24)
 #define LORA_SGMV_MIN_ROWS 64      /* AUTO threshold: segment rows routed to SGMV */
 #define LORA_SGMV_TILE_M 128       /* rows per SGMV tile (work-list granularity) */
+#define LORA_AUTO_SGMV_MIN_TOKENS 1024  /* AUTO: smaller batches run all on BGMV */
 
 /*
  * One LoRA-wrapped layer: the stacked slot table of one (packed) projection.
@@ -178,13 +185,15 @@ int lora_prepare_meta(const lora_meta *meta, lora_stream_t stream);
  *   buf: device fp32, [n_slices, num_tokens, r_max] contiguous; rows of
  *        slot-0 tokens are not written
  *   ws:  device scratch of at least lora_workspace_bytes(desc, num_tokens,
- *        kind) bytes, 16-byte aligned, caller-owned. The CUDA-core family
- *        splits d_in into chunks and keeps each chunk's partial rows there;
- *        its contents need no initialisation and are meaningless between
- *        calls. Calls that share a workspace must not overlap in time (order
- *        them on one stream).
+ *        kind) bytes, 16-byte aligned, caller-owned. Both families split d_in
+ *        and keep the partial rows of each split there (BGMV: chunks of
+ *        32 KB of A; SGMV: as many splits as keep every SM busy, at most
+ *        16); its contents need no initialisation and are meaningless
+ *        between calls. Calls that share a workspace must not overlap in
+ *        time (order them on one stream).
  * bf16 inputs are multiplied exactly and accumulated in fp32 in a fixed
- * order (results do not depend on the batch's other tokens).
+ * order, and the splits are summed in split order (results do not depend
+ * on the batch's other tokens, and repeat bitwise).
  */
 int lora_shrink(const lora_layer_desc *desc, const lora_meta *meta, const void *x, int64_t ldx,
                 float *buf, int32_t kind, void *ws, size_t ws_bytes, lora_stream_t stream);
@@ -195,7 +204,9 @@ int lora_shrink(const lora_layer_desc *desc, const lora_meta *meta, const void *
  * with off_s = out_sizes[0] + ... + out_sizes[s-1] (packed qkv / gate_up
  * outputs; lora_expand of the vLLM page, section "expand 核"). The sum is
  * formed in fp32 and added to y once; a bf16 y is rounded to nearest even.
- * Rows of slot-0 tokens are not read or written.
+ * Rows of slot-0 tokens are not read or written. Columns k >= rank a of buf
+ * are ignored. The SGMV family multiplies buf as two bf16 parts (hi + lo,
+ * relative error about 2^-17) on the tensor cores, with fp32 accumulation.
  *   buf: device fp32 [n_slices, num_tokens, r_max] as written by lora_shrink
  *   y:   device, [num_tokens, sum(out_sizes)] with row stride ldy elements,
  *        y_dtype (LORA_BF16 production; LORA_F32 for accuracy runs; an fp32
@@ -208,14 +219,12 @@ int lora_expand(const lora_layer_desc *desc, const lora_meta *meta, const float 
  * Fused shrink + expand: the whole delta for every LoRA token in one call,
  *   y[t, off_s + n] += sum_k (scale[a] * x[t] . A[s][a])[k] * B[s][a, k, n]
  * with the same arithmetic, rounding and slot-0 rule as lora_shrink followed
- * by lora_expand (results are bitwise equal for segments that run in the
- * BGMV family). In the BGMV family the expand forms the rank-r rows
- * directly from the shrink's chunk partials, so the u buffer is optional
- * (the "batched gather" form of the handbook page, section "不合并权重，批量计算").
+ * by lora_expand (results are bitwise equal). The expand forms the rank-r
+ * rows directly from the shrink's split partials in the workspace, so the
+ * u buffer is optional (the "batched gather" form of the handbook page,
+ * section "不合并权重，批量计算").
  *   buf: device fp32 [n_slices, num_tokens, r_max] or NULL. When non-NULL it
- *        also receives the shrink result. It must be non-NULL when any
- *        segment runs in the SGMV family (kind LORA_SGMV, or LORA_AUTO on a
- *        bf16 table), which goes through the buffer.
+ *        also receives the shrink result.
  *   ws, ws_bytes: scratch as for lora_shrink.
  * Other arguments and errors as lora_shrink / lora_expand.
  */
@@ -223,16 +232,19 @@ int lora_apply(const lora_layer_desc *desc, const lora_meta *meta, const void *x
                void *y, int64_t ldy, int32_t y_dtype, int32_t kind, void *ws, size_t ws_bytes,
                lora_stream_t stream);
 
-/* Scratch bytes lora_shrink / lora_apply need for this layer and up to
- * max_tokens tokens (0: none); 0 for an invalid desc. */
+/* Scratch bytes lora_shrink / lora_apply need for this layer, kind and up to
+ * max_tokens tokens on the current device (the SGMV part scales with its SM
+ * count); 0 for an invalid desc or a kind the table does not support. */
 size_t lora_workspace_bytes(const lora_layer_desc *desc, int32_t max_tokens, int32_t kind);
 
 /* Bytes the meta->tiles work-list buffer needs for a table of num_slots slots. */
 size_t lora_meta_tiles_bytes(int32_t num_slots);
 
 /*
- * Synchronise `stream`, copy meta->status to *out (host) and return LORA_OK
- * if it is 0, LORA_EBADSLOT if some token ids were out of range.
+ * Synchronise `stream`, copy meta->status to *out (host) and return
+ * LORA_EDEVICE if a kernel since the last lora_prepare_meta gave up waiting
+ * on its own pipeline, else LORA_OK if *out is 0 and LORA_EBADSLOT if some
+ * token ids were out of range.
  */
 int lora_query_status(const lora_meta *meta, int32_t *out, lora_stream_t stream);
 

@@ -624,9 +624,8 @@ cudaError_t launch_bgmv_shrink(const lora_layer_desc &d, const MetaView &mv, Lis
                     (size_t)a.g.smem_reduce, st, 1u, a);
 }
 
-cudaError_t launch_bgmv_apply(const lora_layer_desc &d, const MetaView &mv, ListSel sel, const void *x,
-                              int64_t ldx, float *buf, float *ws, void *y, int64_t ldy, int y_dtype,
-                              cudaStream_t st) {
+cudaError_t launch_bgmv_apply_shrink(const lora_layer_desc &d, const MetaView &mv, ListSel sel, const void *x,
+                                     int64_t ldx, float *buf, float *ws, cudaStream_t st) {
   if (std::min(mv.num_slots - 1, mv.num_tokens) <= 0) return cudaSuccess;
   BgmvArgs a{};
   fill_common(a, d, mv, sel);
@@ -636,18 +635,31 @@ cudaError_t launch_bgmv_apply(const lora_layer_desc &d, const MetaView &mv, List
   a.buf = buf;
   a.to_parts = 1;  // the expand forms u from the partials; buf is optional
   cudaError_t e = d.dtype == LORA_BF16 ? dispatch_shrink<__nv_bfloat16>(a, st) : dispatch_shrink<float>(a, st);
-  if (e != cudaSuccess) return e;
+  if (e != cudaSuccess || buf == nullptr) return e;
+  a.u_in = ws;  // the caller also wants the u rows
+  return launch_pdl(bgmv_reduce_kernel, dim3((unsigned)(a.max_items * a.n_slices)), dim3(kThreads),
+                    (size_t)a.g.smem_reduce, st, 1u, a);
+}
+
+cudaError_t launch_bgmv_apply_expand(const lora_layer_desc &d, const MetaView &mv, ListSel sel, const float *ws,
+                                     void *y, int64_t ldy, int y_dtype, cudaStream_t st) {
+  if (std::min(mv.num_slots - 1, mv.num_tokens) <= 0) return cudaSuccess;
+  BgmvArgs a{};
+  fill_common(a, d, mv, sel);
   a.u_in = ws;
-  if (buf != nullptr) {  // the caller also wants the u rows
-    e = launch_pdl(bgmv_reduce_kernel, dim3((unsigned)(a.max_items * a.n_slices)), dim3(kThreads),
-                   (size_t)a.g.smem_reduce, st, 1u, a);
-    if (e != cudaSuccess) return e;
-  }
   a.u_parts = 1;
   a.pre = 1;
   a.y = y;
   a.ldy = ldy;
   return launch_expand(a, d.dtype, y_dtype, st);
+}
+
+cudaError_t launch_bgmv_apply(const lora_layer_desc &d, const MetaView &mv, ListSel sel, const void *x,
+                              int64_t ldx, float *buf, float *ws, void *y, int64_t ldy, int y_dtype,
+                              cudaStream_t st) {
+  cudaError_t e = launch_bgmv_apply_shrink(d, mv, sel, x, ldx, buf, ws, st);
+  if (e != cudaSuccess) return e;
+  return launch_bgmv_apply_expand(d, mv, sel, ws, y, ldy, y_dtype, st);
 }
 
 cudaError_t launch_bgmv_expand(const lora_layer_desc &d, const MetaView &mv, ListSel sel, const float *buf,

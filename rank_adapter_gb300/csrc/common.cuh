@@ -130,7 +130,9 @@ __device__ __forceinline__ void cp_async_wait_upto(int n) {
 //   [2] n_large  LoRA segments with >= LORA_SGMV_MIN_ROWS tokens
 //   [3] tiles_all    sum over all LoRA segments of ceil(count / LORA_SGMV_TILE_M)
 //   [4] tiles_large  the same over the large segments
-//   [5..7] reserved (0)
+//   [5..6] reserved (0)
+//   [7] device error bits (0 when written; a kernel whose pipeline wait ran
+//       out sets a bit, read back by lora_query_status)
 //   then three lists of S = num_slots unit records (all, small, large), each
 //   record 8 ints: {segment, slot, count, first sorted row, first 4 token rows}
 //   (rows past the count are -1; unused records are all -1),
@@ -139,6 +141,7 @@ __device__ __forceinline__ void cp_async_wait_upto(int n) {
 struct WorkLists {
   static constexpr int kHeader = 8;
   static constexpr int kRec = 8;
+  static constexpr int kErrWord = 7;
   __host__ __device__ static inline size_t ints(int S) {
     return kHeader + 3 * (size_t)kRec * S + 2 * ((size_t)S + 1) + 3 * (size_t)S;
   }
@@ -226,12 +229,21 @@ cudaError_t launch_bgmv_expand(const lora_layer_desc &d, const MetaView &mv, Lis
 cudaError_t launch_bgmv_apply(const lora_layer_desc &d, const MetaView &mv, ListSel sel, const void *x,
                               int64_t ldx, float *buf, float *ws, void *y, int64_t ldy, int y_dtype,
                               cudaStream_t st);
+// The expand half of launch_bgmv_apply's work and its shrink half, for callers
+// that launch other kernels in between (AUTO batches with SGMV segments).
+cudaError_t launch_bgmv_apply_shrink(const lora_layer_desc &d, const MetaView &mv, ListSel sel, const void *x,
+                                     int64_t ldx, float *buf, float *ws, cudaStream_t st);
+cudaError_t launch_bgmv_apply_expand(const lora_layer_desc &d, const MetaView &mv, ListSel sel, const float *ws,
+                                     void *y, int64_t ldy, int y_dtype, cudaStream_t st);
+// SGMV family (sgmv.cu, tcgen05). part: split partials, sgmv_workspace_bytes() bytes.
 bool sgmv_supported();
-cudaError_t launch_bgmv_apply(const lora_layer_desc &d, const MetaView &mv, ListSel sel, const void *x,
-                              int64_t ldx, float *buf, void *y, int64_t ldy, int y_dtype, cudaStream_t st);
-cudaError_t launch_sgmv_shrink(const lora_layer_desc &d, const MetaView &mv, ListSel sel,
-                               const void *x, int64_t ldx, float *buf, cudaStream_t st);
-cudaError_t launch_sgmv_expand(const lora_layer_desc &d, const MetaView &mv, ListSel sel,
-                               const float *buf, void *y, int64_t ldy, int y_dtype, cudaStream_t st);
+size_t sgmv_workspace_bytes(const lora_layer_desc &d, int max_tokens);
+cudaError_t launch_sgmv_shrink(const lora_layer_desc &d, const MetaView &mv, ListSel sel, const void *x,
+                               int64_t ldx, float *part, cudaStream_t st);
+cudaError_t launch_sgmv_reduce(const lora_layer_desc &d, const MetaView &mv, ListSel sel, const float *part,
+                               float *buf, cudaStream_t st);
+// u_parts: u_src holds the shrink's split partials (else the u buffer [n_slices, T, r_max]).
+cudaError_t launch_sgmv_expand(const lora_layer_desc &d, const MetaView &mv, ListSel sel, const float *u_src,
+                               int u_parts, void *y, int64_t ldy, int y_dtype, cudaStream_t st);
 
 }  // namespace ra

@@ -76,11 +76,39 @@ int check_meta(const lora_meta *m) {
   return LORA_OK;
 }
 
-// The BGMV family keeps per-chunk partial rows in caller-provided scratch.
-int check_ws(const lora_layer_desc *d, const lora_meta *m, const void *ws, size_t ws_bytes) {
-  const size_t need = ra::bgmv_workspace_bytes(*d, m->num_tokens);
-  if (need == 0) return LORA_OK;
-  if (ws == nullptr || ws_bytes < need) return LORA_EINVAL;
+// The SGMV family exists for bf16 tables with r_max >= 16 (the MMA N / K granularity).
+bool sgmv_available(const lora_layer_desc *d) {
+  return d->dtype == LORA_BF16 && d->r_max >= 16 && ra::sgmv_supported();
+}
+
+// AUTO sends its large segments to SGMV only in batches of at least
+// LORA_AUTO_SGMV_MIN_TOKENS tokens; smaller batches run entirely on BGMV.
+bool auto_uses_sgmv(const lora_layer_desc *d, int num_tokens) {
+  return num_tokens >= LORA_AUTO_SGMV_MIN_TOKENS && sgmv_available(d);
+}
+
+// Which families a (kind, batch) runs and where their scratch lives in the
+// workspace: [BGMV chunk partials | SGMV split partials (256-byte aligned)].
+struct Plan {
+  bool bgmv, sgmv, split;  // split: AUTO with segments on both families
+  size_t bgmv_bytes, sgmv_off, sgmv_bytes, total;
+};
+
+Plan plan_of(const lora_layer_desc *d, int num_tokens, int kind) {
+  Plan p{};
+  p.sgmv = kind == LORA_SGMV || (kind == LORA_AUTO && auto_uses_sgmv(d, num_tokens));
+  p.bgmv = kind != LORA_SGMV;
+  p.split = p.bgmv && p.sgmv;
+  p.bgmv_bytes = p.bgmv ? ra::bgmv_workspace_bytes(*d, num_tokens) : 0;
+  p.sgmv_off = (p.bgmv_bytes + 255) & ~(size_t)255;
+  p.sgmv_bytes = p.sgmv ? ra::sgmv_workspace_bytes(*d, num_tokens) : 0;
+  p.total = p.sgmv_bytes ? p.sgmv_off + p.sgmv_bytes : p.bgmv_bytes;
+  return p;
+}
+
+int check_ws(const Plan &p, const void *ws, size_t ws_bytes) {
+  if (p.total == 0) return LORA_OK;
+  if (ws == nullptr || ws_bytes < p.total) return LORA_EINVAL;
   if (!aligned16(ws)) return LORA_EALIGN;
   return LORA_OK;
 }
@@ -97,9 +125,6 @@ ra::MetaView view_of(const lora_meta *m) {
   return v;
 }
 
-// The SGMV family exists for bf16 tables only.
-bool sgmv_available(const lora_layer_desc *d) { return d->dtype == LORA_BF16 && ra::sgmv_supported(); }
-
 }  // namespace
 
 extern "C" {
@@ -113,6 +138,7 @@ const char *lora_strerror(int status) {
     case LORA_EUNSUPPORTED: return "unsupported combination (e.g. SGMV on an fp32 table)";
     case LORA_ECUDA: return "CUDA launch or copy failed (see lora_last_cuda_error)";
     case LORA_EBADSLOT: return "some token slot ids were outside [0, num_slots) and were treated as slot 0";
+    case LORA_EDEVICE: return "a kernel stopped waiting on its own pipeline; the outputs since the last lora_prepare_meta are invalid";
     default: return "unknown lora_status";
   }
 }
@@ -125,9 +151,10 @@ size_t lora_meta_tiles_bytes(int32_t num_slots) {
 }
 
 size_t lora_workspace_bytes(const lora_layer_desc *desc, int32_t max_tokens, int32_t kind) {
-  (void)kind;  // every kind may route segments through the BGMV family
   if (check_desc(desc) != LORA_OK || max_tokens <= 0) return 0;
-  return ra::bgmv_workspace_bytes(*desc, max_tokens);
+  if (kind != LORA_AUTO && kind != LORA_BGMV && kind != LORA_SGMV) return 0;
+  if (kind == LORA_SGMV && !sgmv_available(desc)) return 0;
+  return plan_of(desc, max_tokens, kind).total;
 }
 
 int lora_set_slot(const lora_layer_desc *desc, int32_t slot, int32_t rank, float scale,
@@ -175,20 +202,22 @@ int lora_shrink(const lora_layer_desc *desc, const lora_meta *meta, const void *
   if (x == nullptr || buf == nullptr) return LORA_EINVAL;
   if (ldx < desc->d_in) return LORA_EINVAL;
   if (!aligned16(x) || !aligned16(buf) || (ldx * (int64_t)elem_size(desc->dtype)) % 16 != 0) return LORA_EALIGN;
-  if (kind != LORA_SGMV) {
-    st = check_ws(desc, meta, ws, ws_bytes);
-    if (st != LORA_OK) return st;
-  }
+  const Plan p = plan_of(desc, meta->num_tokens, kind);
+  st = check_ws(p, ws, ws_bytes);
+  if (st != LORA_OK) return st;
   const ra::MetaView mv = view_of(meta);
   cudaStream_t s = (cudaStream_t)stream;
-  float *wsf = static_cast<float *>(ws);
-  if (kind == LORA_BGMV || (kind == LORA_AUTO && !sgmv_available(desc)))
-    return cuda_status(ra::launch_bgmv_shrink(*desc, mv, ra::kListAll, x, ldx, buf, wsf, s));
-  if (kind == LORA_SGMV)
-    return cuda_status(ra::launch_sgmv_shrink(*desc, mv, ra::kListAll, x, ldx, buf, s));
-  st = cuda_status(ra::launch_bgmv_shrink(*desc, mv, ra::kListSmall, x, ldx, buf, wsf, s));
+  float *wb = static_cast<float *>(ws);
+  float *wsg = reinterpret_cast<float *>(static_cast<char *>(ws) + p.sgmv_off);
+  if (!p.sgmv) return cuda_status(ra::launch_bgmv_shrink(*desc, mv, ra::kListAll, x, ldx, buf, wb, s));
+  const ra::ListSel sel = p.split ? ra::kListLarge : ra::kListAll;
+  if (p.split) {
+    st = cuda_status(ra::launch_bgmv_shrink(*desc, mv, ra::kListSmall, x, ldx, buf, wb, s));
+    if (st != LORA_OK) return st;
+  }
+  st = cuda_status(ra::launch_sgmv_shrink(*desc, mv, sel, x, ldx, wsg, s));
   if (st != LORA_OK) return st;
-  return cuda_status(ra::launch_sgmv_shrink(*desc, mv, ra::kListLarge, x, ldx, buf, s));
+  return cuda_status(ra::launch_sgmv_reduce(*desc, mv, sel, wsg, buf, s));
 }
 
 int lora_expand(const lora_layer_desc *desc, const lora_meta *meta, const float *buf, void *y,
@@ -209,15 +238,16 @@ int lora_expand(const lora_layer_desc *desc, const lora_meta *meta, const float 
   for (int s = 0; s < desc->n_slices; ++s) total += desc->out_sizes[s];
   if (ldy < total) return LORA_EINVAL;
   if (!aligned16(y) || !aligned16(buf) || (ldy * (int64_t)elem_size(y_dtype)) % 16 != 0) return LORA_EALIGN;
+  const Plan p = plan_of(desc, meta->num_tokens, kind);
   const ra::MetaView mv = view_of(meta);
   cudaStream_t s = (cudaStream_t)stream;
-  if (kind == LORA_BGMV || (kind == LORA_AUTO && !sgmv_available(desc)))
-    return cuda_status(ra::launch_bgmv_expand(*desc, mv, ra::kListAll, buf, y, ldy, y_dtype, s));
-  if (kind == LORA_SGMV)
-    return cuda_status(ra::launch_sgmv_expand(*desc, mv, ra::kListAll, buf, y, ldy, y_dtype, s));
-  st = cuda_status(ra::launch_bgmv_expand(*desc, mv, ra::kListSmall, buf, y, ldy, y_dtype, s));
-  if (st != LORA_OK) return st;
-  return cuda_status(ra::launch_sgmv_expand(*desc, mv, ra::kListLarge, buf, y, ldy, y_dtype, s));
+  if (!p.sgmv) return cuda_status(ra::launch_bgmv_expand(*desc, mv, ra::kListAll, buf, y, ldy, y_dtype, s));
+  if (p.split) {
+    st = cuda_status(ra::launch_bgmv_expand(*desc, mv, ra::kListSmall, buf, y, ldy, y_dtype, s));
+    if (st != LORA_OK) return st;
+  }
+  return cuda_status(ra::launch_sgmv_expand(*desc, mv, p.split ? ra::kListLarge : ra::kListAll, buf, 0, y, ldy,
+                                            y_dtype, s));
 }
 
 int lora_apply(const lora_layer_desc *desc, const lora_meta *meta, const void *x, int64_t ldx, float *buf,
@@ -234,43 +264,55 @@ int lora_apply(const lora_layer_desc *desc, const lora_meta *meta, const void *x
   if (desc->dtype == LORA_F32 && y_dtype != LORA_F32) return LORA_EUNSUPPORTED;
   if (kind == LORA_SGMV && !sgmv_available(desc)) return LORA_EUNSUPPORTED;
   if (meta->num_tokens == 0) return LORA_OK;
-  const bool uses_sgmv = kind == LORA_SGMV || (kind == LORA_AUTO && sgmv_available(desc));
-  if (x == nullptr || y == nullptr || (uses_sgmv && buf == nullptr)) return LORA_EINVAL;
+  if (x == nullptr || y == nullptr) return LORA_EINVAL;
   int64_t total = 0;
   for (int s = 0; s < desc->n_slices; ++s) total += desc->out_sizes[s];
   if (ldx < desc->d_in || ldy < total) return LORA_EINVAL;
   if (!aligned16(x) || !aligned16(y) || (buf != nullptr && !aligned16(buf)) ||
       (ldx * (int64_t)elem_size(desc->dtype)) % 16 != 0 || (ldy * (int64_t)elem_size(y_dtype)) % 16 != 0)
     return LORA_EALIGN;
-  if (kind != LORA_SGMV) {
-    st = check_ws(desc, meta, ws, ws_bytes);
-    if (st != LORA_OK) return st;
-  }
+  const Plan p = plan_of(desc, meta->num_tokens, kind);
+  st = check_ws(p, ws, ws_bytes);
+  if (st != LORA_OK) return st;
   const ra::MetaView mv = view_of(meta);
   cudaStream_t s = (cudaStream_t)stream;
-  float *wsf = static_cast<float *>(ws);
-  if (!uses_sgmv)
-    return cuda_status(ra::launch_bgmv_apply(*desc, mv, ra::kListAll, x, ldx, buf, wsf, y, ldy, y_dtype, s));
-  if (kind == LORA_SGMV) {
-    st = cuda_status(ra::launch_sgmv_shrink(*desc, mv, ra::kListAll, x, ldx, buf, s));
+  float *wb = static_cast<float *>(ws);
+  float *wsg = reinterpret_cast<float *>(static_cast<char *>(ws) + p.sgmv_off);
+  if (!p.sgmv)
+    return cuda_status(ra::launch_bgmv_apply(*desc, mv, ra::kListAll, x, ldx, buf, wb, y, ldy, y_dtype, s));
+  const ra::ListSel sel = p.split ? ra::kListLarge : ra::kListAll;
+  // Both shrinks first, then both expands: each expand reads partials that
+  // are at least one launch old.
+  if (p.split) {
+    st = cuda_status(ra::launch_bgmv_apply_shrink(*desc, mv, ra::kListSmall, x, ldx, buf, wb, s));
     if (st != LORA_OK) return st;
-    return cuda_status(ra::launch_sgmv_expand(*desc, mv, ra::kListAll, buf, y, ldy, y_dtype, s));
   }
-  st = cuda_status(ra::launch_bgmv_apply(*desc, mv, ra::kListSmall, x, ldx, buf, wsf, y, ldy, y_dtype, s));
+  st = cuda_status(ra::launch_sgmv_shrink(*desc, mv, sel, x, ldx, wsg, s));
   if (st != LORA_OK) return st;
-  st = cuda_status(ra::launch_sgmv_shrink(*desc, mv, ra::kListLarge, x, ldx, buf, s));
-  if (st != LORA_OK) return st;
-  return cuda_status(ra::launch_sgmv_expand(*desc, mv, ra::kListLarge, buf, y, ldy, y_dtype, s));
+  if (buf != nullptr) {
+    st = cuda_status(ra::launch_sgmv_reduce(*desc, mv, sel, wsg, buf, s));
+    if (st != LORA_OK) return st;
+  }
+  if (p.split) {
+    st = cuda_status(ra::launch_bgmv_apply_expand(*desc, mv, ra::kListSmall, wb, y, ldy, y_dtype, s));
+    if (st != LORA_OK) return st;
+  }
+  return cuda_status(ra::launch_sgmv_expand(*desc, mv, sel, wsg, 1, y, ldy, y_dtype, s));
 }
 
 int lora_query_status(const lora_meta *meta, int32_t *out, lora_stream_t stream) {
   if (meta == nullptr || meta->status == nullptr || out == nullptr) return LORA_EINVAL;
-  int32_t v = 0;
-  cudaError_t e = cudaMemcpyAsync(&v, meta->status, sizeof(int32_t), cudaMemcpyDeviceToHost, (cudaStream_t)stream);
-  if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
+  int32_t v[2] = {0, 0};
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e = cudaMemcpyAsync(&v[0], meta->status, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess && meta->tiles != nullptr)
+    e = cudaMemcpyAsync(&v[1], static_cast<const int32_t *>(meta->tiles) + ra::WorkLists::kErrWord, sizeof(int32_t),
+                        cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return cuda_status(e);
-  *out = v;
-  return v == 0 ? LORA_OK : LORA_EBADSLOT;
+  *out = v[0];
+  if (v[1] != 0) return LORA_EDEVICE;
+  return v[0] == 0 ? LORA_OK : LORA_EBADSLOT;
 }
 
 }  // extern "C"

@@ -1,20 +1,974 @@
-// SGMV shrink / expand on the tcgen05 tensor cores (prefill form). Not built yet:
-// the launchers report "not supported" and the ABI answers LORA_EUNSUPPORTED for
-// an explicit SGMV request, while AUTO runs every segment through BGMV.
+// SGMV shrink / expand on the tcgen05 tensor cores: the prefill form of the
+// multi-LoRA delta (handbook page "多 LoRA 服务：分段矩阵乘与适配器调度", section
+// "不合并权重，批量计算": tokens are stably grouped into same-adapter segments
+// and each segment is one small GEMM; page "vLLM 源码完全拆解(十八): 多 LoRA
+// 服务", section "两个低秩 GEMM:shrink、expand 与 fp32 中转缓冲").
+//
+// Work is cut into 128-row tiles of the segments of a work list (the metadata
+// kernel's cumulative tile counts). Both kernels are persistent (one CTA per
+// SM) and warp-specialised around mbarrier pipelines:
+//
+// * shrink: item = (tile, split of d_in). Producer warps gather the tile's x
+//   rows with 16-byte cp.async into the 128-byte-swizzled K-major operand
+//   layout; one of them loads each slice's block of A (64 rows of d_in by
+//   r_max) with TMA as a swizzled MN-major operand. One thread issues
+//   tcgen05.mma (M = 128, N = r_max per slice, K = 16) into a TMEM
+//   accumulator; epilogue warps read it back (tcgen05.ld) and store
+//   unscaled fp32 partial rows to the workspace. The number of d_in splits
+//   follows the tile count so that every SM gets work (split-K).
+// * expand: item = (tile, slice, 128 columns for bf16 y, 64 for fp32 y). The
+//   tile's rank-r rows u (scale * the split partials summed in split order,
+//   or the caller's buffer) are split into bf16 hi + lo parts and stored once
+//   per (tile, slice) as the K-major A operand, so the product keeps fp32
+//   accuracy; B blocks come by TMA; y rows come in and go out with per-row
+//   bulk copies through shared memory, and the epilogue adds the accumulator
+//   (u_hi B + u_lo B) to them in place.
+// * reduce: the split path's partials -> buffer rows, with the expand's
+//   arithmetic, so split and fused SGMV paths agree bitwise.
+//
+// Every wait on a barrier is bounded: one that runs out records an error in
+// the work-list header (reported by lora_query_status) and the CTA winds
+// down without touching memory it does not own.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cstring>
+#include <map>
+#include <mutex>
+
 #include "common.cuh"
 
 namespace ra {
+namespace {
 
-bool sgmv_supported() { return false; }
+constexpr int kTileM = LORA_SGMV_TILE_M;  // rows per tile (and MMA M)
+constexpr int kKB = 64;                   // d_in elements per shrink K block (one 128-byte swizzle row)
+constexpr int kKCMax = 16;                // at most this many d_in splits
+constexpr int kSmemMax = 227 * 1024;
+constexpr int kAlignSlack = 1024;         // dynamic smem is re-aligned to 1024 bytes
+constexpr int kUKRegion = kTileM * 128;   // bytes of one 64-wide K region of a 128-row operand
+constexpr int kYPitch = 272;              // bytes per staged y row: 256 + 16 (bank spread)
+constexpr int kYStage = kTileM * kYPitch;
+constexpr uint64_t kWaitNs = 200000000ull;  // a pipeline wait longer than 200 ms means a fault
 
-cudaError_t launch_sgmv_shrink(const lora_layer_desc &, const MetaView &, ListSel, const void *, int64_t,
-                               float *, cudaStream_t) {
-  return cudaErrorNotSupported;
+// Error bits in the work-list header (word WorkLists::kErrWord).
+constexpr int kErrShrink = 1;
+constexpr int kErrExpand = 2;
+constexpr int kErrReduce = 4;
+
+// Shared-memory descriptor layouts.
+constexpr uint32_t kSw128 = 2, kSw64 = 4, kSw32 = 6;
+
+// ------------------------------------------------------------------ PTX wrappers
+
+__device__ __forceinline__ void mbar_init(uint64_t *b, uint32_t n) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(b)), "r"(n) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *b) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(b)) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_tx(uint64_t *b, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(b)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint64_t *b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(b)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Wait for the phase of the given parity. Gives up after kWaitNs: records
+// `code` in *err and returns false.
+__device__ __forceinline__ bool mbar_wait(uint64_t *b, uint32_t parity, int *err, int code) {
+  if (mbar_try(b, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (;;) {
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try(b, parity)) return true;
+    if (global_ns() - t0 > kWaitNs) {
+      atomicOr(err, code);
+      return false;
+    }
+  }
+}
+// The same, with one verdict for the whole warp (every lane must call it).
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t *b, uint32_t parity, int *err, int code) {
+  return __all_sync(0xffffffffu, mbar_wait(b, parity, err, code)) != 0;
+}
+__device__ __forceinline__ void fence_mbar_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
+// Order this thread's generic-proxy shared-memory writes before later async-proxy reads.
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void tc_before_sync() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_after_sync() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, int c0, int c1, int c2, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
+      ::"r"(smem_addr(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_addr(bar))
+      : "memory");
+}
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar)) : "memory");
+}
+__device__ __forceinline__ void bulk_store(void *dst, const void *src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+               ::"l"(dst), "r"(smem_addr(src)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_upto1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// 16-byte cp.async that writes zeros when !valid (nothing is read then).
+__device__ __forceinline__ void cp_async16_zfill(void *dst, const void *src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;"
+               ::"r"(smem_addr(dst)), "l"(src), "r"(valid ? 16 : 0) : "memory");
 }
 
-cudaError_t launch_sgmv_expand(const lora_layer_desc &, const MetaView &, ListSel, const float *, void *,
-                               int64_t, int, cudaStream_t) {
-  return cudaErrorNotSupported;
+// TMEM: allocation by one whole warp; the address lands in shared memory.
+__device__ __forceinline__ void tmem_alloc(uint32_t *slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+               ::"r"(smem_addr(slot)), "r"(ncols) : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_free(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+// D[tmem] (+)= A[smem] * B[smem], bf16 operands, fp32 accumulator.
+__device__ __forceinline__ void mma_bf16(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+      ::"r"(d), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc)
+      : "memory");
+}
+// The barrier receives one arrival once every MMA this thread issued so far is complete.
+__device__ __forceinline__ void mma_commit(uint64_t *bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+               ::"r"(smem_addr(bar)) : "memory");
+}
+// 16 consecutive fp32 accumulator columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Shared-memory matrix descriptor (start, leading / stride byte offsets, swizzle).
+// For the swizzled MN-major operands here the leading offset is the distance
+// between blocks along N and the stride offset the distance between groups of
+// 8 rows along K; for the K-major ones the stride offset is the distance
+// between groups of 8 rows (the leading offset is unused).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo, uint32_t layout) {
+  return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | ((uint64_t)layout << 61);
+}
+// Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B, A K-major, B MN-major.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+// Byte offset of 16-byte chunk c of row r in a 128-row, 128-byte-swizzled K-major region.
+__device__ __forceinline__ uint32_t swz128(int r, int c) {
+  return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
+}
+
+__device__ __forceinline__ unsigned char *align1024(unsigned char *p) {
+  return reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(p) + 1023) & ~(uintptr_t)1023);
+}
+
+// ------------------------------------------------------------------ work items
+
+struct SgList {
+  int list;      // int offset of the unit-record list
+  int ts;        // int offset of its cumulative tile counts
+  int hdr_segs;  // header word: records in the list
+  int hdr_tiles; // header word: tiles in the list
+};
+
+// d_in splits of the shrink for a tile count (the expand and reduce use the same).
+__host__ __device__ __forceinline__ int split_count(int n_tiles, int grid, int kcmax) {
+  if (n_tiles <= 0) return 1;
+  int kc = (2 * grid + n_tiles - 1) / n_tiles;
+  return kc < 1 ? 1 : (kc > kcmax ? kcmax : kc);
+}
+
+struct TileInfo {
+  int slot, pos0, rows;
+};
+
+// The segment of tile `tile`: the last record whose first tile is <= tile.
+__device__ __forceinline__ TileInfo tile_info(const int32_t *w, const SgList &L, int n_list, int tile) {
+  const int32_t *ts = w + L.ts;
+  int lo = 0, hi = n_list - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (ts[mid] <= tile) lo = mid;
+    else hi = mid - 1;
+  }
+  const int32_t *rec = w + L.list + lo * WorkLists::kRec;
+  const int k = tile - ts[lo];
+  TileInfo t;
+  t.slot = rec[1];
+  t.pos0 = rec[3] + k * kTileM;
+  t.rows = min(kTileM, rec[2] - k * kTileM);
+  return t;
+}
+
+struct SgMaps {
+  CUtensorMap m[LORA_MAX_SLICES];
+};
+
+// ------------------------------------------------------------------ shrink
+
+struct SgShrinkArgs {
+  const __nv_bfloat16 *x;
+  int64_t ldx;
+  float *part;                // partial rows [item][slice][128][r_max]
+  const int32_t *work;
+  const int32_t *sorted_rows;
+  int *err;
+  SgList L;
+  int d_in, r_max, n_slices, kcmax, nb;  // nb: K blocks of 64
+  int box_n;                  // TMA box width of an A block (<= 64 columns)
+  uint32_t w_layout;          // its swizzle
+  int stages, lag, stage_bytes, w_bytes;
+  int acc_cols, n_acc, tmem_cols;
+};
+
+constexpr int kShrinkProducers = 128;  // warps 0-3
+constexpr int kShrinkThreads = 288;    // + epilogue warps 4-7 + MMA warp 8
+
+__global__ void __launch_bounds__(kShrinkThreads, 1)
+    sgmv_shrink_kernel(const __grid_constant__ SgMaps maps, const SgShrinkArgs a) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char *sm = align1024(smem_raw);
+  uint64_t *full = reinterpret_cast<uint64_t *>(sm + a.stages * a.stage_bytes);
+  uint64_t *empty = full + a.stages;
+  uint64_t *accf = empty + a.stages;
+  uint64_t *acce = accf + 2;
+  uint64_t *fin = acce + 2;
+  uint32_t *tslot = reinterpret_cast<uint32_t *>(fin + 1);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    for (int s = 0; s < a.stages; ++s) {
+      mbar_init(&full[s], kShrinkProducers + 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&accf[i], 1);
+      mbar_init(&acce[i], 128);
+    }
+    mbar_init(fin, 1);
+    fence_mbar_init();
+  }
+  pdl_wait();
+  pdl_trigger();
+  if (warp == 8) tmem_alloc(tslot, (uint32_t)a.tmem_cols);
+  tc_before_sync();
+  __syncthreads();
+  tc_after_sync();
+  const uint32_t tmem = *tslot;
+  const int n_tiles = a.work[a.L.hdr_tiles];
+  const int n_list = a.work[a.L.hdr_segs];
+  const int KC = split_count(n_tiles, (int)gridDim.x, a.kcmax);
+  const int n_items = n_tiles * KC;
+
+  if (warp < 4) {
+    // ---- producers: x rows by cp.async (swizzled), A blocks by TMA (thread 0)
+    int issued = 0;
+    const int chunk = tid & 7;
+    bool ok = true;
+    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+      const int tile = it / KC, kc = it - tile * KC;
+      const TileInfo ti = tile_info(a.work, a.L, n_list, tile);
+      int tok[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int r = (tid >> 3) + 16 * i;
+        tok[i] = r < ti.rows ? a.sorted_rows[ti.pos0 + r] : -1;
+      }
+      const int kb0 = kc * a.nb / KC, kb1 = (kc + 1) * a.nb / KC;
+      for (int kb = kb0; kb < kb1; ++kb) {
+        const int s = issued % a.stages;
+        if (!mbar_wait_warp(&empty[s], ((issued / a.stages) & 1) ^ 1, a.err, kErrShrink)) {
+          ok = false;
+          break;
+        }
+        unsigned char *st = sm + s * a.stage_bytes;
+        if (tid == 0) {
+          mbar_arrive_tx(&full[s], (uint32_t)(a.n_slices * a.w_bytes));
+          for (int sl = 0; sl < a.n_slices; ++sl)
+            for (int bx = 0; bx * a.box_n < a.r_max; ++bx)
+              tma_load_3d(st + kTileM * 128 + sl * a.w_bytes + bx * (kKB * a.box_n * 2), &maps.m[sl],
+                          bx * a.box_n, kb * kKB, ti.slot, &full[s]);
+        }
+        const int col = kb * kKB + chunk * 8;
+        const bool col_ok = col < a.d_in;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int r = (tid >> 3) + 16 * i;
+          const bool v = col_ok && tok[i] >= 0;
+          const __nv_bfloat16 *src = v ? a.x + (int64_t)tok[i] * a.ldx + col : a.x;
+          cp_async16_zfill(st + swz128(r, chunk), src, v);
+        }
+        cp_async_commit();
+        ++issued;
+        if (issued > a.lag) {
+          cp_async_wait_upto(a.lag);
+          fence_async_smem();
+          mbar_arrive(&full[(issued - 1 - a.lag) % a.stages]);
+        }
+      }
+    }
+    cp_async_wait_upto(0);
+    fence_async_smem();
+    for (int j = issued - a.lag < 0 ? 0 : issued - a.lag; j < issued; ++j) mbar_arrive(&full[j % a.stages]);
+  } else if (warp < 8) {
+    // ---- epilogue: accumulator -> unscaled partial rows (thread = row)
+    const int q = warp & 3;
+    const int row = q * 32 + lane;
+    int nitem = 0;
+    for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+      const int tile = it / KC, kc = it - tile * KC;
+      const int acc = nitem % a.n_acc;
+      if (!mbar_wait_warp(&accf[acc], (nitem / a.n_acc) & 1, a.err, kErrShrink)) break;
+      tc_after_sync();
+      const uint32_t t0 = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * a.acc_cols);
+      for (int sl = 0; sl < a.n_slices; ++sl) {
+        float *dst = a.part + ((((int64_t)tile * KC + kc) * a.n_slices + sl) * kTileM + row) * a.r_max;
+        for (int c = 0; c < a.r_max; c += 16) {
+          float v[16];
+          tmem_ld16(t0 + (uint32_t)(sl * a.r_max + c), v);
+          float4 *d4 = reinterpret_cast<float4 *>(dst + c);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) d4[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+        }
+      }
+      tc_before_sync();
+      mbar_arrive(&acce[acc]);
+      ++nitem;
+    }
+  } else if (lane == 0) {
+    // ---- MMA issuer
+    const uint32_t idesc = idesc_bf16(kTileM, a.r_max);
+    const uint32_t sbo_w = 8u * a.box_n * 2, lbo_w = (uint32_t)kKB * a.box_n * 2;
+    int consumed = 0, nitem = 0;
+    bool ok = true;
+    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+      const int tile = it / KC, kc = it - tile * KC;
+      (void)tile;
+      const int kb0 = kc * a.nb / KC, kb1 = (kc + 1) * a.nb / KC;
+      const int acc = nitem % a.n_acc;
+      if (!mbar_wait(&acce[acc], ((nitem / a.n_acc) & 1) ^ 1, a.err, kErrShrink)) break;
+      tc_after_sync();
+      const uint32_t d0 = tmem + (uint32_t)(acc * a.acc_cols);
+      for (int kb = kb0; kb < kb1; ++kb) {
+        const int s = consumed % a.stages;
+        if (!mbar_wait(&full[s], (consumed / a.stages) & 1, a.err, kErrShrink)) {
+          ok = false;
+          break;
+        }
+        tc_after_sync();
+        const uint32_t xs = smem_addr(sm + s * a.stage_bytes);
+#pragma unroll
+        for (int kk = 0; kk < kKB / 16; ++kk) {
+          const uint64_t ad = smem_desc(xs + kk * 32, 16, 1024, kSw128);
+          for (int sl = 0; sl < a.n_slices; ++sl) {
+            const uint64_t bd = smem_desc(xs + kTileM * 128 + sl * a.w_bytes + kk * 2 * sbo_w, lbo_w, sbo_w,
+                                          a.w_layout);
+            mma_bf16(d0 + (uint32_t)(sl * a.r_max), ad, bd, idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
+          }
+        }
+        mma_commit(&empty[s]);
+        ++consumed;
+      }
+      if (!ok) break;
+      mma_commit(&accf[acc]);
+      ++nitem;
+    }
+    mma_commit(fin);
+    mbar_wait(fin, 0, a.err, kErrShrink);  // every MMA is done before TMEM is freed
+  }
+  tc_before_sync();
+  __syncthreads();
+  if (warp == 8) {
+    tc_after_sync();
+    tmem_free(tmem, (uint32_t)a.tmem_cols);
+  }
+}
+
+// ------------------------------------------------------------------ u rows (expand and reduce)
+
+struct URowArgs {
+  const float *src;  // partials [item][slice][128][r_max], or buf [n_s, T, r_max]
+  int parts;
+  int KC, n_slices, r_max, T;
+};
+
+// u[k] for 8 consecutive k (k0 multiple of 8) of one row: scale * the split
+// partials summed in split order (masked to the slot's rank), or the buffer.
+__device__ __forceinline__ void u_row8(const URowArgs &u, int tile, int slice, int row, int tok, int k0, int r_a,
+                                       float scale, float (&v)[8]) {
+  if (k0 >= r_a) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = 0.f;
+    return;
+  }
+  if (u.parts) {
+    float s[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) s[j] = 0.f;
+    for (int kc = 0; kc < u.KC; ++kc) {
+      const float4 *p = reinterpret_cast<const float4 *>(
+          u.src + ((((int64_t)tile * u.KC + kc) * u.n_slices + slice) * kTileM + row) * u.r_max + k0);
+      const float4 p0 = p[0], p1 = p[1];
+      s[0] += p0.x; s[1] += p0.y; s[2] += p0.z; s[3] += p0.w;
+      s[4] += p1.x; s[5] += p1.y; s[6] += p1.z; s[7] += p1.w;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = scale * s[j];
+  } else {
+    const float4 *p = reinterpret_cast<const float4 *>(u.src + ((int64_t)slice * u.T + tok) * u.r_max + k0);
+    const float4 p0 = p[0], p1 = p[1];
+    v[0] = p0.x; v[1] = p0.y; v[2] = p0.z; v[3] = p0.w;
+    v[4] = p1.x; v[5] = p1.y; v[6] = p1.z; v[7] = p1.w;
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    if (k0 + j >= r_a) v[j] = 0.f;
+}
+
+// ------------------------------------------------------------------ reduce (split path)
+
+struct SgReduceArgs {
+  URowArgs u;
+  float *buf;
+  const int32_t *work;
+  const int32_t *sorted_rows;
+  const int32_t *slot_rank;
+  const float *slot_scale;
+  int *err;
+  SgList L;
+  int shrink_grid, kcmax;
+};
+
+// Grid-stride over (tile, slice); thread = row.
+__global__ void __launch_bounds__(kTileM) sgmv_reduce_kernel(const SgReduceArgs a) {
+  pdl_wait();
+  pdl_trigger();
+  const int n_tiles = a.work[a.L.hdr_tiles];
+  const int n_list = a.work[a.L.hdr_segs];
+  URowArgs u = a.u;
+  u.KC = split_count(n_tiles, a.shrink_grid, a.kcmax);
+  const int row = threadIdx.x;
+  for (int p = blockIdx.x; p < n_tiles * u.n_slices; p += gridDim.x) {
+    const int tile = p / u.n_slices, slice = p - tile * u.n_slices;
+    const TileInfo ti = tile_info(a.work, a.L, n_list, tile);
+    if (row >= ti.rows) continue;
+    const int tok = a.sorted_rows[ti.pos0 + row];
+    const int r_a = min(max(a.slot_rank[ti.slot], 0), u.r_max);
+    const float scale = a.slot_scale[ti.slot];
+    float *dst = a.buf + ((int64_t)slice * u.T + tok) * u.r_max;
+    for (int k0 = 0; k0 < u.r_max; k0 += 8) {
+      float v[8];
+      u_row8(u, tile, slice, row, tok, k0, r_a, scale, v);
+      reinterpret_cast<float4 *>(dst + k0)[0] = make_float4(v[0], v[1], v[2], v[3]);
+      reinterpret_cast<float4 *>(dst + k0)[1] = make_float4(v[4], v[5], v[6], v[7]);
+    }
+  }
+}
+
+// ------------------------------------------------------------------ expand
+
+struct SgExpandArgs {
+  URowArgs u;
+  void *y;
+  int64_t ldy;
+  const int32_t *work;
+  const int32_t *sorted_rows;
+  const int32_t *slot_rank;
+  const float *slot_scale;
+  int *err;
+  SgList L;
+  int shrink_grid, kcmax;
+  int out_sizes[LORA_MAX_SLICES];
+  int out_off[LORA_MAX_SLICES];
+  int nb_start[LORA_MAX_SLICES + 1];  // column blocks per slice (cumulative)
+  int nk;                             // 64-wide K regions of the u operand (1 or 2)
+  int b_stages, y_stages, b_bytes;
+};
+
+constexpr int kExpandThreads = 320;  // epilogue 0-3, u builder 4-7, producer 8, MMA 9
+
+template <typename TY> struct YCols { static constexpr int kN = 256 / (int)sizeof(TY); };  // 256 bytes per row
+
+struct ExpandItem {
+  int tile, slice, n0, ncols, group;
+};
+
+__device__ __forceinline__ ExpandItem expand_item(const SgExpandArgs &a, int64_t it, int nbt, int kN, int n_slices) {
+  ExpandItem e;
+  e.tile = (int)(it / nbt);
+  const int j = (int)(it - (int64_t)e.tile * nbt);
+  int s = 0;
+  while (s + 1 < n_slices && j >= a.nb_start[s + 1]) ++s;
+  e.slice = s;
+  e.n0 = (j - a.nb_start[s]) * kN;
+  e.ncols = min(kN, a.out_sizes[s] - e.n0);
+  e.group = e.tile * n_slices + s;
+  return e;
+}
+
+template <typename TY>
+__global__ void __launch_bounds__(kExpandThreads, 1)
+    sgmv_expand_kernel(const __grid_constant__ SgMaps maps, const SgExpandArgs a) {
+  constexpr int kN = YCols<TY>::kN;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char *sm = align1024(smem_raw);
+  const int r_max = a.u.r_max, n_slices = a.u.n_slices;
+  unsigned char *sU = sm;                                  // hi: nk regions, then lo: nk regions
+  unsigned char *sB = sU + 2 * a.nk * kUKRegion;
+  unsigned char *sY = sB + a.b_stages * a.b_bytes;
+  uint64_t *bfull = reinterpret_cast<uint64_t *>(sY + a.y_stages * kYStage);
+  uint64_t *bempty = bfull + a.b_stages;
+  uint64_t *yfull = bempty + a.b_stages;
+  uint64_t *yempty = yfull + a.y_stages;
+  uint64_t *accf = yempty + a.y_stages;
+  uint64_t *acce = accf + 2;
+  uint64_t *ufull = acce + 2;
+  uint64_t *uempty = ufull + 1;
+  uint64_t *fin = uempty + 1;
+  uint32_t *tslot = reinterpret_cast<uint32_t *>(fin + 1);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    for (int s = 0; s < a.b_stages; ++s) {
+      mbar_init(&bfull[s], 1);
+      mbar_init(&bempty[s], 1);
+    }
+    for (int s = 0; s < a.y_stages; ++s) {
+      mbar_init(&yfull[s], 1);
+      mbar_init(&yempty[s], 128);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&accf[i], 1);
+      mbar_init(&acce[i], 128);
+    }
+    mbar_init(ufull, 128);
+    mbar_init(uempty, 1);
+    mbar_init(fin, 1);
+    fence_mbar_init();
+  }
+  pdl_wait();
+  pdl_trigger();
+  constexpr uint32_t kTmemCols = 2 * kN;
+  if (warp == 9) tmem_alloc(tslot, kTmemCols);
+  tc_before_sync();
+  __syncthreads();
+  tc_after_sync();
+  const uint32_t tmem = *tslot;
+  const int n_tiles = a.work[a.L.hdr_tiles];
+  const int n_list = a.work[a.L.hdr_segs];
+  const int nbt = a.nb_start[n_slices];
+  const int64_t n_items = (int64_t)n_tiles * nbt;
+  const int64_t it0 = n_items * blockIdx.x / gridDim.x, it1 = n_items * (blockIdx.x + 1) / gridDim.x;
+  TY *y = static_cast<TY *>(a.y);
+
+  if (warp < 4) {
+    // ---- epilogue: y_smem += accumulator, then one bulk store per row
+    const int row = warp * 32 + lane;
+    int cur_tile = -1, tok = -1, nitem = 0, prev_ys = -1;
+    for (int64_t it = it0; it < it1; ++it) {
+      const ExpandItem e = expand_item(a, it, nbt, kN, n_slices);
+      if (e.tile != cur_tile) {
+        const TileInfo ti = tile_info(a.work, a.L, n_list, e.tile);
+        tok = row < ti.rows ? a.sorted_rows[ti.pos0 + row] : -1;
+        cur_tile = e.tile;
+      }
+      const int acc = nitem & 1, ys = nitem % a.y_stages;
+      if (!mbar_wait_warp(&accf[acc], (nitem >> 1) & 1, a.err, kErrExpand)) break;
+      if (!mbar_wait_warp(&yfull[ys], (nitem / a.y_stages) & 1, a.err, kErrExpand)) break;
+      tc_after_sync();
+      const uint32_t t0 = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(acc * kN);
+      unsigned char *yrow = sY + ys * kYStage + row * kYPitch;
+      for (int c = 0; c < kN; c += 16) {
+        float v[16];
+        tmem_ld16(t0 + (uint32_t)c, v);
+        if (tok >= 0) {
+          if constexpr (sizeof(TY) == 2) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              if (c + 8 * h < e.ncols) {
+                uint4 *p = reinterpret_cast<uint4 *>(yrow + (c + 8 * h) * 2);
+                uint4 q = *p;
+                __nv_bfloat162 *b2 = reinterpret_cast<__nv_bfloat162 *>(&q);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                  const float2 f = __bfloat1622float2(b2[j]);
+                  b2[j] = __floats2bfloat162_rn(f.x + v[8 * h + 2 * j], f.y + v[8 * h + 2 * j + 1]);
+                }
+                *p = q;
+              }
+            }
+          } else {
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+              if (c + 4 * h < e.ncols) {
+                float4 *p = reinterpret_cast<float4 *>(yrow + (c + 4 * h) * 4);
+                float4 q = *p;
+                q.x += v[4 * h]; q.y += v[4 * h + 1]; q.z += v[4 * h + 2]; q.w += v[4 * h + 3];
+                *p = q;
+              }
+            }
+          }
+        }
+      }
+      tc_before_sync();
+      mbar_arrive(&acce[acc]);
+      if (tok >= 0) {
+        fence_async_smem();
+        bulk_store(y + (int64_t)tok * a.ldy + a.out_off[e.slice] + e.n0, yrow, (uint32_t)(e.ncols * sizeof(TY)));
+      }
+      bulk_commit();
+      bulk_wait_read_upto1();  // the previous item's store has read its stage
+      if (prev_ys >= 0) mbar_arrive(&yempty[prev_ys]);
+      prev_ys = ys;
+      ++nitem;
+    }
+    bulk_wait_all();
+    if (prev_ys >= 0) mbar_arrive(&yempty[prev_ys]);
+  } else if (warp < 8) {
+    // ---- u builder: one (tile, slice) at a time, thread = row
+    const int row = tid - 128;
+    URowArgs u = a.u;
+    u.KC = split_count(n_tiles, a.shrink_grid, a.kcmax);
+    int cur_group = -1, g = 0;
+    for (int64_t it = it0; it < it1; ++it) {
+      const ExpandItem e = expand_item(a, it, nbt, kN, n_slices);
+      if (e.group == cur_group) continue;
+      cur_group = e.group;
+      const TileInfo ti = tile_info(a.work, a.L, n_list, e.tile);
+      const int tok = row < ti.rows ? a.sorted_rows[ti.pos0 + row] : -1;
+      const int r_a = tok >= 0 ? min(max(a.slot_rank[ti.slot], 0), r_max) : 0;
+      const float scale = a.slot_scale[ti.slot];
+      if (!mbar_wait_warp(uempty, (g & 1) ^ 1, a.err, kErrExpand)) break;
+      for (int c = 0; c < r_max / 8; ++c) {
+        float v[8];
+        u_row8(u, e.tile, e.slice, row, tok, 8 * c, r_a, scale, v);
+        uint4 hi, lo;
+        __nv_bfloat162 *h2 = reinterpret_cast<__nv_bfloat162 *>(&hi);
+        __nv_bfloat162 *l2 = reinterpret_cast<__nv_bfloat162 *>(&lo);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * j], v[2 * j + 1]);
+          const float2 hf = __bfloat1622float2(h);
+          h2[j] = h;
+          l2[j] = __floats2bfloat162_rn(v[2 * j] - hf.x, v[2 * j + 1] - hf.y);
+        }
+        const uint32_t off = (uint32_t)((c >> 3) * kUKRegion) + swz128(row, c & 7);
+        *reinterpret_cast<uint4 *>(sU + off) = hi;
+        *reinterpret_cast<uint4 *>(sU + a.nk * kUKRegion + off) = lo;
+      }
+      fence_async_smem();
+      mbar_arrive(ufull);
+      ++g;
+    }
+  } else if (warp == 8) {
+    // ---- producer: B blocks by TMA, y rows by bulk copies
+    int cur_tile = -1, nitem = 0;
+    TileInfo ti{0, 0, 0};
+    int tok[4] = {-1, -1, -1, -1};
+    for (int64_t it = it0; it < it1; ++it) {
+      const ExpandItem e = expand_item(a, it, nbt, kN, n_slices);
+      if (e.tile != cur_tile) {
+        ti = tile_info(a.work, a.L, n_list, e.tile);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int r = lane + 32 * q;
+          tok[q] = r < ti.rows ? a.sorted_rows[ti.pos0 + r] : -1;
+        }
+        cur_tile = e.tile;
+      }
+      const int bs = nitem % a.b_stages, ys = nitem % a.y_stages;
+      if (!mbar_wait_warp(&bempty[bs], ((nitem / a.b_stages) & 1) ^ 1, a.err, kErrExpand)) break;
+      if (lane == 0) {
+        const int nbox = (e.ncols + 63) / 64;  // boxes entirely past the slice are not loaded
+        mbar_arrive_tx(&bfull[bs], (uint32_t)(nbox * r_max * 128));
+        for (int bx = 0; bx < nbox; ++bx)
+          tma_load_3d(sB + bs * a.b_bytes + bx * r_max * 128, &maps.m[e.slice], e.n0 + 64 * bx, 0, ti.slot,
+                      &bfull[bs]);
+      }
+      if (!mbar_wait_warp(&yempty[ys], ((nitem / a.y_stages) & 1) ^ 1, a.err, kErrExpand)) break;
+      const uint32_t row_bytes = (uint32_t)(e.ncols * sizeof(TY));
+      if (lane == 0) mbar_arrive_tx(&yfull[ys], (uint32_t)ti.rows * row_bytes);
+      __syncwarp();
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (tok[q] >= 0)
+          bulk_load(sY + ys * kYStage + (lane + 32 * q) * kYPitch,
+                    y + (int64_t)tok[q] * a.ldy + a.out_off[e.slice] + e.n0, row_bytes, &yfull[ys]);
+      ++nitem;
+    }
+  } else if (lane == 0) {
+    // ---- MMA issuer: acc = u_hi B + u_lo B, K = r_max each
+    const uint32_t idesc = idesc_bf16(kTileM, kN);
+    const uint32_t uhi = smem_addr(sU), ulo = uhi + (uint32_t)(a.nk * kUKRegion);
+    const uint32_t lbo_b = (uint32_t)r_max * 128;
+    const int ksteps = r_max / 16;
+    int cur_group = -1, g = 0, nitem = 0;
+    for (int64_t it = it0; it < it1; ++it) {
+      const ExpandItem e = expand_item(a, it, nbt, kN, n_slices);
+      if (e.group != cur_group) {
+        if (cur_group >= 0) mma_commit(uempty);  // the previous u rows are free once its MMAs finish
+        if (!mbar_wait(ufull, g & 1, a.err, kErrExpand)) break;
+        ++g;
+        cur_group = e.group;
+      }
+      const int acc = nitem & 1, bs = nitem % a.b_stages;
+      if (!mbar_wait(&acce[acc], ((nitem >> 1) & 1) ^ 1, a.err, kErrExpand)) break;
+      if (!mbar_wait(&bfull[bs], (nitem / a.b_stages) & 1, a.err, kErrExpand)) break;
+      tc_after_sync();
+      const uint32_t d = tmem + (uint32_t)(acc * kN);
+      const uint32_t bb = smem_addr(sB + bs * a.b_bytes);
+      for (int kk = 0; kk < ksteps; ++kk) {
+        const uint32_t ka = (uint32_t)((kk * 16) / 64 * kUKRegion + ((kk * 16) % 64) * 2);
+        const uint64_t bd = smem_desc(bb + kk * 2048, lbo_b, 1024, kSw128);
+        mma_bf16(d, smem_desc(uhi + ka, 16, 1024, kSw128), bd, idesc, kk > 0 ? 1u : 0u);
+      }
+      for (int kk = 0; kk < ksteps; ++kk) {
+        const uint32_t ka = (uint32_t)((kk * 16) / 64 * kUKRegion + ((kk * 16) % 64) * 2);
+        const uint64_t bd = smem_desc(bb + kk * 2048, lbo_b, 1024, kSw128);
+        mma_bf16(d, smem_desc(ulo + ka, 16, 1024, kSw128), bd, idesc, 1u);
+      }
+      mma_commit(&bempty[bs]);
+      mma_commit(&accf[acc]);
+      ++nitem;
+    }
+    mma_commit(fin);
+    mbar_wait(fin, 0, a.err, kErrExpand);  // every MMA is done before TMEM is freed
+  }
+  tc_before_sync();
+  __syncthreads();
+  if (warp == 9) {
+    tc_after_sync();
+    tmem_free(tmem, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+
+int sm_count() {
+  static std::mutex mu;
+  static std::map<int, int> cache;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = cache.find(dev);
+  if (it != cache.end()) return it->second;
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  cache[dev] = n;
+  return n;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 3-D bf16 tensor map {d0 (contiguous), d1, d2} with a {box0, box1, 1} box.
+cudaError_t make_map(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t box0,
+                     uint32_t box1, CUtensorMapSwizzle sw) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+  if (enc == nullptr) return cudaErrorNotSupported;
+  const cuuint64_t dims[3] = {d0, d1, d2};
+  const cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
+  const cuuint32_t box[3] = {box0, box1, 1};
+  const cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+SgList list_of(const MetaView &mv, ListSel sel) {
+  SgList L;
+  L.list = WorkLists::list(mv.num_slots, sel);
+  if (sel == kListLarge) {
+    L.ts = WorkLists::large_tile_start(mv.num_slots);
+    L.hdr_segs = 2;
+    L.hdr_tiles = 4;
+  } else {
+    L.ts = WorkLists::all_tile_start(mv.num_slots);
+    L.hdr_segs = 0;
+    L.hdr_tiles = 3;
+  }
+  return L;
+}
+
+int kcmax_of(const lora_layer_desc &d) {
+  const int nb = (d.d_in + kKB - 1) / kKB;
+  return nb < kKCMax ? nb : kKCMax;
+}
+
+// Upper bound on the tiles of any work list for T tokens and S slots.
+int64_t tiles_bound(int T, int S) { return (int64_t)T / kTileM + std::min<int64_t>(S - 1, T); }
+
+int shrink_grid() { return sm_count(); }
+
+}  // namespace
+
+bool sgmv_supported() { return encode_fn() != nullptr; }
+
+size_t sgmv_workspace_bytes(const lora_layer_desc &d, int max_tokens) {
+  if (max_tokens <= 0) return 0;
+  const int G = shrink_grid();
+  if (G <= 0) return 0;
+  const int64_t items = 2 * (int64_t)G + tiles_bound(max_tokens, d.num_slots);
+  return (size_t)items * d.n_slices * kTileM * d.r_max * sizeof(float);
+}
+
+cudaError_t launch_sgmv_shrink(const lora_layer_desc &d, const MetaView &mv, ListSel sel, const void *x, int64_t ldx,
+                               float *part, cudaStream_t st) {
+  if (mv.num_tokens <= 0 || mv.num_slots <= 1) return cudaSuccess;
+  SgMaps maps;
+  memset(&maps, 0, sizeof(maps));
+  SgShrinkArgs a{};
+  a.box_n = d.r_max < 64 ? d.r_max : 64;
+  const CUtensorMapSwizzle sw = a.box_n == 64 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                : a.box_n == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
+  a.w_layout = a.box_n == 64 ? kSw128 : a.box_n == 32 ? kSw64 : kSw32;
+  for (int s = 0; s < d.n_slices; ++s) {
+    cudaError_t e = make_map(&maps.m[s], d.A[s], (uint64_t)d.r_max, (uint64_t)d.d_in, (uint64_t)d.num_slots,
+                             (uint32_t)a.box_n, (uint32_t)kKB, sw);
+    if (e != cudaSuccess) return e;
+  }
+  a.x = static_cast<const __nv_bfloat16 *>(x);
+  a.ldx = ldx;
+  a.part = part;
+  a.work = mv.work;
+  a.sorted_rows = mv.sorted_rows;
+  a.err = const_cast<int32_t *>(mv.work) + WorkLists::kErrWord;
+  a.L = list_of(mv, sel);
+  a.d_in = d.d_in;
+  a.r_max = d.r_max;
+  a.n_slices = d.n_slices;
+  a.kcmax = kcmax_of(d);
+  a.nb = (d.d_in + kKB - 1) / kKB;
+  a.w_bytes = kKB * d.r_max * 2;
+  a.stage_bytes = kTileM * 128 + d.n_slices * a.w_bytes;
+  const int fixed = kAlignSlack + 256;
+  a.stages = std::min(6, (kSmemMax - fixed) / a.stage_bytes);
+  if (a.stages < 2) return cudaErrorInvalidValue;
+  a.lag = std::min(2, a.stages - 1);
+  a.acc_cols = d.n_slices * d.r_max;
+  a.n_acc = 2 * a.acc_cols <= 512 ? 2 : 1;
+  int cols = 32;
+  while (cols < a.n_acc * a.acc_cols) cols *= 2;
+  a.tmem_cols = cols;
+  const int smem = fixed + a.stages * a.stage_bytes;
+  cudaError_t e = set_max_dynamic_smem((const void *)sgmv_shrink_kernel, smem);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(sgmv_shrink_kernel, dim3((unsigned)shrink_grid()), dim3(kShrinkThreads), (size_t)smem, st, 1u,
+                    maps, a);
+}
+
+cudaError_t launch_sgmv_reduce(const lora_layer_desc &d, const MetaView &mv, ListSel sel, const float *part,
+                               float *buf, cudaStream_t st) {
+  if (mv.num_tokens <= 0 || mv.num_slots <= 1) return cudaSuccess;
+  SgReduceArgs a{};
+  a.u.src = part;
+  a.u.parts = 1;
+  a.u.n_slices = d.n_slices;
+  a.u.r_max = d.r_max;
+  a.u.T = mv.num_tokens;
+  a.buf = buf;
+  a.work = mv.work;
+  a.sorted_rows = mv.sorted_rows;
+  a.slot_rank = d.slot_rank;
+  a.slot_scale = d.slot_scale;
+  a.err = const_cast<int32_t *>(mv.work) + WorkLists::kErrWord;
+  a.L = list_of(mv, sel);
+  a.shrink_grid = shrink_grid();
+  a.kcmax = kcmax_of(d);
+  return launch_pdl(sgmv_reduce_kernel, dim3((unsigned)(2 * sm_count())), dim3(kTileM), 0, st, 1u, a);
+}
+
+cudaError_t launch_sgmv_expand(const lora_layer_desc &d, const MetaView &mv, ListSel sel, const float *u_src,
+                               int u_parts, void *y, int64_t ldy, int y_dtype, cudaStream_t st) {
+  if (mv.num_tokens <= 0 || mv.num_slots <= 1) return cudaSuccess;
+  const int kN = y_dtype == LORA_BF16 ? YCols<__nv_bfloat16>::kN : YCols<float>::kN;
+  SgMaps maps;
+  memset(&maps, 0, sizeof(maps));
+  for (int s = 0; s < d.n_slices; ++s) {
+    cudaError_t e = make_map(&maps.m[s], d.B[s], (uint64_t)d.out_sizes[s], (uint64_t)d.r_max, (uint64_t)d.num_slots,
+                             64u, (uint32_t)d.r_max, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (e != cudaSuccess) return e;
+  }
+  SgExpandArgs a{};
+  a.u.src = u_src;
+  a.u.parts = u_parts;
+  a.u.n_slices = d.n_slices;
+  a.u.r_max = d.r_max;
+  a.u.T = mv.num_tokens;
+  a.y = y;
+  a.ldy = ldy;
+  a.work = mv.work;
+  a.sorted_rows = mv.sorted_rows;
+  a.slot_rank = d.slot_rank;
+  a.slot_scale = d.slot_scale;
+  a.err = const_cast<int32_t *>(mv.work) + WorkLists::kErrWord;
+  a.L = list_of(mv, sel);
+  a.shrink_grid = shrink_grid();
+  a.kcmax = kcmax_of(d);
+  int off = 0, nb = 0;
+  for (int s = 0; s < d.n_slices; ++s) {
+    a.out_sizes[s] = d.out_sizes[s];
+    a.out_off[s] = off;
+    off += d.out_sizes[s];
+    a.nb_start[s] = nb;
+    nb += (d.out_sizes[s] + kN - 1) / kN;
+  }
+  a.nb_start[d.n_slices] = nb;
+  a.nk = d.r_max > 64 ? 2 : 1;
+  a.b_bytes = d.r_max * kN * 2;
+  const int fixed = kAlignSlack + 256 + 2 * a.nk * kUKRegion;
+  a.b_stages = 3;
+  a.y_stages = 3;
+  while (fixed + a.b_stages * a.b_bytes + a.y_stages * kYStage > kSmemMax && a.y_stages > 2) --a.y_stages;
+  while (fixed + a.b_stages * a.b_bytes + a.y_stages * kYStage > kSmemMax && a.b_stages > 2) --a.b_stages;
+  const int smem = fixed + a.b_stages * a.b_bytes + a.y_stages * kYStage;
+  if (smem > kSmemMax) return cudaErrorInvalidValue;
+  const void *k = y_dtype == LORA_BF16 ? (const void *)sgmv_expand_kernel<__nv_bfloat16>
+                                       : (const void *)sgmv_expand_kernel<float>;
+  cudaError_t e = set_max_dynamic_smem(k, smem);
+  if (e != cudaSuccess) return e;
+  const dim3 grid((unsigned)sm_count());
+  if (y_dtype == LORA_BF16)
+    return launch_pdl(sgmv_expand_kernel<__nv_bfloat16>, grid, dim3(kExpandThreads), (size_t)smem, st, 1u, maps, a);
+  return launch_pdl(sgmv_expand_kernel<float>, grid, dim3(kExpandThreads), (size_t)smem, st, 1u, maps, a);
 }
 
 }  // namespace ra

@@ -37,17 +37,17 @@ def test_every_declared_symbol_is_exported(ra):
 def test_header_constants_match_binding(ra):
     src = open(os.path.join(ROOT, "include", "lora.h")).read()
     for name in ("LORA_MAX_SLICES", "LORA_MAX_NUM_SLOTS", "LORA_MAX_RANK", "LORA_SGMV_MIN_ROWS",
-                 "LORA_SGMV_TILE_M"):
+                 "LORA_SGMV_TILE_M", "LORA_AUTO_SGMV_MIN_TOKENS"):
         m = re.search(rf"#define {name} (\d+)", src)
         assert m and int(m.group(1)) == getattr(ra, name), name
     for i, name in enumerate(["LORA_OK", "LORA_EINVAL", "LORA_ERANGE", "LORA_EALIGN", "LORA_EUNSUPPORTED",
-                              "LORA_ECUDA", "LORA_EBADSLOT"]):
+                              "LORA_ECUDA", "LORA_EBADSLOT", "LORA_EDEVICE"]):
         assert re.search(rf"{name} = {i}\b", src) and getattr(ra, name) == i
 
 
 def test_strerror_and_sizes(ra):
-    for s in range(7):
-        assert ra.lora_strerror(s)
+    for s in range(8):
+        assert ra.lora_strerror(s) and "unknown" not in ra.lora_strerror(s)
     assert "unknown" in ra.lora_strerror(99)
     assert ra.lora_meta_tiles_bytes(0) == 0
     assert ra.lora_meta_tiles_bytes(64) == (8 + 3 * 8 * 64 + 2 * 65 + 3 * 64) * 4
@@ -124,13 +124,21 @@ def test_shrink_expand_validation(ra):
     f = _desc(ra, dtype=ra.LORA_F32)
     assert ra.lora_shrink(f, m, 0x5000, 64, 0x6000, ra.LORA_SGMV, 0, 0, 0) == ra.LORA_EUNSUPPORTED
     assert ra.lora_expand(f, m, 0x6000, 0x7000, 64, ra.LORA_BF16, 1, 0) == ra.LORA_EUNSUPPORTED
+    r8 = _desc(ra, r_max=8)   # the tensor-core family needs r_max >= 16
+    assert ra.lora_shrink(r8, m, 0x5000, 64, 0x6000, ra.LORA_SGMV, 0, 0, 0) == ra.LORA_EUNSUPPORTED
+    assert ra.lora_expand(r8, m, 0x6000, 0x7000, 64, ra.LORA_BF16, ra.LORA_SGMV, 0) == ra.LORA_EUNSUPPORTED
+    assert ra.lora_apply(r8, m, 0x5000, 64, 0, 0x7000, 64, ra.LORA_BF16, ra.LORA_SGMV, 0, 0, 0) == \
+        ra.LORA_EUNSUPPORTED
+    assert ra.lora_workspace_bytes(r8, 256, ra.LORA_SGMV) == 0
     assert ra.lora_expand(d, m, 0x6000, 0x7000, 60, ra.LORA_BF16, 1, 0) == ra.LORA_EINVAL  # ldy < sum(out)
     assert ra.lora_expand(d, m, 0x6000, 0x7000, 64, 5, 1, 0) == ra.LORA_EINVAL
     m0 = _meta(ra, T=0)
     assert ra.lora_shrink(d, m0, 0, 64, 0, 1, 0, 0, 0) == ra.LORA_OK                   # T = 0: no-op
     assert ra.lora_expand(d, m0, 0, 0, 64, ra.LORA_BF16, 1, 0) == ra.LORA_OK
-    assert ra.lora_workspace_bytes(d, 1024, 0) == 2 * 1024 * 1 * 16 * 4   # d_in = 64: one chunk
+    assert ra.lora_workspace_bytes(d, 1024, ra.LORA_BGMV) == 2 * 1024 * 1 * 16 * 4   # d_in = 64: one chunk
+    assert ra.lora_workspace_bytes(d, 1000, ra.LORA_AUTO) == 2 * 1000 * 1 * 16 * 4   # < 1024 tokens: BGMV only
     assert ra.lora_workspace_bytes(d, 0, 0) == 0
+    assert ra.lora_workspace_bytes(d, 16, 7) == 0                                      # bad kind
     big = _desc(ra, d_in=4096, n_slices=3)
     nb = ra.lora_workspace_bytes(big, 256, 0)
     assert nb > 0 and nb % 16 == 0

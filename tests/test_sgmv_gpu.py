@@ -1,0 +1,183 @@
+"""The tensor-core (SGMV) family and the AUTO split against the fp64 oracle, through the C ABI.
+
+SGMV runs 128-row tiles of same-adapter segments on tcgen05 (split-K shrink
+over d_in, hi + lo bf16 expand). The cases cover tiles that end inside a
+segment and segments shorter than a tile, d_in and output widths that are not
+multiples of the K block or the column block, every supported r_max, one to
+four packed slices, padded leading dimensions, heterogeneous ranks with a
+scale, the full-size prefill batch (on sampled rows) and the full mixed batch
+under AUTO. Tolerances are those of the BGMV tests."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+from gpu_harness import TOL_BF16, bf16_half_ulp, load_table, parity, run_gpu, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def _status_ok(lib, meta):
+    st, n = lib.lora_query_status(meta.c)
+    assert st in (lib.LORA_OK, lib.LORA_EBADSLOT), lib.lora_strerror(st)
+
+
+@pytest.mark.parametrize("path", ["split", "apply"])
+@pytest.mark.parametrize("y_dtype", ["f32", "bf16"])
+def test_sgmv_prefill_small(lib, path, y_dtype):
+    inst = wl.make_instance("prefill_gate_up", num_tokens=1500, d_in=512, out_sizes=[640, 384], num_slots=9)
+    _, _, meta = parity(inst, kind=lib.LORA_SGMV, y_dtype=y_dtype, path=path)
+    _status_ok(lib, meta)
+
+
+def _segment_batch(sizes, S, rng):
+    """Token slots whose segments have the given sizes, interleaved with slot-0
+    tokens and split into several requests each, so sorted rows are not contiguous."""
+    reqs = []
+    for i, n in enumerate(sizes):
+        slot = 1 + i % (S - 1)
+        cuts = sorted(rng.choice(np.arange(1, n), size=min(3, n - 1), replace=False)) if n > 1 else []
+        for part in np.split(np.arange(n), cuts):
+            reqs.append(np.full(len(part), slot, np.int32))
+        reqs.append(np.zeros(rng.integers(0, 3), np.int32))
+    order = rng.permutation(len(reqs))
+    return np.concatenate([reqs[i] for i in order]).astype(np.int32)
+
+
+def test_sgmv_segment_and_tile_boundaries(lib):
+    rng = np.random.default_rng(11)
+    sizes = [1, 2, 63, 64, 65, 127, 128, 129, 255, 256, 257, 300]
+    ts = _segment_batch(sizes, 13, rng)
+    inst = wl.make_instance("decode_qkv", num_tokens=len(ts), d_in=320, out_sizes=[136, 72, 200], num_slots=13,
+                            r_max=32)
+    for path in ("split", "apply"):
+        _, _, meta = parity(inst, kind=lib.LORA_SGMV, token_slot=ts, path=path)
+        _status_ok(lib, meta)
+
+
+@pytest.mark.parametrize("r_max,n_slices", [(16, 1), (16, 4), (32, 2), (64, 3), (128, 1), (128, 2), (128, 4)])
+def test_sgmv_ranks_slices_ragged_shapes(lib, r_max, n_slices):
+    """d_in = 200 (not a multiple of the 64-wide K block), widths not multiples of the
+    128-column block, padded strides; ranks 1..r_max within one table."""
+    outs = [72, 200, 136, 64][:n_slices]
+    inst = wl.make_instance("decode_qkv", num_tokens=700, d_in=200, out_sizes=outs, num_slots=7, r_max=r_max)
+    rng = np.random.default_rng(r_max + n_slices)
+    for k, r in zip(sorted(inst.adapters), [1, r_max // 2 + 1, r_max, 7, r_max - 1, r_max]):
+        ad = inst.adapters[k]
+        inst.adapters[k] = wl.Adapter(r, 0.5 + k / 4, [a[:, :r].copy() for a in ad.A], [b[:r].copy() for b in ad.B])
+    ts = _segment_batch([150, 90, 300, 64, 96], 7, rng)
+    inst = _with_tokens(inst, ts, rng)
+    parity(inst, kind=lib.LORA_SGMV, token_slot=ts, ldx_pad=24, ldy_pad=8, path="apply")
+    parity(inst, kind=lib.LORA_SGMV, token_slot=ts, y_dtype="bf16", path="split")
+
+
+def _with_tokens(inst, ts, rng):
+    """The instance re-drawn at len(ts) tokens (x and y_in), adapters kept."""
+    T = len(ts)
+    inst.x = wl.bf16_bits_from_f32(rng.standard_normal((T, inst.d_in), dtype=np.float32))
+    inst.y_in = wl.bf16_bits_from_f32(rng.standard_normal((T, inst.d_out_total), dtype=np.float32))
+    inst.req_lengths, inst.req_slots = oracle.requests_of_token_slots(ts)
+    return inst
+
+
+def test_sgmv_heterogeneous_ranks_and_scale(lib):
+    """Ranks {8, 16, 32, 64} padded to 64 with scale 2 (the mixed batch's adapters), all through SGMV."""
+    inst = wl.make_instance("mixed_o_proj", num_tokens=600, d_in=1024, out_sizes=[768], num_slots=24)
+    parity(inst, kind=lib.LORA_SGMV, y_dtype="bf16", path="apply")
+    parity(inst, kind=lib.LORA_SGMV, path="split")
+
+
+def test_sgmv_apply_equals_split_bitwise_and_repeats(lib):
+    inst = wl.make_instance("prefill_gate_up", num_tokens=2000, d_in=768, out_sizes=[384, 256], num_slots=6)
+    t = load_table(inst)
+    b1, y1, _ = run_gpu(inst, table=t, kind=lib.LORA_SGMV, path="split", y_dtype="bf16")
+    b2, y2, _ = run_gpu(inst, table=t, kind=lib.LORA_SGMV, path="apply", y_dtype="bf16")
+    b3, y3, _ = run_gpu(inst, table=t, kind=lib.LORA_SGMV, path="apply", y_dtype="bf16")
+    assert np.array_equal(b1, b2, equal_nan=True) and np.array_equal(y1, y2)
+    assert np.array_equal(b2, b3, equal_nan=True) and np.array_equal(y2, y3)
+
+
+def test_sgmv_permutation_invariant(lib):
+    """Reordering requests permutes the outputs bitwise: a token's result does not
+    depend on where its row falls in a tile."""
+    inst = wl.make_instance("prefill_gate_up", num_tokens=1200, d_in=512, out_sizes=[256, 128], num_slots=5)
+    t = load_table(inst)
+    _, y1, _ = run_gpu(inst, table=t, kind=lib.LORA_SGMV, path="apply")
+    rng = np.random.default_rng(3)
+    order = rng.permutation(len(inst.req_lengths))
+    starts = np.concatenate([[0], np.cumsum(inst.req_lengths)])
+    perm = np.concatenate([np.arange(starts[i], starts[i + 1]) for i in order])
+    inst_p = wl.make_instance("prefill_gate_up", num_tokens=1200, d_in=512, out_sizes=[256, 128], num_slots=5)
+    inst_p.x, inst_p.y_in = inst.x[perm], inst.y_in[perm]
+    inst_p.req_lengths, inst_p.req_slots = inst.req_lengths[order], inst.req_slots[order]
+    _, y2, _ = run_gpu(inst_p, table=t, kind=lib.LORA_SGMV, path="apply")
+    assert np.array_equal(y1[perm], y2)
+
+
+def test_auto_mixed_full_size(lib):
+    """The mixed batch (3072 tokens, >= LORA_AUTO_SGMV_MIN_TOKENS): long segments on SGMV,
+    the rest on BGMV, in one call."""
+    inst = wl.make_instance("mixed_o_proj")
+    assert inst.num_tokens >= lib.LORA_AUTO_SGMV_MIN_TOKENS
+    t = load_table(inst)
+    _, y_auto, meta = parity(inst, kind=lib.LORA_AUTO, y_dtype="bf16", table=t, path="apply")
+    _status_ok(lib, meta)
+    parity(inst, kind=lib.LORA_AUTO, table=t, path="split")
+    # The long segments really ran on the tensor-core family: their rows differ
+    # (within tolerance) from the all-BGMV result somewhere.
+    _, y_bgmv, _ = run_gpu(inst, table=t, kind=lib.LORA_BGMV, y_dtype="bf16", path="apply")
+    counts = np.bincount(inst.token_slot, minlength=inst.num_slots)
+    long_rows = np.where((counts[inst.token_slot] >= lib.LORA_SGMV_MIN_ROWS) & (inst.token_slot > 0))[0]
+    assert len(long_rows) > 0
+    assert not np.array_equal(y_auto[long_rows], y_bgmv[long_rows])
+
+
+def test_auto_small_batches_stay_on_bgmv(lib):
+    """Below LORA_AUTO_SGMV_MIN_TOKENS, AUTO is the BGMV family bitwise; above it, a batch
+    with no long segment is too (the SGMV kernels find no tiles)."""
+    inst = wl.make_instance("prefill_gate_up", num_tokens=900, d_in=512, out_sizes=[256, 128], num_slots=5)
+    t = load_table(inst)
+    _, ya, _ = run_gpu(inst, table=t, kind=lib.LORA_AUTO, path="apply")
+    _, yb, _ = run_gpu(inst, table=t, kind=lib.LORA_BGMV, path="apply")
+    assert np.array_equal(ya, yb)
+    dec = wl.make_instance("decode_qkv", num_tokens=1100, d_in=512, out_sizes=[256], num_slots=64)
+    assert np.bincount(dec.token_slot)[1:].max() < lib.LORA_SGMV_MIN_ROWS
+    t2 = load_table(dec)
+    ba, ya, meta = run_gpu(dec, table=t2, kind=lib.LORA_AUTO, path="split")
+    bb, yb, _ = run_gpu(dec, table=t2, kind=lib.LORA_BGMV, path="split")
+    assert np.array_equal(ya, yb) and np.array_equal(ba, bb, equal_nan=True)
+    _status_ok(lib, meta)
+
+
+def test_sgmv_prefill_full_size_sampled(lib):
+    """The full prefill batch (gate_up 4096 -> 2 x 14336, r = 64, ~17k tokens) through
+    lora_apply with AUTO and a bf16 y, checked on sampled rows against the oracle run
+    on those rows alone (a token's delta depends only on its own row and slot)."""
+    inst = wl.make_instance("prefill_gate_up")
+    T, W = inst.num_tokens, inst.d_out_total
+    t = load_table(inst)
+    x = to_dev(inst.x, "bf16")
+    y = to_dev(inst.y_in, "bf16")
+    meta = lib.TokenMeta(T, inst.num_slots)
+    meta.prepare(torch.from_numpy(inst.token_slot).cuda())
+    lib.apply(t, meta, x, y, kind=lib.LORA_AUTO)
+    torch.cuda.synchronize()
+    _status_ok(lib, meta)
+    rng = np.random.default_rng(17)
+    rows = np.sort(rng.choice(T, size=128, replace=False))
+    rows[:2] = [0, T - 1]
+    y_gpu = y[torch.from_numpy(rows).cuda()].float().cpu().numpy().astype(np.float64)
+    ts = inst.token_slot[rows]
+    lengths, slots = oracle.requests_of_token_slots(ts)
+    ads = oracle.adapters_f64(inst)
+    x64 = inst.to_f32(inst.x[rows]).astype(np.float64)
+    y64 = inst.to_f32(inst.y_in[rows]).astype(np.float64)
+    buf, written = oracle.shrink_requests(x64, ads, inst.n_slices, inst.r_max, lengths, slots, inst.num_slots)
+    y_ref = oracle.expand_requests(buf, y64, ads, inst.out_sizes, lengths, slots, inst.num_slots)
+    assert written.all()
+    delta = y_ref - y64
+    rms = np.sqrt(np.mean(delta ** 2))
+    excess = np.abs(y_gpu - y_ref) - (TOL_BF16 * rms + bf16_half_ulp(y_ref))
+    assert excess.max() <= 0, f"max excess {excess.max():.3e} (RMS delta {rms:.3e})"
+    assert W == 28672
