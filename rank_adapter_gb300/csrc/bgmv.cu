@@ -527,8 +527,10 @@ Geo make_geo(const lora_layer_desc &d) {
 void fill_common(BgmvArgs &a, const lora_layer_desc &d, const MetaView &mv, ListSel sel) {
   a.list = WorkLists::list(mv.num_slots, sel);
   a.slot_rec = WorkLists::slot_rec(mv.num_slots, sel);
-  // Slot-indexed shrink CTAs when most slots are likely live in this batch.
-  a.by_slot = mv.num_tokens >= mv.num_slots - 1 ? 1 : 0;
+  // Slot-indexed shrink CTAs (A prefetched before the metadata is known) when
+  // most slots are likely live: a whole batch of at least one token per slot.
+  // A sub-list (AUTO's short segments) may hold few of them.
+  a.by_slot = sel == kListAll && mv.num_tokens >= mv.num_slots - 1 ? 1 : 0;
   a.n_slices = d.n_slices;
   a.max_items = std::min(mv.num_slots - 1, mv.num_tokens);
   a.mv = mv;

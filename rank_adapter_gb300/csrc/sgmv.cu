@@ -47,14 +47,11 @@ constexpr int kKCMax = 16;                // at most this many d_in splits
 constexpr int kSmemMax = 227 * 1024;
 constexpr int kAlignSlack = 1024;         // dynamic smem is re-aligned to 1024 bytes
 constexpr int kUKRegion = kTileM * 128;   // bytes of one 64-wide K region of a 128-row operand
-constexpr int kYPitch = 272;              // bytes per staged y row: 256 + 16 (bank spread)
-constexpr int kYStage = kTileM * kYPitch;
 constexpr uint64_t kWaitNs = 200000000ull;  // a pipeline wait longer than 200 ms means a fault
 
 // Error bits in the work-list header (word WorkLists::kErrWord).
 constexpr int kErrShrink = 1;
 constexpr int kErrExpand = 2;
-constexpr int kErrReduce = 4;
 
 // Shared-memory descriptor layouts.
 constexpr uint32_t kSw128 = 2, kSw64 = 4, kSw32 = 6;
@@ -116,17 +113,6 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, i
       ::"r"(smem_addr(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_addr(bar))
       : "memory");
 }
-__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-               ::"r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar)) : "memory");
-}
-__device__ __forceinline__ void bulk_store(void *dst, const void *src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
-               ::"l"(dst), "r"(smem_addr(src)), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_read_upto1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 // 16-byte cp.async that writes zeros when !valid (nothing is read then).
 __device__ __forceinline__ void cp_async16_zfill(void *dst, const void *src, bool valid) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;"
@@ -168,6 +154,23 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
 #pragma unroll
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
+
+// 32 consecutive fp32 accumulator columns, without waiting (see tmem_wait_ld).
+__device__ __forceinline__ void tmem_ld32_async(uint32_t taddr, float *v) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // Shared-memory matrix descriptor (start, leading / stride byte offsets, swizzle).
 // For the swizzled MN-major operands here the leading offset is the distance
@@ -513,7 +516,14 @@ struct SgExpandArgs {
   int b_stages, y_stages, b_bytes;
 };
 
-constexpr int kExpandThreads = 320;  // epilogue 0-3, u builder 4-7, producer 8, MMA 9
+struct SgExpandMaps {
+  CUtensorMap b[LORA_MAX_SLICES];  // B[s] as {out_s, r_max, slots}, boxes of 64 columns x r_max rows
+  CUtensorMap y;                   // y as {sum(out_sizes), T}, boxes of 128 bytes x 128 rows
+};
+
+constexpr int kExpandThreads = 448;  // epilogue 0-7, loaders (u rows, gathered y rows) 8-11, producer 12, MMA 13
+constexpr int kYHalf = kTileM * 128;  // one half (128 bytes per row) of a staged y tile
+constexpr int kYStage = 2 * kYHalf;   // a staged y tile: 128 rows x 256 bytes
 
 template <typename TY> struct YCols { static constexpr int kN = 256 / (int)sizeof(TY); };  // 256 bytes per row
 
@@ -534,10 +544,46 @@ __device__ __forceinline__ ExpandItem expand_item(const SgExpandArgs &a, int64_t
   return e;
 }
 
+// Offset of 16-byte chunk g (0..15) of row r in a staged y tile: two halves
+// of 128-byte rows in the 128-byte swizzle that the tile copy writes.
+__device__ __forceinline__ uint32_t ychunk(int r, int g) {
+  return (uint32_t)((g >> 3) * kYHalf + r * 128 + (((g & 7) ^ (r & 7)) << 4));
+}
+
+// A tile and whether its rows are one run of consecutive tokens (then its y
+// rows arrive as two TMA tile copies; otherwise loader warps gather them).
+struct TileRows {
+  int tile = -1;
+  TileInfo ti{0, 0, 0};
+  int tok0 = 0;
+  bool contiguous = false;
+  __device__ __forceinline__ bool at(const SgExpandArgs &a, int n_list, int t) {
+    if (t == tile) return false;
+    ti = tile_info(a.work, a.L, n_list, t);
+    tok0 = a.sorted_rows[ti.pos0];
+    contiguous = a.sorted_rows[ti.pos0 + ti.rows - 1] - tok0 == ti.rows - 1;
+    tile = t;
+    return true;
+  }
+};
+
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int c0, int c1, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+      ::"r"(smem_addr(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_addr(bar))
+      : "memory");
+}
+// The barrier receives this thread's arrival once its earlier cp.async copies are complete.
+__device__ __forceinline__ void cp_async_arrive(uint64_t *bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
 template <typename TY>
 __global__ void __launch_bounds__(kExpandThreads, 1)
-    sgmv_expand_kernel(const __grid_constant__ SgMaps maps, const SgExpandArgs a) {
-  constexpr int kN = YCols<TY>::kN;
+    sgmv_expand_kernel(const __grid_constant__ SgExpandMaps maps, const SgExpandArgs a) {
+  constexpr int kN = YCols<TY>::kN;           // columns per item (256 bytes of a y row)
+  constexpr int kVec = 16 / (int)sizeof(TY);  // y elements per 16-byte chunk
+  constexpr int kHalf = kN / 2;               // columns per epilogue warp (one staged half)
   extern __shared__ unsigned char smem_raw[];
   unsigned char *sm = align1024(smem_raw);
   const int r_max = a.u.r_max, n_slices = a.u.n_slices;
@@ -548,7 +594,8 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
   uint64_t *bempty = bfull + a.b_stages;
   uint64_t *yfull = bempty + a.b_stages;
   uint64_t *yempty = yfull + a.y_stages;
-  uint64_t *accf = yempty + a.y_stages;
+  uint64_t *ydone = yempty + a.y_stages;  // [stage][quadrant]: both column halves of 32 rows updated
+  uint64_t *accf = ydone + 4 * a.y_stages;
   uint64_t *acce = accf + 2;
   uint64_t *ufull = acce + 2;
   uint64_t *uempty = ufull + 1;
@@ -561,12 +608,13 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
       mbar_init(&bempty[s], 1);
     }
     for (int s = 0; s < a.y_stages; ++s) {
-      mbar_init(&yfull[s], 1);
-      mbar_init(&yempty[s], 128);
+      mbar_init(&yfull[s], 1 + 128);  // the producer + every loader thread
+      mbar_init(&yempty[s], 256);
+      for (int q = 0; q < 4; ++q) mbar_init(&ydone[4 * s + q], 64);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&accf[i], 1);
-      mbar_init(&acce[i], 128);
+      mbar_init(&acce[i], 256);
     }
     mbar_init(ufull, 128);
     mbar_init(uempty, 1);
@@ -576,7 +624,7 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
   pdl_wait();
   pdl_trigger();
   constexpr uint32_t kTmemCols = 2 * kN;
-  if (warp == 9) tmem_alloc(tslot, kTmemCols);
+  if (warp == 13) tmem_alloc(tslot, kTmemCols);
   tc_before_sync();
   __syncthreads();
   tc_after_sync();
@@ -588,139 +636,173 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
   const int64_t it0 = n_items * blockIdx.x / gridDim.x, it1 = n_items * (blockIdx.x + 1) / gridDim.x;
   TY *y = static_cast<TY *>(a.y);
 
-  if (warp < 4) {
-    // ---- epilogue: y_smem += accumulator, then one bulk store per row
-    const int row = warp * 32 + lane;
-    int cur_tile = -1, tok = -1, nitem = 0, prev_ys = -1;
+  if (warp < 8) {
+    // ---- epilogue. Warp w adds accumulator lanes 32 (w % 4), column half
+    // w / 4, into the staged rows (thread = row); then the two warps of a
+    // quadrant store its 32 rows with coalesced 16-byte stores.
+    const int q = warp & 3, h = warp >> 2;
+    const int row = q * 32 + lane;
+    const int g_st = lane & 15;  // chunk this lane stores
+    int cur_tile = -1, tok = -1, nitem = 0;
+    int stok[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) stok[i] = -1;
     for (int64_t it = it0; it < it1; ++it) {
       const ExpandItem e = expand_item(a, it, nbt, kN, n_slices);
       if (e.tile != cur_tile) {
         const TileInfo ti = tile_info(a.work, a.L, n_list, e.tile);
         tok = row < ti.rows ? a.sorted_rows[ti.pos0 + row] : -1;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int r = 32 * q + 16 * h + 2 * i + (lane >> 4);
+          stok[i] = r < ti.rows ? a.sorted_rows[ti.pos0 + r] : -1;
+        }
         cur_tile = e.tile;
       }
       const int acc = nitem & 1, ys = nitem % a.y_stages;
+      const uint32_t par = (nitem / a.y_stages) & 1;
       if (!mbar_wait_warp(&accf[acc], (nitem >> 1) & 1, a.err, kErrExpand)) break;
-      if (!mbar_wait_warp(&yfull[ys], (nitem / a.y_stages) & 1, a.err, kErrExpand)) break;
       tc_after_sync();
-      const uint32_t t0 = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(acc * kN);
-      unsigned char *yrow = sY + ys * kYStage + row * kYPitch;
-      for (int c = 0; c < kN; c += 16) {
-        float v[16];
-        tmem_ld16(t0 + (uint32_t)c, v);
-        if (tok >= 0) {
-          if constexpr (sizeof(TY) == 2) {
+      float v[kHalf];
+      const uint32_t t0 = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kN + h * kHalf);
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              if (c + 8 * h < e.ncols) {
-                uint4 *p = reinterpret_cast<uint4 *>(yrow + (c + 8 * h) * 2);
-                uint4 q = *p;
-                __nv_bfloat162 *b2 = reinterpret_cast<__nv_bfloat162 *>(&q);
+      for (int c = 0; c < kHalf; c += 32) tmem_ld32_async(t0 + (uint32_t)c, v + c);
+      tmem_wait_ld();
+      tc_before_sync();
+      mbar_arrive(&acce[acc]);
+      if (!mbar_wait_warp(&yfull[ys], par, a.err, kErrExpand)) break;
+      unsigned char *st = sY + ys * kYStage;
+      if (tok >= 0) {
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                  const float2 f = __bfloat1622float2(b2[j]);
-                  b2[j] = __floats2bfloat162_rn(f.x + v[8 * h + 2 * j], f.y + v[8 * h + 2 * j + 1]);
-                }
-                *p = q;
+        for (int g = 0; g < 8; ++g) {
+          if (h * kHalf + g * kVec < e.ncols) {
+            uint4 *p = reinterpret_cast<uint4 *>(st + ychunk(row, 8 * h + g));
+            uint4 w = *p;
+            if constexpr (sizeof(TY) == 2) {
+              __nv_bfloat162 *b2 = reinterpret_cast<__nv_bfloat162 *>(&w);
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const float2 f = __bfloat1622float2(b2[j]);
+                b2[j] = __floats2bfloat162_rn(f.x + v[g * 8 + 2 * j], f.y + v[g * 8 + 2 * j + 1]);
               }
-            }
-          } else {
+            } else {
+              float *f = reinterpret_cast<float *>(&w);
 #pragma unroll
-            for (int h = 0; h < 4; ++h) {
-              if (c + 4 * h < e.ncols) {
-                float4 *p = reinterpret_cast<float4 *>(yrow + (c + 4 * h) * 4);
-                float4 q = *p;
-                q.x += v[4 * h]; q.y += v[4 * h + 1]; q.z += v[4 * h + 2]; q.w += v[4 * h + 3];
-                *p = q;
-              }
+              for (int j = 0; j < 4; ++j) f[j] += v[g * 4 + j];
             }
+            *p = w;
           }
         }
       }
-      tc_before_sync();
-      mbar_arrive(&acce[acc]);
-      if (tok >= 0) {
-        fence_async_smem();
-        bulk_store(y + (int64_t)tok * a.ldy + a.out_off[e.slice] + e.n0, yrow, (uint32_t)(e.ncols * sizeof(TY)));
+      mbar_arrive(&ydone[4 * ys + q]);
+      if (!mbar_wait_warp(&ydone[4 * ys + q], par, a.err, kErrExpand)) break;
+      TY *ybase = y + a.out_off[e.slice] + e.n0 + g_st * kVec;
+      if (g_st * kVec < e.ncols) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int r = 32 * q + 16 * h + 2 * i + (lane >> 4);
+          if (stok[i] >= 0)
+            *reinterpret_cast<uint4 *>(ybase + (int64_t)stok[i] * a.ldy) =
+                *reinterpret_cast<const uint4 *>(st + ychunk(r, g_st));
+        }
       }
-      bulk_commit();
-      bulk_wait_read_upto1();  // the previous item's store has read its stage
-      if (prev_ys >= 0) mbar_arrive(&yempty[prev_ys]);
-      prev_ys = ys;
+      mbar_arrive(&yempty[ys]);
       ++nitem;
     }
-    bulk_wait_all();
-    if (prev_ys >= 0) mbar_arrive(&yempty[prev_ys]);
-  } else if (warp < 8) {
-    // ---- u builder: one (tile, slice) at a time, thread = row
-    const int row = tid - 128;
+  } else if (warp < 12) {
+    // ---- loaders: the u rows of each (tile, slice) (thread = row), and the
+    // y rows of tiles that are not one run of tokens (16-byte cp.async,
+    // lanes along a row)
+    const int lt = tid - 256;
+    const int wb = lt >> 5;
     URowArgs u = a.u;
     u.KC = split_count(n_tiles, a.shrink_grid, a.kcmax);
-    int cur_group = -1, g = 0;
+    int cur_group = -1, g = 0, nitem = 0;
+    TileRows tr;
+    int ltok[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) ltok[i] = -1;
     for (int64_t it = it0; it < it1; ++it) {
       const ExpandItem e = expand_item(a, it, nbt, kN, n_slices);
-      if (e.group == cur_group) continue;
-      cur_group = e.group;
-      const TileInfo ti = tile_info(a.work, a.L, n_list, e.tile);
-      const int tok = row < ti.rows ? a.sorted_rows[ti.pos0 + row] : -1;
-      const int r_a = tok >= 0 ? min(max(a.slot_rank[ti.slot], 0), r_max) : 0;
-      const float scale = a.slot_scale[ti.slot];
-      if (!mbar_wait_warp(uempty, (g & 1) ^ 1, a.err, kErrExpand)) break;
-      for (int c = 0; c < r_max / 8; ++c) {
-        float v[8];
-        u_row8(u, e.tile, e.slice, row, tok, 8 * c, r_a, scale, v);
-        uint4 hi, lo;
-        __nv_bfloat162 *h2 = reinterpret_cast<__nv_bfloat162 *>(&hi);
-        __nv_bfloat162 *l2 = reinterpret_cast<__nv_bfloat162 *>(&lo);
+      if (tr.at(a, n_list, e.tile)) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * j], v[2 * j + 1]);
-          const float2 hf = __bfloat1622float2(h);
-          h2[j] = h;
-          l2[j] = __floats2bfloat162_rn(v[2 * j] - hf.x, v[2 * j + 1] - hf.y);
+        for (int i = 0; i < 16; ++i) {
+          const int r = 8 * i + 2 * wb + (lane >> 4);
+          ltok[i] = r < tr.ti.rows ? a.sorted_rows[tr.ti.pos0 + r] : -1;
         }
-        const uint32_t off = (uint32_t)((c >> 3) * kUKRegion) + swz128(row, c & 7);
-        *reinterpret_cast<uint4 *>(sU + off) = hi;
-        *reinterpret_cast<uint4 *>(sU + a.nk * kUKRegion + off) = lo;
       }
-      fence_async_smem();
-      mbar_arrive(ufull);
-      ++g;
+      if (e.group != cur_group) {
+        cur_group = e.group;
+        const int tok = lt < tr.ti.rows ? a.sorted_rows[tr.ti.pos0 + lt] : -1;
+        const int r_a = tok >= 0 ? min(max(a.slot_rank[tr.ti.slot], 0), r_max) : 0;
+        const float scale = a.slot_scale[tr.ti.slot];
+        if (!mbar_wait_warp(uempty, (g & 1) ^ 1, a.err, kErrExpand)) break;
+        for (int c = 0; c < r_max / 8; ++c) {
+          float v[8];
+          u_row8(u, e.tile, e.slice, lt, tok, 8 * c, r_a, scale, v);
+          uint4 hi, lo;
+          __nv_bfloat162 *h2 = reinterpret_cast<__nv_bfloat162 *>(&hi);
+          __nv_bfloat162 *l2 = reinterpret_cast<__nv_bfloat162 *>(&lo);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const __nv_bfloat162 hh = __floats2bfloat162_rn(v[2 * j], v[2 * j + 1]);
+            const float2 hf = __bfloat1622float2(hh);
+            h2[j] = hh;
+            l2[j] = __floats2bfloat162_rn(v[2 * j] - hf.x, v[2 * j + 1] - hf.y);
+          }
+          const uint32_t off = (uint32_t)((c >> 3) * kUKRegion) + swz128(lt, c & 7);
+          *reinterpret_cast<uint4 *>(sU + off) = hi;
+          *reinterpret_cast<uint4 *>(sU + a.nk * kUKRegion + off) = lo;
+        }
+        fence_async_smem();
+        mbar_arrive(ufull);
+        ++g;
+      }
+      const int ys = nitem % a.y_stages;
+      if (!mbar_wait_warp(&yempty[ys], ((nitem / a.y_stages) & 1) ^ 1, a.err, kErrExpand)) break;
+      if (!tr.contiguous) {
+        unsigned char *st = sY + ys * kYStage;
+        const int gg = lane & 15;
+        const bool col_ok = gg * kVec < e.ncols;
+        const TY *src0 = y + a.out_off[e.slice] + e.n0 + gg * kVec;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int r = 8 * i + 2 * wb + (lane >> 4);
+          if (col_ok && ltok[i] >= 0) cp_async16(st + ychunk(r, gg), src0 + (int64_t)ltok[i] * a.ldy);
+        }
+      }
+      cp_async_arrive(&yfull[ys]);
+      ++nitem;
     }
-  } else if (warp == 8) {
-    // ---- producer: B blocks by TMA, y rows by bulk copies
-    int cur_tile = -1, nitem = 0;
-    TileInfo ti{0, 0, 0};
-    int tok[4] = {-1, -1, -1, -1};
+    asm volatile("cp.async.wait_all;" ::: "memory");
+  } else if (warp == 12) {
+    // ---- producer: B blocks, and y rows of contiguous tiles, by TMA
+    TileRows tr;
+    int nitem = 0;
     for (int64_t it = it0; it < it1; ++it) {
       const ExpandItem e = expand_item(a, it, nbt, kN, n_slices);
-      if (e.tile != cur_tile) {
-        ti = tile_info(a.work, a.L, n_list, e.tile);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int r = lane + 32 * q;
-          tok[q] = r < ti.rows ? a.sorted_rows[ti.pos0 + r] : -1;
-        }
-        cur_tile = e.tile;
-      }
+      tr.at(a, n_list, e.tile);
       const int bs = nitem % a.b_stages, ys = nitem % a.y_stages;
       if (!mbar_wait_warp(&bempty[bs], ((nitem / a.b_stages) & 1) ^ 1, a.err, kErrExpand)) break;
       if (lane == 0) {
         const int nbox = (e.ncols + 63) / 64;  // boxes entirely past the slice are not loaded
         mbar_arrive_tx(&bfull[bs], (uint32_t)(nbox * r_max * 128));
         for (int bx = 0; bx < nbox; ++bx)
-          tma_load_3d(sB + bs * a.b_bytes + bx * r_max * 128, &maps.m[e.slice], e.n0 + 64 * bx, 0, ti.slot,
+          tma_load_3d(sB + bs * a.b_bytes + bx * r_max * 128, &maps.b[e.slice], e.n0 + 64 * bx, 0, tr.ti.slot,
                       &bfull[bs]);
       }
       if (!mbar_wait_warp(&yempty[ys], ((nitem / a.y_stages) & 1) ^ 1, a.err, kErrExpand)) break;
-      const uint32_t row_bytes = (uint32_t)(e.ncols * sizeof(TY));
-      if (lane == 0) mbar_arrive_tx(&yfull[ys], (uint32_t)ti.rows * row_bytes);
-      __syncwarp();
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-        if (tok[q] >= 0)
-          bulk_load(sY + ys * kYStage + (lane + 32 * q) * kYPitch,
-                    y + (int64_t)tok[q] * a.ldy + a.out_off[e.slice] + e.n0, row_bytes, &yfull[ys]);
+      if (lane == 0) {
+        if (tr.contiguous) {
+          const int halves = e.ncols > kHalf ? 2 : 1;
+          unsigned char *st = sY + ys * kYStage;
+          mbar_arrive_tx(&yfull[ys], (uint32_t)(halves * kYHalf));
+          for (int hh = 0; hh < halves; ++hh)
+            tma_load_2d(st + hh * kYHalf, &maps.y, a.out_off[e.slice] + e.n0 + hh * kHalf, tr.tok0, &yfull[ys]);
+        } else {
+          mbar_arrive(&yfull[ys]);
+        }
+      }
       ++nitem;
     }
   } else if (lane == 0) {
@@ -763,7 +845,7 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
   }
   tc_before_sync();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == 13) {
     tc_after_sync();
     tmem_free(tmem, kTmemCols);
   }
@@ -810,6 +892,22 @@ cudaError_t make_map(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1,
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, es,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// 2-D tensor map of a row-major matrix {cols (contiguous), rows} with row
+// stride `ld` elements, 128-byte x 128-row boxes in the 128-byte swizzle.
+cudaError_t make_rows_map(CUtensorMap *m, const void *base, bool bf16, uint64_t cols, uint64_t rows, int64_t ld) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+  if (enc == nullptr) return cudaErrorNotSupported;
+  const uint64_t es = bf16 ? 2 : 4;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)ld * es};
+  const cuuint32_t box[2] = {(cuuint32_t)(128 / es), (cuuint32_t)kTileM};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+                   const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
@@ -882,7 +980,7 @@ cudaError_t launch_sgmv_shrink(const lora_layer_desc &d, const MetaView &mv, Lis
   const int fixed = kAlignSlack + 256;
   a.stages = std::min(6, (kSmemMax - fixed) / a.stage_bytes);
   if (a.stages < 2) return cudaErrorInvalidValue;
-  a.lag = std::min(2, a.stages - 1);
+  a.lag = a.stages - 1;  // every stage may be in flight
   a.acc_cols = d.n_slices * d.r_max;
   a.n_acc = 2 * a.acc_cols <= 512 ? 2 : 1;
   int cols = 32;
@@ -920,13 +1018,17 @@ cudaError_t launch_sgmv_expand(const lora_layer_desc &d, const MetaView &mv, Lis
                                int u_parts, void *y, int64_t ldy, int y_dtype, cudaStream_t st) {
   if (mv.num_tokens <= 0 || mv.num_slots <= 1) return cudaSuccess;
   const int kN = y_dtype == LORA_BF16 ? YCols<__nv_bfloat16>::kN : YCols<float>::kN;
-  SgMaps maps;
+  SgExpandMaps maps;
   memset(&maps, 0, sizeof(maps));
+  int64_t width = 0;
   for (int s = 0; s < d.n_slices; ++s) {
-    cudaError_t e = make_map(&maps.m[s], d.B[s], (uint64_t)d.out_sizes[s], (uint64_t)d.r_max, (uint64_t)d.num_slots,
+    cudaError_t e = make_map(&maps.b[s], d.B[s], (uint64_t)d.out_sizes[s], (uint64_t)d.r_max, (uint64_t)d.num_slots,
                              64u, (uint32_t)d.r_max, CU_TENSOR_MAP_SWIZZLE_128B);
     if (e != cudaSuccess) return e;
+    width += d.out_sizes[s];
   }
+  cudaError_t em = make_rows_map(&maps.y, y, y_dtype == LORA_BF16, (uint64_t)width, (uint64_t)mv.num_tokens, ldy);
+  if (em != cudaSuccess) return em;
   SgExpandArgs a{};
   a.u.src = u_src;
   a.u.parts = u_parts;
@@ -954,9 +1056,9 @@ cudaError_t launch_sgmv_expand(const lora_layer_desc &d, const MetaView &mv, Lis
   a.nb_start[d.n_slices] = nb;
   a.nk = d.r_max > 64 ? 2 : 1;
   a.b_bytes = d.r_max * kN * 2;
-  const int fixed = kAlignSlack + 256 + 2 * a.nk * kUKRegion;
+  const int fixed = kAlignSlack + 512 + 2 * a.nk * kUKRegion;  // 512: barriers
   a.b_stages = 3;
-  a.y_stages = 3;
+  a.y_stages = 4;
   while (fixed + a.b_stages * a.b_bytes + a.y_stages * kYStage > kSmemMax && a.y_stages > 2) --a.y_stages;
   while (fixed + a.b_stages * a.b_bytes + a.y_stages * kYStage > kSmemMax && a.b_stages > 2) --a.b_stages;
   const int smem = fixed + a.b_stages * a.b_bytes + a.y_stages * kYStage;
