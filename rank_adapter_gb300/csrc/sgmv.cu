@@ -43,7 +43,6 @@ namespace {
 
 constexpr int kTileM = LORA_SGMV_TILE_M;  // rows per tile (and MMA M)
 constexpr int kKB = 64;                   // d_in elements per shrink K block (one 128-byte swizzle row)
-constexpr int kKCMax = 16;                // at most this many d_in splits
 constexpr int kSmemMax = 227 * 1024;
 constexpr int kAlignSlack = 1024;         // dynamic smem is re-aligned to 1024 bytes
 constexpr int kUKRegion = kTileM * 128;   // bytes of one 64-wide K region of a 128-row operand
@@ -107,6 +106,12 @@ __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.a
 __device__ __forceinline__ void tc_before_sync() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_after_sync() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int c0, int c1, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+      ::"r"(smem_addr(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_addr(bar))
+      : "memory");
+}
 __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, int c0, int c1, int c2, uint64_t *bar) {
   asm volatile(
       "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
@@ -203,12 +208,25 @@ struct SgList {
   int hdr_tiles; // header word: tiles in the list
 };
 
-// d_in splits of the shrink for a tile count (the expand and reduce use the same).
-__host__ __device__ __forceinline__ int split_count(int n_tiles, int grid, int kcmax) {
-  if (n_tiles <= 0) return 1;
-  int kc = (2 * grid + n_tiles - 1) / n_tiles;
-  return kc < 1 ? 1 : (kc > kcmax ? kcmax : kc);
-}
+// The shrink's work: the flattened space of (tile, K block of 64) units,
+// U = n_tiles * nb, cut into G contiguous ranges whose sizes differ by at most
+// one unit (one per CTA). A CTA's range covers pieces of one or more tiles;
+// each piece leaves an unscaled partial at (CTA, piece index in the CTA), and
+// a tile's rank-r rows are the sum of its pieces in CTA order.
+// At most kMaxFanIn CTAs share a tile (fewer CTAs work when tiles are few),
+// which bounds the partials a u row sums.
+constexpr int kMaxFanIn = 4;
+struct Split {
+  int64_t U;
+  int G, nb, maxp;  // G: CTAs that take part; maxp: pieces per CTA the workspace holds
+  __host__ __device__ __forceinline__ static Split of(int n_tiles, int grid, int nb, int maxp) {
+    const int64_t cap = (int64_t)n_tiles * kMaxFanIn;
+    return Split{(int64_t)n_tiles * nb, (int)(cap < grid ? (cap > 0 ? cap : 1) : grid), nb, maxp};
+  }
+  __host__ __device__ __forceinline__ int64_t u0(int c) const { return c < G ? (int64_t)c * U / G : U; }
+  // The CTA whose range holds unit u (0 <= u < U).
+  __host__ __device__ __forceinline__ int cta_of(int64_t u) const { return (int)(((u + 1) * G - 1) / U); }
+};
 
 struct TileInfo {
   int slot, pos0, rows;
@@ -232,8 +250,26 @@ __device__ __forceinline__ TileInfo tile_info(const int32_t *w, const SgList &L,
   return t;
 }
 
+struct PieceInfo {
+  int slot, pos0, rows, tok0, contiguous;
+};
+constexpr int kPieceCache = 64;  // pieces per CTA whose info is kept in shared memory
+
+__device__ __forceinline__ PieceInfo piece_info(const int32_t *w, const int32_t *sorted_rows, const SgList &L,
+                                                int n_list, int tile) {
+  const TileInfo ti = tile_info(w, L, n_list, tile);
+  PieceInfo p;
+  p.slot = ti.slot;
+  p.pos0 = ti.pos0;
+  p.rows = ti.rows;
+  p.tok0 = sorted_rows[ti.pos0];
+  p.contiguous = sorted_rows[ti.pos0 + ti.rows - 1] - p.tok0 == ti.rows - 1;
+  return p;
+}
+
 struct SgMaps {
-  CUtensorMap m[LORA_MAX_SLICES];
+  CUtensorMap m[LORA_MAX_SLICES];  // A[s] as {r_max, d_in, slots}, boxes of box_n columns x 64 rows
+  CUtensorMap x;                   // x as {d_in, T}, boxes of 64 columns x 128 rows (shrink)
 };
 
 // ------------------------------------------------------------------ shrink
@@ -246,7 +282,7 @@ struct SgShrinkArgs {
   const int32_t *sorted_rows;
   int *err;
   SgList L;
-  int d_in, r_max, n_slices, kcmax, nb;  // nb: K blocks of 64
+  int d_in, r_max, n_slices, nb, maxp;  // nb: K blocks of 64; maxp: pieces per CTA
   int box_n;                  // TMA box width of an A block (<= 64 columns)
   uint32_t w_layout;          // its swizzle
   int stages, lag, stage_bytes, w_bytes;
@@ -282,30 +318,47 @@ __global__ void __launch_bounds__(kShrinkThreads, 1)
   pdl_wait();
   pdl_trigger();
   if (warp == 8) tmem_alloc(tslot, (uint32_t)a.tmem_cols);
+  const int n_tiles = a.work[a.L.hdr_tiles];
+  const int n_list = a.work[a.L.hdr_segs];
+  const Split sp = Split::of(n_tiles, (int)gridDim.x, a.nb, a.maxp);
+  const int64_t u0 = sp.u0(blockIdx.x), u1 = sp.u0(blockIdx.x + 1);
+  const int t_first = (int)(u0 / a.nb);
+  int n_pieces = u1 > u0 ? (int)((u1 - 1) / a.nb) - t_first + 1 : 0;
+  if (n_pieces > a.maxp) {  // cannot happen with the host's bound; refuse rather than overrun
+    if (tid == 0) atomicOr(a.err, kErrShrink);
+    n_pieces = 0;
+  }
+  // The segment, rows and contiguity of every piece's tile, resolved once
+  // (in parallel) before the pipeline starts.
+  PieceInfo *pinfo = reinterpret_cast<PieceInfo *>(tslot + 4);
+  if (warp == 4)
+    for (int p = lane; p < min(n_pieces, kPieceCache); p += 32) pinfo[p] = piece_info(a.work, a.sorted_rows, a.L, n_list, t_first + p);
   tc_before_sync();
   __syncthreads();
   tc_after_sync();
   const uint32_t tmem = *tslot;
-  const int n_tiles = a.work[a.L.hdr_tiles];
-  const int n_list = a.work[a.L.hdr_segs];
-  const int KC = split_count(n_tiles, (int)gridDim.x, a.kcmax);
-  const int n_items = n_tiles * KC;
 
   if (warp < 4) {
     // ---- producers: x rows by cp.async (swizzled), A blocks by TMA (thread 0)
     int issued = 0;
     const int chunk = tid & 7;
     bool ok = true;
-    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
-      const int tile = it / KC, kc = it - tile * KC;
-      const TileInfo ti = tile_info(a.work, a.L, n_list, tile);
+    for (int p = 0; p < n_pieces && ok; ++p) {
+      const int tile = t_first + p;
+      const PieceInfo pi = p < kPieceCache ? pinfo[p] : piece_info(a.work, a.sorted_rows, a.L, n_list, tile);
+      const TileInfo ti{pi.slot, pi.pos0, pi.rows};
+      // A tile of consecutive tokens comes by one TMA tile copy per K block,
+      // already in the swizzled operand layout; others are gathered.
+      const int tok0 = pi.tok0;
+      const bool contiguous = pi.contiguous != 0;
       int tok[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int r = (tid >> 3) + 16 * i;
-        tok[i] = r < ti.rows ? a.sorted_rows[ti.pos0 + r] : -1;
+        tok[i] = (!contiguous && r < ti.rows) ? a.sorted_rows[ti.pos0 + r] : -1;
       }
-      const int kb0 = kc * a.nb / KC, kb1 = (kc + 1) * a.nb / KC;
+      const int kb0 = (int)(max(u0, (int64_t)tile * a.nb) - (int64_t)tile * a.nb);
+      const int kb1 = (int)(min(u1, (int64_t)(tile + 1) * a.nb) - (int64_t)tile * a.nb);
       for (int kb = kb0; kb < kb1; ++kb) {
         const int s = issued % a.stages;
         if (!mbar_wait_warp(&empty[s], ((issued / a.stages) & 1) ^ 1, a.err, kErrShrink)) {
@@ -314,20 +367,23 @@ __global__ void __launch_bounds__(kShrinkThreads, 1)
         }
         unsigned char *st = sm + s * a.stage_bytes;
         if (tid == 0) {
-          mbar_arrive_tx(&full[s], (uint32_t)(a.n_slices * a.w_bytes));
+          mbar_arrive_tx(&full[s], (uint32_t)(a.n_slices * a.w_bytes + (contiguous ? kTileM * 128 : 0)));
           for (int sl = 0; sl < a.n_slices; ++sl)
             for (int bx = 0; bx * a.box_n < a.r_max; ++bx)
               tma_load_3d(st + kTileM * 128 + sl * a.w_bytes + bx * (kKB * a.box_n * 2), &maps.m[sl],
                           bx * a.box_n, kb * kKB, ti.slot, &full[s]);
+          if (contiguous) tma_load_2d(st, &maps.x, kb * kKB, tok0, &full[s]);
         }
-        const int col = kb * kKB + chunk * 8;
-        const bool col_ok = col < a.d_in;
+        if (!contiguous) {
+          const int col = kb * kKB + chunk * 8;
+          const bool col_ok = col < a.d_in;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int r = (tid >> 3) + 16 * i;
-          const bool v = col_ok && tok[i] >= 0;
-          const __nv_bfloat16 *src = v ? a.x + (int64_t)tok[i] * a.ldx + col : a.x;
-          cp_async16_zfill(st + swz128(r, chunk), src, v);
+          for (int i = 0; i < 8; ++i) {
+            const int r = (tid >> 3) + 16 * i;
+            const bool v = col_ok && tok[i] >= 0;
+            const __nv_bfloat16 *src = v ? a.x + (int64_t)tok[i] * a.ldx + col : a.x;
+            cp_async16_zfill(st + swz128(r, chunk), src, v);
+          }
         }
         cp_async_commit();
         ++issued;
@@ -346,14 +402,13 @@ __global__ void __launch_bounds__(kShrinkThreads, 1)
     const int q = warp & 3;
     const int row = q * 32 + lane;
     int nitem = 0;
-    for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
-      const int tile = it / KC, kc = it - tile * KC;
+    for (int p = 0; p < n_pieces; ++p) {
       const int acc = nitem % a.n_acc;
       if (!mbar_wait_warp(&accf[acc], (nitem / a.n_acc) & 1, a.err, kErrShrink)) break;
       tc_after_sync();
       const uint32_t t0 = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * a.acc_cols);
       for (int sl = 0; sl < a.n_slices; ++sl) {
-        float *dst = a.part + ((((int64_t)tile * KC + kc) * a.n_slices + sl) * kTileM + row) * a.r_max;
+        float *dst = a.part + ((((int64_t)blockIdx.x * a.maxp + p) * a.n_slices + sl) * kTileM + row) * a.r_max;
         for (int c = 0; c < a.r_max; c += 16) {
           float v[16];
           tmem_ld16(t0 + (uint32_t)(sl * a.r_max + c), v);
@@ -372,10 +427,10 @@ __global__ void __launch_bounds__(kShrinkThreads, 1)
     const uint32_t sbo_w = 8u * a.box_n * 2, lbo_w = (uint32_t)kKB * a.box_n * 2;
     int consumed = 0, nitem = 0;
     bool ok = true;
-    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
-      const int tile = it / KC, kc = it - tile * KC;
-      (void)tile;
-      const int kb0 = kc * a.nb / KC, kb1 = (kc + 1) * a.nb / KC;
+    for (int p = 0; p < n_pieces && ok; ++p) {
+      const int tile = t_first + p;
+      const int kb0 = (int)(max(u0, (int64_t)tile * a.nb) - (int64_t)tile * a.nb);
+      const int kb1 = (int)(min(u1, (int64_t)(tile + 1) * a.nb) - (int64_t)tile * a.nb);
       const int acc = nitem % a.n_acc;
       if (!mbar_wait(&acce[acc], ((nitem / a.n_acc) & 1) ^ 1, a.err, kErrShrink)) break;
       tc_after_sync();
@@ -418,41 +473,54 @@ __global__ void __launch_bounds__(kShrinkThreads, 1)
 // ------------------------------------------------------------------ u rows (expand and reduce)
 
 struct URowArgs {
-  const float *src;  // partials [item][slice][128][r_max], or buf [n_s, T, r_max]
+  const float *src;  // partials [CTA][piece][slice][128][r_max], or buf [n_s, T, r_max]
   int parts;
-  int KC, n_slices, r_max, T;
+  Split sp;          // the shrink's partition (parts only)
+  int n_slices, r_max, T;
 };
 
-// u[k] for 8 consecutive k (k0 multiple of 8) of one row: scale * the split
-// partials summed in split order (masked to the slot's rank), or the buffer.
-__device__ __forceinline__ void u_row8(const URowArgs &u, int tile, int slice, int row, int tok, int k0, int r_a,
-                                       float scale, float (&v)[8]) {
-  if (k0 >= r_a) {
+// u[k] for 16 consecutive k (k0 multiple of 16) of one row: scale * the
+// tile's pieces summed in CTA order (masked to the slot's rank), or the
+// buffer. All loads of one piece are issued together.
+__device__ __forceinline__ void u_row16(const URowArgs &u, int tile, int slice, int row, int tok, int k0, int r_a,
+                                        float scale, float (&v)[16]) {
 #pragma unroll
-    for (int j = 0; j < 8; ++j) v[j] = 0.f;
-    return;
-  }
+  for (int j = 0; j < 16; ++j) v[j] = 0.f;
+  if (k0 >= r_a) return;
   if (u.parts) {
-    float s[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) s[j] = 0.f;
-    for (int kc = 0; kc < u.KC; ++kc) {
+    const int c0 = u.sp.cta_of((int64_t)tile * u.sp.nb), c1 = u.sp.cta_of((int64_t)(tile + 1) * u.sp.nb - 1);
+    for (int c = c0; c <= c1; ++c) {
+      const int64_t cu0 = u.sp.u0(c);
+      if (u.sp.u0(c + 1) == cu0) continue;  // fewer units than CTAs: this CTA has none
+      const int j = tile - (int)(cu0 / u.sp.nb);
       const float4 *p = reinterpret_cast<const float4 *>(
-          u.src + ((((int64_t)tile * u.KC + kc) * u.n_slices + slice) * kTileM + row) * u.r_max + k0);
-      const float4 p0 = p[0], p1 = p[1];
-      s[0] += p0.x; s[1] += p0.y; s[2] += p0.z; s[3] += p0.w;
-      s[4] += p1.x; s[5] += p1.y; s[6] += p1.z; s[7] += p1.w;
+          u.src + ((((int64_t)c * u.sp.maxp + j) * u.n_slices + slice) * kTileM + row) * u.r_max + k0);
+      float4 q[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) q[i] = p[i];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        v[4 * i] += q[i].x;
+        v[4 * i + 1] += q[i].y;
+        v[4 * i + 2] += q[i].z;
+        v[4 * i + 3] += q[i].w;
+      }
     }
 #pragma unroll
-    for (int j = 0; j < 8; ++j) v[j] = scale * s[j];
+    for (int j = 0; j < 16; ++j) v[j] *= scale;
   } else {
     const float4 *p = reinterpret_cast<const float4 *>(u.src + ((int64_t)slice * u.T + tok) * u.r_max + k0);
-    const float4 p0 = p[0], p1 = p[1];
-    v[0] = p0.x; v[1] = p0.y; v[2] = p0.z; v[3] = p0.w;
-    v[4] = p1.x; v[5] = p1.y; v[6] = p1.z; v[7] = p1.w;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float4 q = p[i];
+      v[4 * i] = q.x;
+      v[4 * i + 1] = q.y;
+      v[4 * i + 2] = q.z;
+      v[4 * i + 3] = q.w;
+    }
   }
 #pragma unroll
-  for (int j = 0; j < 8; ++j)
+  for (int j = 0; j < 16; ++j)
     if (k0 + j >= r_a) v[j] = 0.f;
 }
 
@@ -467,7 +535,7 @@ struct SgReduceArgs {
   const float *slot_scale;
   int *err;
   SgList L;
-  int shrink_grid, kcmax;
+  int shrink_grid, nb, maxp;
 };
 
 // Grid-stride over (tile, slice); thread = row.
@@ -477,7 +545,7 @@ __global__ void __launch_bounds__(kTileM) sgmv_reduce_kernel(const SgReduceArgs 
   const int n_tiles = a.work[a.L.hdr_tiles];
   const int n_list = a.work[a.L.hdr_segs];
   URowArgs u = a.u;
-  u.KC = split_count(n_tiles, a.shrink_grid, a.kcmax);
+  u.sp = Split::of(n_tiles, a.shrink_grid, a.nb, a.maxp);
   const int row = threadIdx.x;
   for (int p = blockIdx.x; p < n_tiles * u.n_slices; p += gridDim.x) {
     const int tile = p / u.n_slices, slice = p - tile * u.n_slices;
@@ -487,11 +555,12 @@ __global__ void __launch_bounds__(kTileM) sgmv_reduce_kernel(const SgReduceArgs 
     const int r_a = min(max(a.slot_rank[ti.slot], 0), u.r_max);
     const float scale = a.slot_scale[ti.slot];
     float *dst = a.buf + ((int64_t)slice * u.T + tok) * u.r_max;
-    for (int k0 = 0; k0 < u.r_max; k0 += 8) {
-      float v[8];
-      u_row8(u, tile, slice, row, tok, k0, r_a, scale, v);
-      reinterpret_cast<float4 *>(dst + k0)[0] = make_float4(v[0], v[1], v[2], v[3]);
-      reinterpret_cast<float4 *>(dst + k0)[1] = make_float4(v[4], v[5], v[6], v[7]);
+    for (int k0 = 0; k0 < u.r_max; k0 += 16) {
+      float v[16];
+      u_row16(u, tile, slice, row, tok, k0, r_a, scale, v);
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        reinterpret_cast<float4 *>(dst + k0)[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
     }
   }
 }
@@ -508,7 +577,7 @@ struct SgExpandArgs {
   const float *slot_scale;
   int *err;
   SgList L;
-  int shrink_grid, kcmax;
+  int shrink_grid, nb, maxp;
   int out_sizes[LORA_MAX_SLICES];
   int out_off[LORA_MAX_SLICES];
   int nb_start[LORA_MAX_SLICES + 1];  // column blocks per slice (cumulative)
@@ -567,12 +636,6 @@ struct TileRows {
   }
 };
 
-__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int c0, int c1, uint64_t *bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
-      ::"r"(smem_addr(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_addr(bar))
-      : "memory");
-}
 // The barrier receives this thread's arrival once its earlier cp.async copies are complete.
 __device__ __forceinline__ void cp_async_arrive(uint64_t *bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
@@ -716,7 +779,7 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
     const int lt = tid - 256;
     const int wb = lt >> 5;
     URowArgs u = a.u;
-    u.KC = split_count(n_tiles, a.shrink_grid, a.kcmax);
+    u.sp = Split::of(n_tiles, a.shrink_grid, a.nb, a.maxp);
     int cur_group = -1, g = 0, nitem = 0;
     TileRows tr;
     int ltok[16];
@@ -737,22 +800,26 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
         const int r_a = tok >= 0 ? min(max(a.slot_rank[tr.ti.slot], 0), r_max) : 0;
         const float scale = a.slot_scale[tr.ti.slot];
         if (!mbar_wait_warp(uempty, (g & 1) ^ 1, a.err, kErrExpand)) break;
-        for (int c = 0; c < r_max / 8; ++c) {
-          float v[8];
-          u_row8(u, e.tile, e.slice, lt, tok, 8 * c, r_a, scale, v);
-          uint4 hi, lo;
-          __nv_bfloat162 *h2 = reinterpret_cast<__nv_bfloat162 *>(&hi);
-          __nv_bfloat162 *l2 = reinterpret_cast<__nv_bfloat162 *>(&lo);
+        for (int k0 = 0; k0 < r_max; k0 += 16) {
+          float v[16];
+          u_row16(u, e.tile, e.slice, lt, tok, k0, r_a, scale, v);
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const __nv_bfloat162 hh = __floats2bfloat162_rn(v[2 * j], v[2 * j + 1]);
-            const float2 hf = __bfloat1622float2(hh);
-            h2[j] = hh;
-            l2[j] = __floats2bfloat162_rn(v[2 * j] - hf.x, v[2 * j + 1] - hf.y);
+          for (int hc = 0; hc < 2; ++hc) {  // two 16-byte chunks of 8 k values
+            uint4 hi, lo;
+            __nv_bfloat162 *h2 = reinterpret_cast<__nv_bfloat162 *>(&hi);
+            __nv_bfloat162 *l2 = reinterpret_cast<__nv_bfloat162 *>(&lo);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const __nv_bfloat162 hh = __floats2bfloat162_rn(v[8 * hc + 2 * j], v[8 * hc + 2 * j + 1]);
+              const float2 hf = __bfloat1622float2(hh);
+              h2[j] = hh;
+              l2[j] = __floats2bfloat162_rn(v[8 * hc + 2 * j] - hf.x, v[8 * hc + 2 * j + 1] - hf.y);
+            }
+            const int c = k0 / 8 + hc;
+            const uint32_t off = (uint32_t)((c >> 3) * kUKRegion) + swz128(lt, c & 7);
+            *reinterpret_cast<uint4 *>(sU + off) = hi;
+            *reinterpret_cast<uint4 *>(sU + a.nk * kUKRegion + off) = lo;
           }
-          const uint32_t off = (uint32_t)((c >> 3) * kUKRegion) + swz128(lt, c & 7);
-          *reinterpret_cast<uint4 *>(sU + off) = hi;
-          *reinterpret_cast<uint4 *>(sU + a.nk * kUKRegion + off) = lo;
         }
         fence_async_smem();
         mbar_arrive(ufull);
@@ -896,14 +963,16 @@ cudaError_t make_map(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1,
 }
 
 // 2-D tensor map of a row-major matrix {cols (contiguous), rows} with row
-// stride `ld` elements, 128-byte x 128-row boxes in the 128-byte swizzle.
-cudaError_t make_rows_map(CUtensorMap *m, const void *base, bool bf16, uint64_t cols, uint64_t rows, int64_t ld) {
+// stride `ld` elements, boxes of box_cols columns (128 bytes) x 128 rows in the
+// 128-byte swizzle.
+cudaError_t make_rows_map(CUtensorMap *m, const void *base, bool bf16, uint64_t cols, uint64_t rows, int64_t ld,
+                          uint32_t box_cols) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
   if (enc == nullptr) return cudaErrorNotSupported;
   const uint64_t es = bf16 ? 2 : 4;
   const cuuint64_t dims[2] = {cols, rows};
   const cuuint64_t strides[1] = {(cuuint64_t)ld * es};
-  const cuuint32_t box[2] = {(cuuint32_t)(128 / es), (cuuint32_t)kTileM};
+  const cuuint32_t box[2] = {box_cols, (cuuint32_t)kTileM};
   const cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
                    const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -926,15 +995,16 @@ SgList list_of(const MetaView &mv, ListSel sel) {
   return L;
 }
 
-int kcmax_of(const lora_layer_desc &d) {
-  const int nb = (d.d_in + kKB - 1) / kKB;
-  return nb < kKCMax ? nb : kKCMax;
-}
+int nb_of(const lora_layer_desc &d) { return (d.d_in + kKB - 1) / kKB; }
 
 // Upper bound on the tiles of any work list for T tokens and S slots.
 int64_t tiles_bound(int T, int S) { return (int64_t)T / kTileM + std::min<int64_t>(S - 1, T); }
 
 int shrink_grid() { return sm_count(); }
+
+// Pieces per CTA of the shrink's partition, for any batch of T tokens: a
+// range of at most ceil(U / G) units spans at most n_tiles / G + 2 tiles.
+int maxp_of(int T, int S, int G) { return (int)(tiles_bound(T, S) / G) + 2; }
 
 }  // namespace
 
@@ -944,8 +1014,8 @@ size_t sgmv_workspace_bytes(const lora_layer_desc &d, int max_tokens) {
   if (max_tokens <= 0) return 0;
   const int G = shrink_grid();
   if (G <= 0) return 0;
-  const int64_t items = 2 * (int64_t)G + tiles_bound(max_tokens, d.num_slots);
-  return (size_t)items * d.n_slices * kTileM * d.r_max * sizeof(float);
+  const int64_t pieces = (int64_t)G * maxp_of(max_tokens, d.num_slots, G);
+  return (size_t)pieces * d.n_slices * kTileM * d.r_max * sizeof(float);
 }
 
 cudaError_t launch_sgmv_shrink(const lora_layer_desc &d, const MetaView &mv, ListSel sel, const void *x, int64_t ldx,
@@ -963,6 +1033,10 @@ cudaError_t launch_sgmv_shrink(const lora_layer_desc &d, const MetaView &mv, Lis
                              (uint32_t)a.box_n, (uint32_t)kKB, sw);
     if (e != cudaSuccess) return e;
   }
+  {
+    cudaError_t e = make_rows_map(&maps.x, x, true, (uint64_t)d.d_in, (uint64_t)mv.num_tokens, ldx, kKB);
+    if (e != cudaSuccess) return e;
+  }
   a.x = static_cast<const __nv_bfloat16 *>(x);
   a.ldx = ldx;
   a.part = part;
@@ -973,14 +1047,14 @@ cudaError_t launch_sgmv_shrink(const lora_layer_desc &d, const MetaView &mv, Lis
   a.d_in = d.d_in;
   a.r_max = d.r_max;
   a.n_slices = d.n_slices;
-  a.kcmax = kcmax_of(d);
-  a.nb = (d.d_in + kKB - 1) / kKB;
+  a.nb = nb_of(d);
+  a.maxp = maxp_of(mv.num_tokens, mv.num_slots, shrink_grid());
   a.w_bytes = kKB * d.r_max * 2;
   a.stage_bytes = kTileM * 128 + d.n_slices * a.w_bytes;
-  const int fixed = kAlignSlack + 256;
+  const int fixed = kAlignSlack + 2048;  // barriers, TMEM address, piece cache
   a.stages = std::min(6, (kSmemMax - fixed) / a.stage_bytes);
   if (a.stages < 2) return cudaErrorInvalidValue;
-  a.lag = a.stages - 1;  // every stage may be in flight
+  a.lag = std::min(2, a.stages - 1);
   a.acc_cols = d.n_slices * d.r_max;
   a.n_acc = 2 * a.acc_cols <= 512 ? 2 : 1;
   int cols = 32;
@@ -1010,7 +1084,8 @@ cudaError_t launch_sgmv_reduce(const lora_layer_desc &d, const MetaView &mv, Lis
   a.err = const_cast<int32_t *>(mv.work) + WorkLists::kErrWord;
   a.L = list_of(mv, sel);
   a.shrink_grid = shrink_grid();
-  a.kcmax = kcmax_of(d);
+  a.nb = nb_of(d);
+  a.maxp = maxp_of(mv.num_tokens, mv.num_slots, a.shrink_grid);
   return launch_pdl(sgmv_reduce_kernel, dim3((unsigned)(2 * sm_count())), dim3(kTileM), 0, st, 1u, a);
 }
 
@@ -1027,7 +1102,8 @@ cudaError_t launch_sgmv_expand(const lora_layer_desc &d, const MetaView &mv, Lis
     if (e != cudaSuccess) return e;
     width += d.out_sizes[s];
   }
-  cudaError_t em = make_rows_map(&maps.y, y, y_dtype == LORA_BF16, (uint64_t)width, (uint64_t)mv.num_tokens, ldy);
+  cudaError_t em = make_rows_map(&maps.y, y, y_dtype == LORA_BF16, (uint64_t)width, (uint64_t)mv.num_tokens, ldy,
+                                 y_dtype == LORA_BF16 ? 64u : 32u);
   if (em != cudaSuccess) return em;
   SgExpandArgs a{};
   a.u.src = u_src;
@@ -1044,7 +1120,8 @@ cudaError_t launch_sgmv_expand(const lora_layer_desc &d, const MetaView &mv, Lis
   a.err = const_cast<int32_t *>(mv.work) + WorkLists::kErrWord;
   a.L = list_of(mv, sel);
   a.shrink_grid = shrink_grid();
-  a.kcmax = kcmax_of(d);
+  a.nb = nb_of(d);
+  a.maxp = maxp_of(mv.num_tokens, mv.num_slots, a.shrink_grid);
   int off = 0, nb = 0;
   for (int s = 0; s < d.n_slices; ++s) {
     a.out_sizes[s] = d.out_sizes[s];
