@@ -657,8 +657,7 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
   uint64_t *bempty = bfull + a.b_stages;
   uint64_t *yfull = bempty + a.b_stages;
   uint64_t *yempty = yfull + a.y_stages;
-  uint64_t *ydone = yempty + a.y_stages;  // [stage][quadrant]: both column halves of 32 rows updated
-  uint64_t *accf = ydone + 4 * a.y_stages;
+  uint64_t *accf = yempty + a.y_stages;
   uint64_t *acce = accf + 2;
   uint64_t *ufull = acce + 2;
   uint64_t *uempty = ufull + 1;
@@ -673,7 +672,6 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
     for (int s = 0; s < a.y_stages; ++s) {
       mbar_init(&yfull[s], 1 + 128);  // the producer + every loader thread
       mbar_init(&yempty[s], 256);
-      for (int q = 0; q < 4; ++q) mbar_init(&ydone[4 * s + q], 64);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&accf[i], 1);
@@ -701,11 +699,10 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
 
   if (warp < 8) {
     // ---- epilogue. Warp w adds accumulator lanes 32 (w % 4), column half
-    // w / 4, into the staged rows (thread = row); then the two warps of a
-    // quadrant store its 32 rows with coalesced 16-byte stores.
+    // w / 4, into the staged rows (thread = row), then stores that half of
+    // its 32 rows with coalesced 16-byte stores.
     const int q = warp & 3, h = warp >> 2;
     const int row = q * 32 + lane;
-    const int g_st = lane & 15;  // chunk this lane stores
     int cur_tile = -1, tok = -1, nitem = 0;
     int stok[8];
 #pragma unroll
@@ -717,7 +714,7 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
         tok = row < ti.rows ? a.sorted_rows[ti.pos0 + row] : -1;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const int r = 32 * q + 16 * h + 2 * i + (lane >> 4);
+          const int r = 32 * q + 4 * i + (lane >> 3);
           stok[i] = r < ti.rows ? a.sorted_rows[ti.pos0 + r] : -1;
         }
         cur_tile = e.tile;
@@ -735,39 +732,44 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
       mbar_arrive(&acce[acc]);
       if (!mbar_wait_warp(&yfull[ys], par, a.err, kErrExpand)) break;
       unsigned char *st = sY + ys * kYStage;
-      if (tok >= 0) {
+      if (tok >= 0) {  // this row's half: all eight chunks in flight at once
+        uint4 w[8];
+#pragma unroll
+        for (int g = 0; g < 8; ++g) w[g] = *reinterpret_cast<const uint4 *>(st + ychunk(row, 8 * h + g));
 #pragma unroll
         for (int g = 0; g < 8; ++g) {
-          if (h * kHalf + g * kVec < e.ncols) {
-            uint4 *p = reinterpret_cast<uint4 *>(st + ychunk(row, 8 * h + g));
-            uint4 w = *p;
-            if constexpr (sizeof(TY) == 2) {
-              __nv_bfloat162 *b2 = reinterpret_cast<__nv_bfloat162 *>(&w);
+          if constexpr (sizeof(TY) == 2) {
+            uint32_t *u32 = reinterpret_cast<uint32_t *>(&w[g]);
 #pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                const float2 f = __bfloat1622float2(b2[j]);
-                b2[j] = __floats2bfloat162_rn(f.x + v[g * 8 + 2 * j], f.y + v[g * 8 + 2 * j + 1]);
-              }
-            } else {
-              float *f = reinterpret_cast<float *>(&w);
-#pragma unroll
-              for (int j = 0; j < 4; ++j) f[j] += v[g * 4 + j];
+            for (int j = 0; j < 4; ++j) {
+              const float2 f = make_float2(__uint_as_float(u32[j] << 16), __uint_as_float(u32[j] & 0xffff0000u));
+              const float2 sum = __fadd2_rn(f, make_float2(v[g * 8 + 2 * j], v[g * 8 + 2 * j + 1]));
+              const __nv_bfloat162 b = __floats2bfloat162_rn(sum.x, sum.y);
+              u32[j] = *reinterpret_cast<const uint32_t *>(&b);
             }
-            *p = w;
+          } else {
+            float *f = reinterpret_cast<float *>(&w[g]);
+            const float2 lo = __fadd2_rn(make_float2(f[0], f[1]), make_float2(v[g * 4], v[g * 4 + 1]));
+            const float2 hi = __fadd2_rn(make_float2(f[2], f[3]), make_float2(v[g * 4 + 2], v[g * 4 + 3]));
+            f[0] = lo.x; f[1] = lo.y; f[2] = hi.x; f[3] = hi.y;
           }
         }
-      }
-      mbar_arrive(&ydone[4 * ys + q]);
-      if (!mbar_wait_warp(&ydone[4 * ys + q], par, a.err, kErrExpand)) break;
-      TY *ybase = y + a.out_off[e.slice] + e.n0 + g_st * kVec;
-      if (g_st * kVec < e.ncols) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int r = 32 * q + 16 * h + 2 * i + (lane >> 4);
-          if (stok[i] >= 0)
-            *reinterpret_cast<uint4 *>(ybase + (int64_t)stok[i] * a.ldy) =
-                *reinterpret_cast<const uint4 *>(st + ychunk(r, g_st));
-        }
+        for (int g = 0; g < 8; ++g) *reinterpret_cast<uint4 *>(st + ychunk(row, 8 * h + g)) = w[g];
+      }
+      __syncwarp();
+      // Store this warp's half of its 32 rows: lanes along the row, four rows
+      // (4 x 128 bytes) per instruction. Columns past the slice stay unstored.
+      const int gl = lane & 7;
+      if (h * kHalf + gl * kVec < e.ncols) {
+        TY *ybase = y + a.out_off[e.slice] + e.n0 + h * kHalf + gl * kVec;
+        uint4 w[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          w[i] = *reinterpret_cast<const uint4 *>(st + ychunk(32 * q + 4 * i + (lane >> 3), 8 * h + gl));
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          if (stok[i] >= 0) *reinterpret_cast<uint4 *>(ybase + (int64_t)stok[i] * a.ldy) = w[i];
       }
       mbar_arrive(&yempty[ys]);
       ++nitem;
