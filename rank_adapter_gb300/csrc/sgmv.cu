@@ -590,7 +590,8 @@ struct SgExpandMaps {
   CUtensorMap y;                   // y as {sum(out_sizes), T}, boxes of 128 bytes x 128 rows
 };
 
-constexpr int kExpandThreads = 448;  // epilogue 0-7, loaders (u rows, gathered y rows) 8-11, producer 12, MMA 13
+constexpr int kEpiWarps = 8;  // epilogue warps, a multiple of 4 (one group per TMEM lane quadrant); 8 measured best
+constexpr int kExpandThreads = 32 * (kEpiWarps + 6);  // + loaders (u rows, gathered y rows) x4, producer, MMA
 constexpr int kYHalf = kTileM * 128;  // one half (128 bytes per row) of a staged y tile
 constexpr int kYStage = 2 * kYHalf;   // a staged y tile: 128 rows x 256 bytes
 
@@ -646,7 +647,12 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
     sgmv_expand_kernel(const __grid_constant__ SgExpandMaps maps, const SgExpandArgs a) {
   constexpr int kN = YCols<TY>::kN;           // columns per item (256 bytes of a y row)
   constexpr int kVec = 16 / (int)sizeof(TY);  // y elements per 16-byte chunk
-  constexpr int kHalf = kN / 2;               // columns per epilogue warp (one staged half)
+  constexpr int kHalf = kN / 2;               // columns per 128-byte staged half
+  constexpr int kParts = kEpiWarps / 4;       // epilogue warps per TMEM lane quadrant
+  constexpr int kPartCols = kN / kParts;      // accumulator columns per epilogue warp
+  constexpr int kPartChunks = 16 / kParts;    // 16-byte chunks per row in a part
+  constexpr int kRowsPerInst = 32 / kPartChunks;
+  constexpr int kStoreInsts = 32 / kRowsPerInst;
   extern __shared__ unsigned char smem_raw[];
   unsigned char *sm = align1024(smem_raw);
   const int r_max = a.u.r_max, n_slices = a.u.n_slices;
@@ -671,11 +677,11 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
     }
     for (int s = 0; s < a.y_stages; ++s) {
       mbar_init(&yfull[s], 1 + 128);  // the producer + every loader thread
-      mbar_init(&yempty[s], 256);
+      mbar_init(&yempty[s], 32 * kEpiWarps);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&accf[i], 1);
-      mbar_init(&acce[i], 256);
+      mbar_init(&acce[i], 32 * kEpiWarps);
     }
     mbar_init(ufull, 128);
     mbar_init(uempty, 1);
@@ -685,7 +691,7 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
   pdl_wait();
   pdl_trigger();
   constexpr uint32_t kTmemCols = 2 * kN;
-  if (warp == 13) tmem_alloc(tslot, kTmemCols);
+  if (warp == kEpiWarps + 5) tmem_alloc(tslot, kTmemCols);
   tc_before_sync();
   __syncthreads();
   tc_after_sync();
@@ -697,24 +703,25 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
   const int64_t it0 = n_items * blockIdx.x / gridDim.x, it1 = n_items * (blockIdx.x + 1) / gridDim.x;
   TY *y = static_cast<TY *>(a.y);
 
-  if (warp < 8) {
-    // ---- epilogue. Warp w adds accumulator lanes 32 (w % 4), column half
-    // w / 4, into the staged rows (thread = row), then stores that half of
-    // its 32 rows with coalesced 16-byte stores.
-    const int q = warp & 3, h = warp >> 2;
+  if (warp < kEpiWarps) {
+    // ---- epilogue. Warp w adds accumulator lanes 32 (w % 4), column part
+    // w / 4 (kPartCols columns), into the staged rows (thread = row), then
+    // stores that part of its 32 rows with coalesced 16-byte stores.
+    const int q = warp & 3, part = warp >> 2;
     const int row = q * 32 + lane;
+    const int g0 = part * kPartChunks;  // first 16-byte chunk of this part
     int cur_tile = -1, tok = -1, nitem = 0;
-    int stok[8];
+    int stok[kStoreInsts];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) stok[i] = -1;
+    for (int i = 0; i < kStoreInsts; ++i) stok[i] = -1;
     for (int64_t it = it0; it < it1; ++it) {
       const ExpandItem e = expand_item(a, it, nbt, kN, n_slices);
       if (e.tile != cur_tile) {
         const TileInfo ti = tile_info(a.work, a.L, n_list, e.tile);
         tok = row < ti.rows ? a.sorted_rows[ti.pos0 + row] : -1;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int r = 32 * q + 4 * i + (lane >> 3);
+        for (int i = 0; i < kStoreInsts; ++i) {
+          const int r = 32 * q + kRowsPerInst * i + lane / kPartChunks;
           stok[i] = r < ti.rows ? a.sorted_rows[ti.pos0 + r] : -1;
         }
         cur_tile = e.tile;
@@ -723,21 +730,28 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
       const uint32_t par = (nitem / a.y_stages) & 1;
       if (!mbar_wait_warp(&accf[acc], (nitem >> 1) & 1, a.err, kErrExpand)) break;
       tc_after_sync();
-      float v[kHalf];
-      const uint32_t t0 = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kN + h * kHalf);
+      float v[kPartCols];
+      const uint32_t t0 = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kN + part * kPartCols);
+      if constexpr (kPartCols >= 32) {
 #pragma unroll
-      for (int c = 0; c < kHalf; c += 32) tmem_ld32_async(t0 + (uint32_t)c, v + c);
-      tmem_wait_ld();
+        for (int c = 0; c < kPartCols; c += 32) tmem_ld32_async(t0 + (uint32_t)c, v + c);
+        tmem_wait_ld();
+      } else {
+        float v16[16];
+        tmem_ld16(t0, v16);
+#pragma unroll
+        for (int c = 0; c < 16; ++c) v[c] = v16[c];
+      }
       tc_before_sync();
       mbar_arrive(&acce[acc]);
       if (!mbar_wait_warp(&yfull[ys], par, a.err, kErrExpand)) break;
       unsigned char *st = sY + ys * kYStage;
-      if (tok >= 0) {  // this row's half: all eight chunks in flight at once
-        uint4 w[8];
+      if (tok >= 0) {  // this row's part: all its chunks in flight at once
+        uint4 w[kPartChunks];
 #pragma unroll
-        for (int g = 0; g < 8; ++g) w[g] = *reinterpret_cast<const uint4 *>(st + ychunk(row, 8 * h + g));
+        for (int g = 0; g < kPartChunks; ++g) w[g] = *reinterpret_cast<const uint4 *>(st + ychunk(row, g0 + g));
 #pragma unroll
-        for (int g = 0; g < 8; ++g) {
+        for (int g = 0; g < kPartChunks; ++g) {
           if constexpr (sizeof(TY) == 2) {
             uint32_t *u32 = reinterpret_cast<uint32_t *>(&w[g]);
 #pragma unroll
@@ -755,30 +769,30 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
           }
         }
 #pragma unroll
-        for (int g = 0; g < 8; ++g) *reinterpret_cast<uint4 *>(st + ychunk(row, 8 * h + g)) = w[g];
+        for (int g = 0; g < kPartChunks; ++g) *reinterpret_cast<uint4 *>(st + ychunk(row, g0 + g)) = w[g];
       }
       __syncwarp();
-      // Store this warp's half of its 32 rows: lanes along the row, four rows
-      // (4 x 128 bytes) per instruction. Columns past the slice stay unstored.
-      const int gl = lane & 7;
-      if (h * kHalf + gl * kVec < e.ncols) {
-        TY *ybase = y + a.out_off[e.slice] + e.n0 + h * kHalf + gl * kVec;
-        uint4 w[8];
+      // Store this warp's part of its 32 rows: lanes along the row,
+      // kRowsPerInst rows per instruction. Columns past the slice stay unstored.
+      const int gl = lane % kPartChunks;
+      if ((g0 + gl) * kVec < e.ncols) {
+        TY *ybase = y + a.out_off[e.slice] + e.n0 + (g0 + gl) * kVec;
+        uint4 w[kStoreInsts];
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-          w[i] = *reinterpret_cast<const uint4 *>(st + ychunk(32 * q + 4 * i + (lane >> 3), 8 * h + gl));
+        for (int i = 0; i < kStoreInsts; ++i)
+          w[i] = *reinterpret_cast<const uint4 *>(st + ychunk(32 * q + kRowsPerInst * i + lane / kPartChunks, g0 + gl));
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
+        for (int i = 0; i < kStoreInsts; ++i)
           if (stok[i] >= 0) *reinterpret_cast<uint4 *>(ybase + (int64_t)stok[i] * a.ldy) = w[i];
       }
       mbar_arrive(&yempty[ys]);
       ++nitem;
     }
-  } else if (warp < 12) {
+  } else if (warp < kEpiWarps + 4) {
     // ---- loaders: the u rows of each (tile, slice) (thread = row), and the
     // y rows of tiles that are not one run of tokens (16-byte cp.async,
     // lanes along a row)
-    const int lt = tid - 256;
+    const int lt = tid - 32 * kEpiWarps;
     const int wb = lt >> 5;
     URowArgs u = a.u;
     u.sp = Split::of(n_tiles, a.shrink_grid, a.nb, a.maxp);
@@ -844,7 +858,7 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
       ++nitem;
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
-  } else if (warp == 12) {
+  } else if (warp == kEpiWarps + 4) {
     // ---- producer: B blocks, and y rows of contiguous tiles, by TMA
     TileRows tr;
     int nitem = 0;
@@ -914,7 +928,7 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
   }
   tc_before_sync();
   __syncthreads();
-  if (warp == 13) {
+  if (warp == kEpiWarps + 5) {
     tc_after_sync();
     tmem_free(tmem, kTmemCols);
   }
