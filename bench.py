@@ -340,7 +340,9 @@ def time_path(torch, ra, reps, stream, path, steps, G, clocks=None, dist=None):
                 reps[i % R].launch(ra, i, evs[i] if evs else None, path=path)
         return gr, evs
 
+    n0 = ra.lora_launch_count()
     graph, _ = capture(G, False)
+    per_step = (ra.lora_launch_count() - n0) / G  # kernels the library launches per step
     tail = steps % G
     graph_tail = capture(tail, False)[0] if tail else None
     with torch.cuda.stream(stream):
@@ -388,7 +390,20 @@ def time_path(torch, ra, reps, stream, path, steps, G, clocks=None, dist=None):
         stream.synchronize()
         durs = {k: [e[j].elapsed_time(e[j + 1]) for e in evs2] for j, k in enumerate(names)}
         how = f"CUDA events around {n} eager launches enqueued behind a sleep kernel (upper bounds)"
-    return elapsed_ms, {k: statistics.mean(v) for k, v in durs.items()}, how
+    return elapsed_ms, {k: statistics.mean(v) for k, v in durs.items()}, how, per_step
+
+
+def reduce_over_ranks(torch, dist, elapsed_ms, e2e_ms, lora_tokens, device):
+    """Whole-job numbers of a data-parallel run: the slowest rank's timings (max)
+    and the LoRA tokens of all ranks (sum). dist is None for a single process."""
+    if dist is None:
+        return float(elapsed_ms), float(e2e_ms), float(lora_tokens)
+    vals = torch.tensor([elapsed_ms, e2e_ms, float(lora_tokens)], dtype=torch.float64, device=device)
+    mx = vals.clone()
+    dist.all_reduce(mx, op=dist.ReduceOp.MAX)
+    tl = vals.clone()
+    dist.all_reduce(tl, op=dist.ReduceOp.SUM)
+    return float(mx[0]), float(mx[1]), float(tl[2])
 
 
 def run_ours(args):
@@ -439,10 +454,11 @@ def run_ours(args):
     G = min(G, max(1, args.steps))
     vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
     clocks = ClockSampler(vis.split(",")[local].strip() if vis else str(local))
-    elapsed_ms, avg, kernel_timing = time_path(torch, ra, reps, stream, args.path, args.steps, G, clocks, dist)
+    elapsed_ms, avg, kernel_timing, per_step = time_path(torch, ra, reps, stream, args.path, args.steps, G, clocks,
+                                                         dist)
     other = "split" if args.path == "fused" else "fused"
     other_steps = min(args.steps, 20 * G)
-    o_ms, o_avg, _ = time_path(torch, ra, reps, stream, other, other_steps, G)
+    o_ms, o_avg, _, _ = time_path(torch, ra, reps, stream, other, other_steps, G)
 
     # End to end: the same step through the ABI with pinned host buffers and copies in / out.
     h_x = torch.empty_like(x0, device="cpu").pin_memory()
@@ -482,17 +498,8 @@ def run_ours(args):
     e2e_wall = time.perf_counter() - t0
     e2e_ms = e0.elapsed_time(e1)
 
-    # Max over ranks.
-    vals = torch.tensor([elapsed_ms, e2e_ms, float(alg["T_L"])], dtype=torch.float64, device="cuda")
-    if dist is not None:
-        mx = vals.clone()
-        dist.all_reduce(mx, op=dist.ReduceOp.MAX)
-        tl = vals.clone()
-        dist.all_reduce(tl, op=dist.ReduceOp.SUM)
-        elapsed_ms, e2e_ms, total_TL = float(mx[0]), float(mx[1]), float(tl[2])
-    else:
-        total_TL = float(alg["T_L"])
-    launches = len(KERNELS[args.path]) * args.steps
+    elapsed_ms, e2e_ms, total_TL = reduce_over_ranks(torch, dist, elapsed_ms, e2e_ms, alg["T_L"], "cuda")
+    launches = int(round(per_step * args.steps))  # counted by the library while capturing the step graph
 
     if rank == 0:
         hbm, tc, src = load_peaks()

@@ -282,6 +282,10 @@ const char *lora_strerror(int status);
 /* CUDA error code of the last LORA_ECUDA returned on this host thread (0 if none). */
 int lora_last_cuda_error(void);
 
+/* Kernels this library has launched in this process, on every device and
+ * thread, counting launches captured into CUDA graphs once (at capture). */
+uint64_t lora_launch_count(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -29,7 +29,7 @@ __all__ = [
     "lora_set_slot", "lora_reset_slot", "lora_prepare_meta", "lora_shrink", "lora_expand", "lora_apply",
     "lora_shrink_noalloc", "lora_noalloc_scratch_bytes",
     "lora_workspace_bytes", "lora_meta_tiles_bytes", "lora_query_status", "lora_strerror",
-    "lora_last_cuda_error", "SlotTable", "TokenMeta", "shrink", "expand", "apply", "workspace", "check",
+    "lora_last_cuda_error", "lora_launch_count", "SlotTable", "TokenMeta", "shrink", "expand", "apply", "workspace", "check",
 ]
 
 LORA_OK, LORA_EINVAL, LORA_ERANGE, LORA_EALIGN, LORA_EUNSUPPORTED, LORA_ECUDA, LORA_EBADSLOT, LORA_EDEVICE = range(8)
@@ -97,6 +97,7 @@ _sig = {
     "lora_query_status": (_i32, [_P(Meta), _P(_i32), _vp]),
     "lora_strerror": (ctypes.c_char_p, [_i32]),
     "lora_last_cuda_error": (_i32, []),
+    "lora_launch_count": (ctypes.c_uint64, []),
 }
 for _name, (_res, _args) in _sig.items():
     _f = getattr(_lib, _name)
@@ -198,6 +199,11 @@ def lora_strerror(status: int) -> str:
 
 def lora_last_cuda_error() -> int:
     return int(_lib.lora_last_cuda_error())
+
+
+def lora_launch_count() -> int:
+    """Kernels the library has launched in this process (graph captures count once)."""
+    return int(_lib.lora_launch_count())
 
 
 # ----------------------------------------------------------------------------- torch-owned buffers

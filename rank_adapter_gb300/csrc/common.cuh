@@ -187,6 +187,9 @@ __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.lau
 // Raise a kernel's dynamic shared-memory limit to at least `bytes` (per kernel and device).
 cudaError_t set_max_dynamic_smem(const void *kernel, int bytes);
 
+// Kernels this library has launched in the process (launch_pdl counts them).
+void count_launch();
+
 // Launch with programmatic stream serialization (see pdl_wait) and, when
 // cluster_x > 1, thread-block clusters of cluster_x CTAs along x.
 template <typename... KArgs, typename... Args>
@@ -211,7 +214,9 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   }
   cfg.attrs = attr;
   cfg.numAttrs = n;
-  return cudaLaunchKernelEx(&cfg, kernel, args...);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
+  if (e == cudaSuccess) count_launch();
+  return e;
 }
 
 // ------------------------------------------------------------------ internal launchers

@@ -3,6 +3,7 @@
 // device memory or keeps state between calls beyond per-(kernel, device)
 // launch attributes.
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 #include <map>
 #include <utility>
@@ -10,6 +11,12 @@
 #include "common.cuh"
 
 namespace ra {
+
+namespace {
+std::atomic<unsigned long long> g_launches{0};
+}  // namespace
+
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
 cudaError_t set_max_dynamic_smem(const void *kernel, int bytes) {
   static std::mutex mu;
@@ -144,6 +151,8 @@ const char *lora_strerror(int status) {
 }
 
 int lora_last_cuda_error(void) { return g_last_cuda_error; }
+
+uint64_t lora_launch_count(void) { return ra::g_launches.load(std::memory_order_relaxed); }
 
 size_t lora_meta_tiles_bytes(int32_t num_slots) {
   if (num_slots < 1) return 0;
