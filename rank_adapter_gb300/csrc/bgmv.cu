@@ -30,6 +30,12 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
+// Shrink CTAs are smaller (128 threads, ~43 KB) so that five fit on an SM and a
+// decode batch's whole shrink grid is resident at once: every A chunk is then
+// requested at kernel start, before the metadata wait.
+constexpr int kSThreads = 128;
+constexpr int kSWarps = kSThreads / 32;
+constexpr int kSMinBlocks = 5;
 constexpr int kTT = 4;               // tokens per tile
 constexpr int kAStageBytes = 16384;  // A bytes per stretch
 constexpr int kStretches = 2;        // stretches per shrink CTA (all in flight at once)
@@ -88,7 +94,7 @@ __device__ __forceinline__ bool load_unit(const BgmvArgs &a, int item, Unit &u, 
   int32_t *rank_s = reinterpret_cast<int32_t *>(smem + a.g.off_rs);
   float *scale_s = reinterpret_cast<float *>(rank_s + kSmallTable);
   if (small_table) {
-    for (int i = threadIdx.x; i < S; i += kThreads) {
+    for (int i = threadIdx.x; i < S; i += blockDim.x) {
       rank_s[i] = a.slot_rank[i];
       scale_s[i] = a.slot_scale[i];
     }
@@ -253,9 +259,9 @@ __device__ __forceinline__ void expand_pass(const TW *Bs, int pw, const float *u
 // Shrink. Grid: (max_items * n_slices, kc_count); block (b, c) -> unit
 // (slice_order[b / max_items], item b % max_items), rows [c * kchunk, +kchunk).
 template <typename TW, int NV>
-__global__ void __launch_bounds__(kThreads, 3) bgmv_shrink_kernel(BgmvArgs a) {
+__global__ void __launch_bounds__(kSThreads, kSMinBlocks) bgmv_shrink_kernel(BgmvArgs a) {
   constexpr int VEC = Elem<TW>::kVec;
-  constexpr int NRG = kThreads / NV;    // row groups
+  constexpr int NRG = kSThreads / NV;   // row groups
   constexpr int NVAL = kTT * VEC;       // accumulators per thread
   constexpr int LPV = 32 / NV;          // lanes sharing one vector column
   constexpr int NKEEP = NVAL / (LPV > NVAL ? NVAL : LPV);
@@ -272,7 +278,7 @@ __global__ void __launch_bounds__(kThreads, 3) bgmv_shrink_kernel(BgmvArgs a) {
   const int klen = min(g.kchunk, g.d_in - k0);
   const int nst = (klen + g.sc - 1) / g.sc;  // stretches of this chunk (<= kStretches)
   const TW *x = static_cast<const TW *>(a.x);
-  float *wred = reinterpret_cast<float *>(smem + g.off_red);  // [kWarps][kTT][r_max]
+  float *wred = reinterpret_cast<float *>(smem + g.off_red);  // [kSWarps][kTT][r_max]
   auto stA = [&](int b) { return reinterpret_cast<TW *>(smem + g.off_ring + b * (g.a_stage + g.x_stage)); };
   auto stX = [&](int b) {
     return reinterpret_cast<TW *>(smem + g.off_ring + b * (g.a_stage + g.x_stage) + g.a_stage);
@@ -284,7 +290,7 @@ __global__ void __launch_bounds__(kThreads, 3) bgmv_shrink_kernel(BgmvArgs a) {
       const int r0 = s * g.sc, nr = min(g.sc, klen - r0);
       const uint4 *src = reinterpret_cast<const uint4 *>(Aslot + (int64_t)r0 * r_max);
       uint4 *dst = reinterpret_cast<uint4 *>(stA(s));
-      for (int i = tid; i < nr * NV; i += kThreads)
+      for (int i = tid; i < nr * NV; i += kSThreads)
         if ((i & (NV - 1)) < nva) cp_async16(dst + i, src + i);
     }
     cp_async_commit();
@@ -326,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 3) bgmv_shrink_kernel(BgmvArgs a) {
       const int r0 = s * g.sc, nr = min(g.sc, klen - r0);
       const int upr = nr / VEC;
       TW *xs = stX(s);
-      for (int t = warp; t < nt; t += kWarps) {
+      for (int t = warp; t < nt; t += kSWarps) {
         const TW *xsrc = x + (int64_t)rows[t] * a.ldx + k0 + r0;
         for (int c = tid & 31; c < upr; c += 32) cp_async16(xs + t * g.sc + c * VEC, xsrc + c * VEC);
       }
@@ -372,11 +378,11 @@ __global__ void __launch_bounds__(kThreads, 3) bgmv_shrink_kernel(BgmvArgs a) {
       wred[(warp * kTT + t) * r_max + v * VEC + e] = acc[i];
     }
     __syncthreads();
-    for (int i = tid; i < nt * r_max; i += kThreads) {
+    for (int i = tid; i < nt * r_max; i += kSThreads) {
       const int t = i / r_max, k = i - t * r_max;
       float sum = 0.f;
 #pragma unroll
-      for (int w2 = 0; w2 < kWarps; ++w2) sum += wred[w2 * kTT * r_max + i];
+      for (int w2 = 0; w2 < kSWarps; ++w2) sum += wred[w2 * kTT * r_max + i];
       if (!a.to_parts) {
         a.buf[((int64_t)slice * a.mv.num_tokens + rows[t]) * r_max + k] = k < u.r_a ? u.scale * sum : 0.f;
       } else {
@@ -515,7 +521,7 @@ Geo make_geo(const lora_layer_desc &d) {
   g.off_ring = off;
   off += kStretches * (g.a_stage + g.x_stage);
   g.off_red = off;
-  off += align16(kWarps * kTT * d.r_max * 4);
+  off += align16(kSWarps * kTT * d.r_max * 4);
   g.smem_shrink = off;
   // expand: one B chunk (+ the zero partner row of an odd rank)
   g.off_b = common;
@@ -563,7 +569,7 @@ cudaError_t launch_shrink_nv(const BgmvArgs &a, cudaStream_t st) {
   cudaError_t e = set_max_dynamic_smem((const void *)k, a.g.smem_shrink);
   if (e != cudaSuccess) return e;
   const int rows_per = a.by_slot ? a.mv.num_slots - 1 : a.max_items;
-  return launch_pdl(k, dim3((unsigned)(rows_per * a.n_slices), (unsigned)a.g.kc_count), dim3(kThreads),
+  return launch_pdl(k, dim3((unsigned)(rows_per * a.n_slices), (unsigned)a.g.kc_count), dim3(kSThreads),
                     (size_t)a.g.smem_shrink, st, 1u, a);
 }
 
