@@ -48,6 +48,8 @@ WORKLOADS = {
     "prefill_gate_up": "prefill SGMV: gate_up_proj 4096->[14336,14336], r=64, 32 slots, 16 requests U[128,2048]",
     "mixed_o_proj": "mixed: o_proj 4096->4096, 128 slots, ranks {8..64} pad 64, 1024 decode + 4x512 prefill",
     "toy_fp32": "toy fp32: d=256, r=16, 8 slots, 6 requests (53 tokens)",
+    "full_decode": "full-model decode step: 32 layers x {qkv, o, gate_up, down}, r=16, 100 resident adapters "
+                   "(~84 MB each), 512 tokens uniform over them; one metadata pass, 128 lora_apply calls",
 }
 
 
@@ -226,7 +228,9 @@ def run_cpu_baseline(args):
                 "error": p.stderr.strip().splitlines()[-1:] }
     r = json.loads(p.stdout.strip().splitlines()[-1])
     return {"value": r["value"], "unit": "tokens/s", "cores": cores, "kind": "oracle",
-            "sample": f"{r['reps']} full steps of the {args.workload} batch (fp64 per-request loop, "
+            "sample": (f"{r['reps']} x one layer (4 groups) of the full-model step, scaled x32 " if
+                       args.workload == "full_decode" else f"{r['reps']} full steps of the {args.workload} batch ") +
+                      "(fp64 per-request loop, "
                       f"numpy BLAS with {cores} threads), {r['seconds']:.1f} s",
             "sec_per_step": r["sec_per_step"]}
 
@@ -235,8 +239,8 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
-    inst = make_workload(args.workload)
-    cfg = {"workload": args.workload, "desc": WORKLOADS[args.workload], "global_batch": inst.num_tokens,
+    batch = 512 if args.workload == "full_decode" else make_workload(args.workload).num_tokens
+    cfg = {"workload": args.workload, "desc": WORKLOADS[args.workload], "global_batch": batch,
            "n_gpus_ignored": args.gpus}
     cpu = run_cpu_baseline(argparse.Namespace(workload=args.workload,
                                               cpu_seconds=max(1.0, args.cpu_seconds)))
@@ -546,13 +550,197 @@ def run_ours(args):
     return 0
 
 
+def full_decode_cpu(args):
+    """The oracle on one layer (4 groups) of the full-model step, scaled to the step; one JSON line."""
+    import numpy as np
+    import oracle
+    import workloads as wl
+    groups = []
+    for inst in wl.full_decode_groups():
+        groups.append(inst)
+        if len(groups) == len(wl.FULL_DECODE_GROUPS):
+            break
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        oracle.prepare_meta(groups[0].token_slot, groups[0].num_slots)
+        for inst in groups:
+            oracle.apply_requests(inst.to_f32(inst.x).astype(np.float64), inst.to_f32(inst.y_in).astype(np.float64),
+                                  oracle.adapters_f64(inst), inst.out_sizes, inst.r_max, inst.req_lengths,
+                                  inst.req_slots, inst.num_slots)
+        reps += 1
+        if time.perf_counter() - t0 >= args.cpu_seconds:
+            break
+    el = time.perf_counter() - t0
+    sec_per_step = el / reps * 32          # 32 layers per step
+    T_L = int((groups[0].token_slot > 0).sum())
+    print(json.dumps({"value": T_L / sec_per_step, "seconds": el, "reps": reps, "sec_per_step": sec_per_step}))
+
+
+def run_full_decode(args):
+    """Full-model decode step: one lora_prepare_meta, then lora_apply for each
+    of the 32 x 4 projection groups (own slot table, x and y each)."""
+    import numpy as np
+    import torch
+    import workloads as wl
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    import rank_adapter_gb300 as ra
+    kind = {"auto": ra.LORA_AUTO, "bgmv": ra.LORA_BGMV, "sgmv": ra.LORA_SGMV}[args.kind]
+
+    def dev(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
+
+    tables, xs, ys, step_bytes, T_L, ts = [], [], [], 0, 0, None
+    for inst in wl.full_decode_groups(seed=5 + 1000 * rank):
+        t = ra.SlotTable(inst.d_in, inst.out_sizes, inst.num_slots, inst.r_max, ra.LORA_BF16)
+        for k, ad in sorted(inst.adapters.items()):
+            t.set_slot(k, ad.rank, ad.scale, [dev(m) for m in ad.A], [dev(m) for m in ad.B])
+        tables.append(t)
+        xs.append(dev(inst.x))
+        ys.append(dev(inst.y_in))
+        alg = algorithmic(inst)
+        step_bytes += alg["step_bytes"]
+        T_L, ts, S = alg["T_L"], inst.token_slot, inst.num_slots
+    torch.cuda.synchronize()
+    T = len(ts)
+    meta = ra.TokenMeta(T, S)
+    meta.token_slot[:T].copy_(torch.from_numpy(ts))
+    meta.set_num_tokens(T)
+    ws = ra.workspace(max(tables, key=lambda t: ra.lora_workspace_bytes(t.desc, T, kind)), T, kind)
+    ws_ptr, ws_bytes = (ws.data_ptr(), ws.numel() * 4) if ws is not None else (0, 0)
+
+    def step(st):
+        ra.check(ra.lora_prepare_meta(meta.c, st), "prepare_meta")
+        for t, x, y in zip(tables, xs, ys):
+            ra.check(ra.lora_apply(t.desc, meta.c, x.data_ptr(), x.stride(0), 0, y.data_ptr(), y.stride(0),
+                                   ra.LORA_BF16, kind, ws_ptr, ws_bytes, st), "apply")
+
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            step(None)
+    stream.synchronize()
+    n0 = ra.lora_launch_count()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step(None)
+    per_step = ra.lora_launch_count() - n0
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            graph.replay()
+    stream.synchronize()
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    clocks = ClockSampler(vis.split(",")[local].strip() if vis else str(local))
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record()
+        for _ in range(args.steps):
+            graph.replay()
+        e1.record()
+    stream.synchronize()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.stop()
+    elapsed_ms = e0.elapsed_time(e1)
+
+    # End to end: token slots and every group's x and y_in in from pinned host memory, every y out.
+    hx = [torch.empty_like(x, device="cpu").pin_memory().copy_(x) for x in xs]
+    hy = [torch.empty_like(y, device="cpu").pin_memory().copy_(y) for y in ys]
+    hout = [torch.empty_like(y, device="cpu").pin_memory() for y in ys]
+    hts = torch.from_numpy(ts).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in hx + hy) + hts.numel() * 4
+    d2h = sum(t.numel() * t.element_size() for t in hout)
+
+    def e2e_step():
+        meta.token_slot[:T].copy_(hts, non_blocking=True)
+        for x, y, a, b in zip(xs, ys, hx, hy):
+            x.copy_(a, non_blocking=True)
+            y.copy_(b, non_blocking=True)
+        step(None)
+        for y, o in zip(ys, hout):
+            o.copy_(y, non_blocking=True)
+
+    ne = max(2, args.e2e_steps)
+    with torch.cuda.stream(stream):
+        e2e_step()
+    stream.synchronize()
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        f0.record()
+        for _ in range(ne):
+            e2e_step()
+        f1.record()
+    stream.synchronize()
+    e2e_ms = f0.elapsed_time(f1)
+    elapsed_ms, e2e_ms, total_TL = reduce_over_ranks(torch, dist, elapsed_ms, e2e_ms, T_L, "cuda")
+    if rank == 0:
+        hbm, tc, src = load_peaks()
+        step_ms = elapsed_ms / args.steps
+        ach = step_bytes / (step_ms * 1e-3) / 1e9
+        line = {
+            "metric": METRIC, "value": total_TL * args.steps / (elapsed_ms * 1e-3), "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": "full_decode", "desc": WORKLOADS["full_decode"], "kind": args.kind,
+                       "path": "fused", "global_batch": T * world, "lora_tokens_per_gpu": T_L,
+                       "parallelism": f"dp{world}", "groups": len(tables),
+                       "l2": f"{step_bytes / 2**30:.1f} GiB touched per step (>> L2)",
+                       "timing": "CUDA-graph replays of one step (library launches only), CUDA events"},
+            "gpu_launches": per_step * args.steps,
+            "step_algorithmic_bytes": step_bytes,
+            "roofline": {"bound": "hbm", "kernel": "step (1 metadata + 128 lora_apply)", "achieved": ach,
+                         "peak": hbm, "unit": "GB/s", "frac": ach / hbm, "peak_source": src,
+                         "algorithmic_bytes_per_launch": step_bytes, "traffic": None},
+            "clocks": clocks.summary(),
+            "e2e": {"value": total_TL * ne / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / ne,
+                    "path": "pinned host token slots and every group's x, y_in -> device; one step; every y -> host"},
+        }
+        if world == 1 and not args.no_cpu_baseline:
+            cores = len(os.sched_getaffinity(0))
+            env = dict(os.environ)
+            for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+                env[v] = str(cores)
+            p = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-child", "--workload", "full_decode",
+                                "--cpu-seconds", str(args.cpu_seconds)], capture_output=True, text=True, env=env,
+                               cwd=ROOT)
+            if p.returncode == 0:
+                r = json.loads(p.stdout.strip().splitlines()[-1])
+                line["cpu_baseline"] = {"value": r["value"], "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                                        "sample": f"{r['reps']} x one layer (4 groups) of the step, scaled x32, "
+                                                  f"{r['seconds']:.1f} s", "sec_per_step": r["sec_per_step"]}
+        print(json.dumps(line))
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.cpu_child:
-        cpu_child(args)
+        if args.workload == "full_decode":
+            full_decode_cpu(args)
+        else:
+            cpu_child(args)
         return 0
     if args.impl == "reference":
         return run_reference(args)
+    if args.workload == "full_decode":
+        return run_full_decode(args)
     return run_ours(args)
 
 

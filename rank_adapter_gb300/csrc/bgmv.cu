@@ -71,7 +71,6 @@ struct BgmvArgs {
   int n_slices, max_items;
   MetaView mv;
   int list;      // int offset of the unit-record list inside the work lists
-  int slot_rec;  // int offset of that list's slot -> record index
   int by_slot;   // shrink: grid rows are slots 1..S-1 (A prefetched before the wait)
   int pre;       // expand: runs right behind this library's shrink / reduce
   const int32_t *slot_rank;
@@ -112,18 +111,6 @@ __device__ __forceinline__ bool load_unit(const BgmvArgs &a, int item, Unit &u, 
   u.r_a = min(max(rk, 0), a.g.r_max);
   u.scale = small_table ? scale_s[u.slot] : a.slot_scale[u.slot];
   return true;
-}
-
-// Record `idx` of the list (count, start, first rows -> rows[]) for a slot
-// whose rank and scale are already known.
-__device__ __forceinline__ void read_record(const BgmvArgs &a, int idx, Unit &u, int *rows) {
-  const int4 *rec = reinterpret_cast<const int4 *>(a.mv.work + a.list + idx * WorkLists::kRec);
-  const int4 h = rec[0], r = rec[1];
-  u.cnt = h.z;
-  u.start = h.w;
-  if (threadIdx.x < kTT)
-    rows[threadIdx.x] = threadIdx.x == 0 ? r.x : threadIdx.x == 1 ? r.y : threadIdx.x == 2 ? r.z : r.w;
-  __syncthreads();
 }
 
 // Widen bf16 / fp32 weights to fp32.
@@ -306,12 +293,19 @@ __global__ void __launch_bounds__(kSThreads, kSMinBlocks) bgmv_shrink_kernel(Bgm
     issue_a(u.slot, (u.r_a + VEC - 1) / VEC);
     pdl_wait();
     pdl_trigger();
-    const int ri = a.mv.work[a.slot_rec + u.slot];
-    if (ri < 0) {  // the slot has no tokens in this batch
+    // The slot-indexed copy of the slot's record: one load, no index lookup.
+    const int4 *rec = reinterpret_cast<const int4 *>(a.mv.work + WorkLists::by_slot(a.mv.num_slots) +
+                                                     u.slot * WorkLists::kRec);
+    const int4 h = rec[0], r = rec[1];
+    if (h.y < 0) {  // the slot has no tokens in this batch
       cp_async_wait_upto(0);
       return;
     }
-    read_record(a, ri, u, rows);
+    u.cnt = h.z;
+    u.start = h.w;
+    if (threadIdx.x < kTT)
+      rows[threadIdx.x] = threadIdx.x == 0 ? r.x : threadIdx.x == 1 ? r.y : threadIdx.x == 2 ? r.z : r.w;
+    __syncthreads();
   } else {
     pdl_wait();
     pdl_trigger();
@@ -532,7 +526,6 @@ Geo make_geo(const lora_layer_desc &d) {
 
 void fill_common(BgmvArgs &a, const lora_layer_desc &d, const MetaView &mv, ListSel sel) {
   a.list = WorkLists::list(mv.num_slots, sel);
-  a.slot_rec = WorkLists::slot_rec(mv.num_slots, sel);
   // Slot-indexed shrink CTAs (A prefetched before the metadata is known) when
   // most slots are likely live: a whole batch of at least one token per slot.
   // A sub-list (AUTO's short segments) may hold few of them.

@@ -136,6 +136,7 @@ __device__ __forceinline__ void cp_async_wait_upto(int n) {
 //   then three lists of S = num_slots unit records (all, small, large), each
 //   record 8 ints: {segment, slot, count, first sorted row, first 4 token rows}
 //   (rows past the count are -1; unused records are all -1),
+//   then S records indexed by slot (slot s's record of the "all" list, or all -1),
 //   then all_tile_start[S+1] and large_tile_start[S+1] (cumulative tile counts),
 //   then for each list, slot_rec[S]: the index of slot s's record in that list, or -1.
 struct WorkLists {
@@ -143,12 +144,13 @@ struct WorkLists {
   static constexpr int kRec = 8;
   static constexpr int kErrWord = 7;
   __host__ __device__ static inline size_t ints(int S) {
-    return kHeader + 3 * (size_t)kRec * S + 2 * ((size_t)S + 1) + 3 * (size_t)S;
+    return kHeader + 4 * (size_t)kRec * S + 2 * ((size_t)S + 1) + 3 * (size_t)S;
   }
   __host__ __device__ static inline int list(int S, int which) { return kHeader + which * kRec * S; }
-  __host__ __device__ static inline int all_tile_start(int S) { return kHeader + 3 * kRec * S; }
-  __host__ __device__ static inline int large_tile_start(int S) { return kHeader + 3 * kRec * S + S + 1; }
-  __host__ __device__ static inline int slot_rec(int S, int which) { return kHeader + 3 * kRec * S + 2 * (S + 1) + which * S; }
+  __host__ __device__ static inline int by_slot(int S) { return kHeader + 3 * kRec * S; }
+  __host__ __device__ static inline int all_tile_start(int S) { return kHeader + 4 * kRec * S; }
+  __host__ __device__ static inline int large_tile_start(int S) { return kHeader + 4 * kRec * S + S + 1; }
+  __host__ __device__ static inline int slot_rec(int S, int which) { return kHeader + 4 * kRec * S + 2 * (S + 1) + which * S; }
 };
 
 enum ListSel { kListAll = 0, kListSmall = 1, kListLarge = 2 };

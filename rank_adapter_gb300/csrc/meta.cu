@@ -4,7 +4,8 @@
 // start offsets that begin at 0), the no-LoRA flag, and the work lists the
 // shrink / expand kernels read.
 //
-// One CTA of 32 warps. Each warp owns a contiguous range of tokens and keeps a
+// One CTA (256 threads for small batches and tables, else 1024). Each warp
+// owns a contiguous range of tokens and keeps a
 // private histogram row in shared memory; a per-slot pass turns the histograms
 // into exclusive per-(warp, slot) offsets; the scatter pass walks every warp's
 // range in batch order and ranks equal slots inside each 32-token chunk with
@@ -15,8 +16,10 @@
 namespace ra {
 namespace {
 
-constexpr int kThreads = 1024;
-constexpr int kWarps = kThreads / 32;
+constexpr int kSmallThreads = 256;  // batches of at most kSmallT tokens and tables of at most 256 slots
+constexpr int kSmallT = 2048;
+constexpr int kBigThreads = 1024;
+constexpr int kCache = 8;            // 32-token chunks per warp whose slot ids stay in registers
 
 struct MetaArgs {
   const int32_t *token_slot;
@@ -43,7 +46,7 @@ __device__ __forceinline__ int warp_incl_scan(int x) {
 
 // Exclusive prefix sums of N values per thread over the whole CTA, with one
 // pair of barriers for all N. All threads call it.
-template <int N>
+template <int N, int kWarps>
 __device__ void block_excl_scan_n(const int (&v)[N], int (&excl)[N], int (&total)[N], int *tmp /*[N][kWarps]*/) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int incl[N];
@@ -53,9 +56,12 @@ __device__ void block_excl_scan_n(const int (&v)[N], int (&excl)[N], int (&total
     if (lane == 31) tmp[i * kWarps + warp] = incl[i];
   }
   __syncthreads();
-  if (warp == 0) {
+  if (warp == 0) {  // lanes past the warp count scan zeros and write nothing
 #pragma unroll
-    for (int i = 0; i < N; ++i) tmp[i * kWarps + lane] = warp_incl_scan(tmp[i * kWarps + lane]);
+    for (int i = 0; i < N; ++i) {
+      const int w = warp_incl_scan(lane < kWarps ? tmp[i * kWarps + lane] : 0);
+      if (lane < kWarps) tmp[i * kWarps + lane] = w;
+    }
   }
   __syncthreads();
 #pragma unroll
@@ -66,7 +72,9 @@ __device__ void block_excl_scan_n(const int (&v)[N], int (&excl)[N], int (&total
   __syncthreads();
 }
 
+template <int kThreads>
 __global__ void __launch_bounds__(kThreads, 1) prepare_meta_kernel(MetaArgs a) {
+  constexpr int kWarps = kThreads / 32;
   extern __shared__ int32_t sm[];
   const int S = a.S, T = a.T;
   const int hs = S + 1;             // odd row stride: a warp reading one slot's column hits 32 banks
@@ -75,6 +83,7 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_meta_kernel(MetaArgs a) {
   int32_t *base_s = tot_s + S;         // [S] first sorted row of each slot
   int32_t *rec_a = base_s + S;         // [S] int offset of the slot's record in the "all" list, or -1
   int32_t *rec_k = rec_a + S;          // [S] int offset of its record in the small or large list
+  // (the slot-indexed copy of a slot's "all" record is at WorkLists::by_slot(S) + slot * kRec)
   __shared__ int tmp[7 * kWarps];
   __shared__ int s_bad;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -89,7 +98,10 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_meta_kernel(MetaArgs a) {
   const int per = (T + kWarps - 1) / kWarps;
   const int t0 = min(T, warp * per), t1 = min(T, t0 + per);
   int bad = 0;
-  for (int b = t0; b < t1; b += 32) {
+  int cache[kCache];  // slot ids of this lane's first kCache chunks, for pass 2
+#pragma unroll
+  for (int c = 0; c < kCache; ++c) cache[c] = 0;
+  for (int b = t0, c = 0; b < t1; b += 32, ++c) {
     const int t = b + lane;
     const bool valid = t < t1;
     int s = 0;
@@ -97,6 +109,9 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_meta_kernel(MetaArgs a) {
       s = a.token_slot[t];
       if (s < 0 || s >= S) { s = 0; ++bad; }
     }
+#pragma unroll
+    for (int cc = 0; cc < kCache; ++cc)
+      if (cc == c) cache[cc] = s;
     const uint32_t act = __ballot_sync(0xffffffffu, valid);
     if (valid) {
       const uint32_t peers = __match_any_sync(act, s);
@@ -109,11 +124,11 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_meta_kernel(MetaArgs a) {
   if (lane == 0 && bad) atomicAdd(&s_bad, bad);
   __syncthreads();
 
-  // Per slot, across the 32 warp rows: exclusive offsets (one warp scan per slot).
+  // Per slot, across the kWarps warp rows: exclusive offsets (one warp scan per slot).
   for (int s = warp; s < S; s += kWarps) {
-    const int c = hist[lane * hs + s];
+    const int c = lane < kWarps ? hist[lane * hs + s] : 0;
     const int incl = warp_incl_scan(c);
-    hist[lane * hs + s] = incl - c;
+    if (lane < kWarps) hist[lane * hs + s] = incl - c;
     if (lane == 31) tot_s[s] = incl;
   }
   __syncthreads();
@@ -127,7 +142,7 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_meta_kernel(MetaArgs a) {
   const int tiles = lora ? (tot + LORA_SGMV_TILE_M - 1) / LORA_SGMV_TILE_M : 0;
   const int vals[7] = {tot, present, lora, small, large, tiles, large ? tiles : 0};
   int ex[7], tl[7];
-  block_excl_scan_n<7>(vals, ex, tl, tmp);
+  block_excl_scan_n<7, kWarps>(vals, ex, tl, tmp);
   const int base = ex[0], seg_idx = ex[1];
   const int nsegs = tl[1], n_all = tl[2], n_small = tl[3], n_large = tl[4];
   const int tiles_all = tl[5], tiles_large = tl[6];
@@ -157,11 +172,18 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_meta_kernel(MetaArgs a) {
     reinterpret_cast<int4 *>(ra_)[1] = none;
     reinterpret_cast<int4 *>(rk_)[0] = head;
     reinterpret_cast<int4 *>(rk_)[1] = none;
+    int32_t *rs_ = W + WorkLists::by_slot(S) + tid * R;
+    reinterpret_cast<int4 *>(rs_)[0] = head;
+    reinterpret_cast<int4 *>(rs_)[1] = none;
     W[WorkLists::all_tile_start(S) + ex[2]] = ex[5];
     if (large) W[WorkLists::large_tile_start(S) + ex[4]] = ex[6];
   }
   // Unused records, tails, scalars.
   const int4 none = make_int4(-1, -1, -1, -1);
+  if (tid < S && !lora) {
+    reinterpret_cast<int4 *>(W + WorkLists::by_slot(S) + tid * R)[0] = none;
+    reinterpret_cast<int4 *>(W + WorkLists::by_slot(S) + tid * R)[1] = none;
+  }
   for (int i = tid; i < S; i += kThreads) {
     if (i >= n_all) {
       reinterpret_cast<int4 *>(W + WorkLists::list(S, kListAll) + i * R)[0] = none;
@@ -193,13 +215,19 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_meta_kernel(MetaArgs a) {
 
   // Pass 2: stable scatter of token indices; the first 4 rows of each LoRA
   // segment also go into its unit records.
-  for (int b = t0; b < t1; b += 32) {
+  for (int b = t0, c = 0; b < t1; b += 32, ++c) {
     const int t = b + lane;
     const bool valid = t < t1;
     int s = 0;
     if (valid) {
-      s = a.token_slot[t];
-      if (s < 0 || s >= S) s = 0;
+      if (c < kCache) {
+#pragma unroll
+        for (int cc = 0; cc < kCache; ++cc)
+          if (cc == c) s = cache[cc];
+      } else {
+        s = a.token_slot[t];
+        if (s < 0 || s >= S) s = 0;
+      }
     }
     const uint32_t act = __ballot_sync(0xffffffffu, valid);
     uint32_t peers = 0;
@@ -210,6 +238,7 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_meta_kernel(MetaArgs a) {
       if (rel < 4 && rec_a[s] >= 0) {
         W[rec_a[s] + 4 + rel] = t;
         W[rec_k[s] + 4 + rel] = t;
+        W[WorkLists::by_slot(S) + s * WorkLists::kRec + 4 + rel] = t;
       }
     }
     __syncwarp();
@@ -233,10 +262,13 @@ cudaError_t launch_prepare_meta(const lora_meta &m, cudaStream_t st) {
   a.no_lora = m.no_lora;
   a.status = m.status;
   a.work = static_cast<int32_t *>(m.tiles);
-  const size_t smem = ((size_t)kWarps * (m.num_slots + 1) + 4 * (size_t)m.num_slots) * sizeof(int32_t);
-  cudaError_t e = set_max_dynamic_smem((const void *)prepare_meta_kernel, (int)smem);
+  const bool small = m.num_tokens <= kSmallT && m.num_slots <= kSmallThreads;
+  const int nt = small ? kSmallThreads : kBigThreads;
+  void (*k)(MetaArgs) = small ? prepare_meta_kernel<kSmallThreads> : prepare_meta_kernel<kBigThreads>;
+  const size_t smem = ((size_t)(nt / 32) * (m.num_slots + 1) + 4 * (size_t)m.num_slots) * sizeof(int32_t);
+  cudaError_t e = set_max_dynamic_smem((const void *)k, (int)smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(prepare_meta_kernel, dim3(1), dim3(kThreads), smem, st, 1u, a);
+  return launch_pdl(k, dim3(1), dim3(nt), smem, st, 1u, a);
 }
 
 }  // namespace ra

@@ -50,7 +50,7 @@ def test_strerror_and_sizes(ra):
         assert ra.lora_strerror(s) and "unknown" not in ra.lora_strerror(s)
     assert "unknown" in ra.lora_strerror(99)
     assert ra.lora_meta_tiles_bytes(0) == 0
-    assert ra.lora_meta_tiles_bytes(64) == (8 + 3 * 8 * 64 + 2 * 65 + 3 * 64) * 4
+    assert ra.lora_meta_tiles_bytes(64) == (8 + 4 * 8 * 64 + 2 * 65 + 3 * 64) * 4
     assert ra.lora_last_cuda_error() == 0
     assert ra.lora_launch_count() == 0      # nothing launched on a host-only run
 

@@ -36,7 +36,8 @@ def _run(ra, ts, S):
 def _work_lists(ref, S):
     """The work lists by their definition: LoRA segments (slot != 0), split at
     LORA_SGMV_MIN_ROWS, as 8-int records {segment, slot, count, start, first 4
-    rows (-1 past the count)}, unused records all -1, then cumulative counts of
+    rows (-1 past the count)}, unused records all -1, then the "all" records
+    indexed by slot (all -1 for absent slots), then cumulative counts of
     128-row tiles over all LoRA segments and over the large ones, then per
     list the record index of every slot (-1 when absent)."""
     import rank_adapter_gb300 as ra
@@ -67,8 +68,15 @@ def _work_lists(ref, S):
             idx[slot[i]] = j
         return idx
 
+    def by_slot():
+        out = [-1] * 8 * S
+        for i in segs:
+            out[8 * slot[i]:8 * slot[i] + 8] = rec(i)
+        return out
+
     ca, cl = cum(segs), cum(large)
-    w = [len(segs), len(small), len(large), ca[-1], cl[-1], 0, 0, 0] + lst(segs) + lst(small) + lst(large) + ca + cl
+    w = [len(segs), len(small), len(large), ca[-1], cl[-1], 0, 0, 0] + lst(segs) + lst(small) + lst(large)
+    w += by_slot() + ca + cl
     w += slot_index(segs) + slot_index(small) + slot_index(large)
     return np.asarray(w, np.int32)
 
