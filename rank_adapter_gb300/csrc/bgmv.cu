@@ -41,6 +41,8 @@ constexpr int kAStageBytes = 16384;  // A bytes per stretch
 constexpr int kStretches = 2;        // stretches per shrink CTA (all in flight at once)
 constexpr int kBPassBytes = 32768;   // B bytes per expand CTA
 constexpr int kSmallTable = 256;     // slot tables up to this size: rank / scale copied whole
+constexpr int kRowsWin = 32;         // token rows of a unit kept in shared memory (a sliding window)
+constexpr int kKCReg = 16;           // expand: chunk partials of the next tile held in registers
 
 struct Geo {
   int d_in, r_max;
@@ -209,7 +211,8 @@ __device__ __forceinline__ void issue_b(TW *Bs, int pw, const TW *Bslot, int out
 // the two lanes of packed FMAs.
 template <typename TW, typename TY>
 __device__ __forceinline__ void expand_pass(const TW *Bs, int pw, const float *us, int r_max, int r_pad,
-                                            const int *rows, int nt, TY *y, int64_t ldy, int col_base, int pcn) {
+                                            const int *rows, int rbase, int nt, TY *y, int64_t ldy, int col_base,
+                                            int pcn) {
   for (int cq = threadIdx.x * 4; cq < pcn; cq += kThreads * 4) {
     float2 acc[kTT][4];
 #pragma unroll
@@ -232,7 +235,7 @@ __device__ __forceinline__ void expand_pass(const TW *Bs, int pw, const float *u
 #pragma unroll
     for (int t = 0; t < kTT; ++t) {
       if (t < nt) {
-        TY *yp = y + (int64_t)rows[t] * ldy + col_base + cq;
+        TY *yp = y + (int64_t)rows[(rbase + t) % kRowsWin] * ldy + col_base + cq;
         float yv[4];
         load4(yp, yv);
 #pragma unroll
@@ -314,26 +317,28 @@ __global__ void __launch_bounds__(kSThreads, kSMinBlocks) bgmv_shrink_kernel(Bgm
   }
   const int nva = (u.r_a + VEC - 1) / VEC;
   const int ntiles = (u.cnt + kTT - 1) / kTT;
-  for (int tile = 0; tile < ntiles; ++tile) {
+  // Token i of the unit is row rows[i % kRowsWin]. The x columns of a tile
+  // are requested as soon as the previous tile's products are done, so their
+  // latency overlaps that tile's reduction and stores.
+  auto issue_x = [&](int tile) {
     const int nt = min(kTT, u.cnt - tile * kTT);
-    if (tile > 0) {
-      __syncthreads();
-      if (tid < nt) rows[tid] = a.mv.sorted_rows[u.start + tile * kTT + tid];
-      __syncthreads();
-    }
-    // This tile's x columns for every stretch (the A chunk stays resident across tiles).
     for (int s = 0; s < nst; ++s) {
       const int r0 = s * g.sc, nr = min(g.sc, klen - r0);
       const int upr = nr / VEC;
       TW *xs = stX(s);
       for (int t = warp; t < nt; t += kSWarps) {
-        const TW *xsrc = x + (int64_t)rows[t] * a.ldx + k0 + r0;
+        const TW *xsrc = x + (int64_t)rows[(tile * kTT + t) % kRowsWin] * a.ldx + k0 + r0;
         for (int c = tid & 31; c < upr; c += 32) cp_async16(xs + t * g.sc + c * VEC, xsrc + c * VEC);
       }
     }
     cp_async_commit();
+  };
+  issue_x(0);  // rows 0..kTT-1 came with the unit record
+  for (int i = kTT + tid; i < min(u.cnt, kRowsWin); i += kSThreads) rows[i] = a.mv.sorted_rows[u.start + i];
+  for (int tile = 0; tile < ntiles; ++tile) {
+    const int nt = min(kTT, u.cnt - tile * kTT);
     cp_async_wait_upto(0);
-    __syncthreads();
+    __syncthreads();  // this tile's x, the A chunk and the token rows are in shared memory
     float2 acc2[NVAL / 2];  // (acc[t][2p], acc[t][2p + 1]) at t * VEC / 2 + p
 #pragma unroll
     for (int i = 0; i < NVAL / 2; ++i) acc2[i] = make_float2(0.f, 0.f);
@@ -357,6 +362,10 @@ __global__ void __launch_bounds__(kSThreads, kSMinBlocks) bgmv_shrink_kernel(Bgm
         }
       }
     }
+    __syncthreads();  // every thread is done with the x stage
+    const int nxt = tile + 1;
+    const bool next_in_window = nxt < ntiles && (nxt * kTT) % kRowsWin != 0;
+    if (next_in_window) issue_x(nxt);
     // Row groups (in-warp), then warps in order. Entries of absent tokens
     // (t >= nt) carry garbage and are never written out.
     float acc[NVAL];
@@ -378,13 +387,20 @@ __global__ void __launch_bounds__(kSThreads, kSMinBlocks) bgmv_shrink_kernel(Bgm
 #pragma unroll
       for (int w2 = 0; w2 < kSWarps; ++w2) sum += wred[w2 * kTT * r_max + i];
       if (!a.to_parts) {
-        a.buf[((int64_t)slice * a.mv.num_tokens + rows[t]) * r_max + k] = k < u.r_a ? u.scale * sum : 0.f;
+        a.buf[((int64_t)slice * a.mv.num_tokens + rows[(tile * kTT + t) % kRowsWin]) * r_max + k] =
+            k < u.r_a ? u.scale * sum : 0.f;
       } else {
         const int64_t pos = (int64_t)slice * a.mv.num_tokens + u.start + tile * kTT + t;
         a.part[(pos * g.kc_count + kc) * r_max + k] = sum;
       }
     }
-    __syncthreads();  // rows / wred / ring are reused by the next tile
+    if (nxt < ntiles && !next_in_window) {  // the next tile starts a new window of token rows
+      __syncthreads();
+      for (int i = tid; i < kRowsWin && nxt * kTT + i < u.cnt; i += kSThreads)
+        rows[i] = a.mv.sorted_rows[u.start + nxt * kTT + i];
+      __syncthreads();
+      issue_x(nxt);
+    }
   }
 }
 
@@ -418,7 +434,7 @@ __global__ void __launch_bounds__(kThreads) bgmv_reduce_kernel(BgmvArgs a) {
 // Expand: one CTA per (segment, slice, column chunk of pw). Grid: (chunks over all slices, max_items).
 // u comes from the chunk partials (u_parts) or from the u buffer.
 template <typename TW, typename TY>
-__global__ void __launch_bounds__(kThreads, 4) bgmv_expand_kernel(BgmvArgs a) {
+__global__ void __launch_bounds__(kThreads, 3) bgmv_expand_kernel(BgmvArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
   // Behind this library's shrink (or reduce), the metadata and the slot
   // table are complete (see pdl_wait): the record, the B chunk and the y
@@ -450,33 +466,80 @@ __global__ void __launch_bounds__(kThreads, 4) bgmv_expand_kernel(BgmvArgs a) {
   cp_async_commit();
   if (r_pad > u.r_a)  // odd rank: the partner row of the last pair is zero
     for (int c = threadIdx.x; c < g.pw; c += kThreads) Bs[u.r_a * g.pw + c] = Elem<TW>::from_f(0.f);
+  // Token i of the unit is row rows[i % kRowsWin]; the first kTT came with
+  // the record, the rest of the window (metadata, complete before this kernel
+  // starts behind this library's shrink) and their y lines are fetched now.
+  for (int i = kTT + (int)threadIdx.x; i < min(u.cnt, kRowsWin); i += kThreads)
+    rows[i] = a.mv.sorted_rows[u.start + i];
+  __syncthreads();
+  if ((int)threadIdx.x < min(u.cnt, kRowsWin))
+    prefetch_l2(y + (int64_t)rows[threadIdx.x] * a.ldy + col_base, (uint32_t)(pcn * sizeof(TY)));
   if (a.pre) {
-    if (threadIdx.x < min(kTT, u.cnt))
-      prefetch_l2(y + (int64_t)rows[threadIdx.x] * a.ldy + col_base, (uint32_t)(pcn * sizeof(TY)));
     pdl_wait();
     pdl_trigger();
   }
-  const int ntiles = (u.cnt + kTT - 1) / kTT;
-  for (int tile = 0; tile < ntiles; ++tile) {
+  // u of token t (of the unit) and rank index k: the partials summed in chunk
+  // order and scaled, or the u buffer. A tile's values go to one of two buffers.
+  auto u_val = [&](int tok, int k) -> float {
+    if (k >= u.r_a) return 0.f;
+    if (a.u_parts) return u_from_partials(a, s, u.start + tok, k, u);
+    return a.u_in[((int64_t)s * a.mv.num_tokens + rows[tok % kRowsWin]) * r_max + k];
+  };
+  auto fill = [&](int tile, float *dst) {
     const int nt = min(kTT, u.cnt - tile * kTT);
-    if (tile > 0) {
-      __syncthreads();
-      if (threadIdx.x < nt) rows[threadIdx.x] = a.mv.sorted_rows[u.start + tile * kTT + threadIdx.x];
-      __syncthreads();
-    }
-    if (threadIdx.x < nt) prefetch_l2(y + (int64_t)rows[threadIdx.x] * a.ldy + col_base, (uint32_t)(pcn * sizeof(TY)));
     for (int i = threadIdx.x; i < kTT * r_max; i += kThreads) {
       const int t = i / r_max, k = i - t * r_max;
-      float val = 0.f;
-      if (t < nt) {
-        if (a.u_parts) val = u_from_partials(a, s, u.start + tile * kTT + t, k, u);
-        else if (k < u.r_a) val = a.u_in[((int64_t)s * a.mv.num_tokens + rows[t]) * r_max + k];
-      }
-      us[i] = val;
+      dst[i] = t < nt ? u_val(tile * kTT + t, k) : 0.f;
     }
+  };
+  // The next tile's partials are loaded into registers before this tile's
+  // products and summed after them, so their latency is hidden.
+  const bool overlap = a.u_parts && g.kc_count <= kKCReg && kTT * r_max <= kThreads;
+  const int ntiles = (u.cnt + kTT - 1) / kTT;
+  fill(0, us);
+  for (int tile = 0; tile < ntiles; ++tile) {
+    const int nt = min(kTT, u.cnt - tile * kTT);
+    float *cur = us + (tile & 1) * kTT * r_max, *nxt_us = us + ((tile + 1) & 1) * kTT * r_max;
     cp_async_wait_upto(0);
-    __syncthreads();
-    expand_pass<TW, TY>(Bs, g.pw, us, r_max, r_pad, rows, nt, y, a.ldy, col_base, pcn);
+    __syncthreads();  // the B chunk, this tile's u and token rows are in shared memory
+    const int nxt = tile + 1;
+    const bool next_in_window = nxt < ntiles && (nxt * kTT) % kRowsWin != 0;
+    float pref[kKCReg];
+    const int i = threadIdx.x, pt = i / r_max, pk = i - pt * r_max;
+    const bool mine = overlap && next_in_window && i < kTT * r_max && pt < min(kTT, u.cnt - nxt * kTT) &&
+                      pk < u.r_a;
+    if (mine) {
+      const float *p = a.u_in + (((int64_t)s * a.mv.num_tokens + u.start + nxt * kTT + pt) * g.kc_count) * r_max + pk;
+#pragma unroll
+      for (int c = 0; c < kKCReg; ++c)
+        if (c < g.kc_count) pref[c] = p[c * r_max];
+    }
+    expand_pass<TW, TY>(Bs, g.pw, cur, r_max, r_pad, rows, tile * kTT, nt, y, a.ldy, col_base, pcn);
+    if (nxt < ntiles) {
+      if (!next_in_window) {  // a new window of token rows
+        __syncthreads();
+        for (int j = threadIdx.x; j < kRowsWin && nxt * kTT + j < u.cnt; j += kThreads)
+          rows[j] = a.mv.sorted_rows[u.start + nxt * kTT + j];
+        __syncthreads();
+        if ((int)threadIdx.x < min(u.cnt - nxt * kTT, kRowsWin))
+          prefetch_l2(y + (int64_t)rows[threadIdx.x] * a.ldy + col_base, (uint32_t)(pcn * sizeof(TY)));
+        fill(nxt, nxt_us);
+      } else if (overlap) {
+        if (i < kTT * r_max) {
+          float v = 0.f;
+          if (mine) {  // same order and arithmetic as u_from_partials
+            float sum = 0.f;
+#pragma unroll
+            for (int c = 0; c < kKCReg; ++c)
+              if (c < g.kc_count) sum += pref[c];
+            v = u.scale * sum;
+          }
+          nxt_us[i] = v;
+        }
+      } else {
+        fill(nxt, nxt_us);
+      }
+    }
   }
 }
 
@@ -507,9 +570,9 @@ Geo make_geo(const lora_layer_desc &d) {
   g.off_rs = off;
   off += align16(2 * kSmallTable * 4);
   g.off_rows = off;
-  off += align16(kTT * 4);
+  off += align16(kRowsWin * 4);
   g.off_u = off;
-  off += align16(kTT * d.r_max * 4);
+  off += align16(2 * kTT * d.r_max * 4);  // two tiles of u (expand)
   const int common = off;
   // shrink: ring + reduction buffer
   g.off_ring = off;
