@@ -13,8 +13,8 @@ replicated on the device R times so that the rotation touches more than
 Warm-up steps run eagerly; the K timed steps are CUDA-graph replays
 bracketed by CUDA events on the launching stream, with a barrier and
 torch.cuda.synchronize() on both sides; the value is the max over ranks.
-Per-kernel durations come from CUDA events recorded around every launch
-inside the captured graph. The end-to-end figure repeats the step through
+Per-call durations come from graphs of G launches of one call alone (on
+inputs the steps prepared), timed around their replays. The end-to-end figure repeats the step through
 the same ABI with pinned host buffers: the copies in and out are inside its
 timed region.
 
@@ -284,10 +284,26 @@ class Replica:
         return self.table.nbytes() + self.x.numel() * self.x.element_size() + \
             self.y.numel() * self.y.element_size()
 
-    def launch(self, ra, i, ev=None, path="fused"):
+    def launch(self, ra, i, ev=None, path="fused", only=None):
         """Enqueue one step on the current stream: prepare_meta then lora_apply (path "fused")
-        or lora_shrink + lora_expand (path "split"). ev: optional events around each call."""
+        or lora_shrink + lora_expand (path "split"). ev: optional events around each call.
+        only: enqueue just that call ("meta", "apply", "shrink" or "expand"; the metadata and
+        buffers it reads were prepared by earlier steps)."""
         st = None
+        if only is not None:
+            if only == "meta":
+                ra.check(ra.lora_prepare_meta(self.meta.c, st), "prepare_meta")
+            elif only == "apply":
+                ra.check(ra.lora_apply(self.table.desc, self.meta.c, self.x.data_ptr(), self.x.stride(0), 0,
+                                       self.y.data_ptr(), self.y.stride(0), self.ydt, self.kind, self.ws_ptr,
+                                       self.ws_bytes, st), "apply")
+            elif only == "shrink":
+                ra.check(ra.lora_shrink(self.table.desc, self.meta.c, self.x.data_ptr(), self.x.stride(0),
+                                        self.buf.data_ptr(), self.kind, self.ws_ptr, self.ws_bytes, st), "shrink")
+            else:
+                ra.check(ra.lora_expand(self.table.desc, self.meta.c, self.buf.data_ptr(), self.y.data_ptr(),
+                                        self.y.stride(0), self.ydt, self.kind, st), "expand")
+            return
         if ev is not None:
             ev[0].record()
         ra.check(ra.lora_prepare_meta(self.meta.c, st), "prepare_meta")
@@ -311,38 +327,25 @@ class Replica:
             ev[3].record()
 
 
-def _external_events(torch):
-    try:
-        torch.cuda.Event(enable_timing=True, external=True)
-        return True
-    except TypeError:
-        return False
-
-
 KERNELS = {"fused": ("meta", "apply"), "split": ("meta", "shrink", "expand")}
 
 
 def time_path(torch, ra, reps, stream, path, steps, G, clocks=None, dist=None):
     """Time `steps` steps of one path as replays of a CUDA graph of G steps (rotating replicas).
 
-    The timed graph holds only the library's launches. Per-kernel durations come
-    afterwards from a second graph of the same G steps with CUDA events recorded
-    around each call (event nodes add their own latency, so those durations are
-    upper bounds). Returns (elapsed_ms over all steps, per-kernel mean ms, how).
+    The timed graph holds only the library's launches. Per-call durations come
+    afterwards from graphs of G launches of one call alone. Returns (elapsed_ms
+    over all steps, per-call mean ms, how, kernels launched per step).
     """
     R = len(reps)
     names = KERNELS[path]
 
     def capture(n, with_events):
-        evs = None
-        if with_events:
-            evs = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(len(names) + 1)]
-                   for _ in range(n)]
         gr = torch.cuda.CUDAGraph()
         with torch.cuda.graph(gr, stream=stream):
             for i in range(n):
-                reps[i % R].launch(ra, i, evs[i] if evs else None, path=path)
-        return gr, evs
+                reps[i % R].launch(ra, i, path=path)
+        return gr, None
 
     n0 = ra.lora_launch_count()
     graph, _ = capture(G, False)
@@ -376,24 +379,28 @@ def time_path(torch, ra, reps, stream, path, steps, G, clocks=None, dist=None):
         clocks.stop()
     elapsed_ms = start.elapsed_time(end)
 
-    if _external_events(torch):
-        gev, evs = capture(G, True)
+    # Per call: a graph of G launches of that call alone (on metadata and
+    # buffers the steps above prepared), timed around its replays. No event
+    # sits between the kernels, so these are the calls' own durations.
+    durs = {}
+    for name in names:
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=stream):
+            for i in range(G):
+                reps[i % R].launch(ra, i, path=path, only=name)
         with torch.cuda.stream(stream):
+            gr.replay()
+        stream.synchronize()
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            c0.record()
             for _ in range(3):
-                gev.replay()
+                gr.replay()
+            c1.record()
         stream.synchronize()
-        durs = {k: [e[j].elapsed_time(e[j + 1]) for e in evs] for j, k in enumerate(names)}
-        how = f"CUDA events around each call in a separate captured graph of {G} steps (upper bounds)"
-    else:
-        n = min(200, max(R, steps))
-        evs2 = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)] for _ in range(n)]
-        with torch.cuda.stream(stream):
-            torch.cuda._sleep(int(2e8))
-            for i in range(n):
-                reps[i % R].launch(ra, i, evs2[i], path=path)
-        stream.synchronize()
-        durs = {k: [e[j].elapsed_time(e[j + 1]) for e in evs2] for j, k in enumerate(names)}
-        how = f"CUDA events around {n} eager launches enqueued behind a sleep kernel (upper bounds)"
+        durs[name] = [c0.elapsed_time(c1) / (3 * G)]
+    how = (f"each call alone: CUDA-graph replays of {G} launches of that call on prepared inputs, "
+           f"CUDA events around the replays")
     return elapsed_ms, {k: statistics.mean(v) for k, v in durs.items()}, how, per_step
 
 
