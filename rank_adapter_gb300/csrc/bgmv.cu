@@ -248,73 +248,27 @@ __device__ __forceinline__ void expand_pass(const TW *Bs, int pw, const float *u
 
 // Shrink. Grid: (max_items * n_slices, kc_count); block (b, c) -> unit
 // (slice_order[b / max_items], item b % max_items), rows [c * kchunk, +kchunk).
-template <typename TW, int NV>
-__global__ void __launch_bounds__(kSThreads, kSMinBlocks) bgmv_shrink_kernel(BgmvArgs a) {
+// The token tiles of one shrink unit, with NVE lanes per A row (the slot's
+// rank rounded up to whole 16-byte vectors, then to a power of two): a
+// low-rank slot puts its threads on more row groups instead of idle lanes.
+template <typename TW, int NVE>
+__device__ __forceinline__ void shrink_tiles(const BgmvArgs &a, unsigned char *smem, int *rows, const Unit &u,
+                                             int slice, int kc, int k0, int klen, int nst) {
   constexpr int VEC = Elem<TW>::kVec;
-  constexpr int NRG = kSThreads / NV;   // row groups
+  constexpr int NRG = kSThreads / NVE;  // row groups
   constexpr int NVAL = kTT * VEC;       // accumulators per thread
-  constexpr int LPV = 32 / NV;          // lanes sharing one vector column
+  constexpr int LPV = 32 / NVE;         // lanes sharing one vector column
   constexpr int NKEEP = NVAL / (LPV > NVAL ? NVAL : LPV);
-  extern __shared__ __align__(16) unsigned char smem[];
   const Geo &g = a.g;
-  const int kc = blockIdx.y;
-  const int rows_per = a.by_slot ? a.mv.num_slots - 1 : a.max_items;
-  const int slice = a.slice_order[blockIdx.x / rows_per];
-  int *rows = reinterpret_cast<int *>(smem + g.off_rows);
   const int tid = threadIdx.x, warp = tid >> 5;
-  const int v = tid % NV, rq = tid / NV;
+  const int v = tid % NVE, rq = tid / NVE;
   const int r_max = g.r_max;
-  const int k0 = kc * g.kchunk;
-  const int klen = min(g.kchunk, g.d_in - k0);
-  const int nst = (klen + g.sc - 1) / g.sc;  // stretches of this chunk (<= kStretches)
   const TW *x = static_cast<const TW *>(a.x);
   float *wred = reinterpret_cast<float *>(smem + g.off_red);  // [kSWarps][kTT][r_max]
   auto stA = [&](int b) { return reinterpret_cast<TW *>(smem + g.off_ring + b * (g.a_stage + g.x_stage)); };
   auto stX = [&](int b) {
     return reinterpret_cast<TW *>(smem + g.off_ring + b * (g.a_stage + g.x_stage) + g.a_stage);
   };
-  // All A stretches of this chunk in flight at once, rank tail skipped.
-  auto issue_a = [&](int slot, int nva) {
-    const TW *Aslot = static_cast<const TW *>(a.A[slice]) + ((int64_t)slot * g.d_in + k0) * r_max;
-    for (int s = 0; s < nst; ++s) {
-      const int r0 = s * g.sc, nr = min(g.sc, klen - r0);
-      const uint4 *src = reinterpret_cast<const uint4 *>(Aslot + (int64_t)r0 * r_max);
-      uint4 *dst = reinterpret_cast<uint4 *>(stA(s));
-      for (int i = tid; i < nr * NV; i += kSThreads)
-        if ((i & (NV - 1)) < nva) cp_async16(dst + i, src + i);
-    }
-    cp_async_commit();
-  };
-  Unit u;
-  if (a.by_slot) {
-    // The slot table is complete before any kernel of this library starts
-    // (see pdl_wait), so this slot's A chunk streams in while the metadata
-    // kernel may still be running.
-    u.slot = 1 + (int)blockIdx.x % rows_per;
-    u.r_a = min(max(a.slot_rank[u.slot], 0), r_max);
-    u.scale = a.slot_scale[u.slot];
-    issue_a(u.slot, (u.r_a + VEC - 1) / VEC);
-    pdl_wait();
-    pdl_trigger();
-    // The slot-indexed copy of the slot's record: one load, no index lookup.
-    const int4 *rec = reinterpret_cast<const int4 *>(a.mv.work + WorkLists::by_slot(a.mv.num_slots) +
-                                                     u.slot * WorkLists::kRec);
-    const int4 h = rec[0], r = rec[1];
-    if (h.y < 0) {  // the slot has no tokens in this batch
-      cp_async_wait_upto(0);
-      return;
-    }
-    u.cnt = h.z;
-    u.start = h.w;
-    if (threadIdx.x < kTT)
-      rows[threadIdx.x] = threadIdx.x == 0 ? r.x : threadIdx.x == 1 ? r.y : threadIdx.x == 2 ? r.z : r.w;
-    __syncthreads();
-  } else {
-    pdl_wait();
-    pdl_trigger();
-    if (!load_unit(a, (int)blockIdx.x % rows_per, u, smem, rows)) return;
-    issue_a(u.slot, (u.r_a + VEC - 1) / VEC);
-  }
   const int nva = (u.r_a + VEC - 1) / VEC;
   const int ntiles = (u.cnt + kTT - 1) / kTT;
   // Token i of the unit is row rows[i % kRowsWin]. The x columns of a tile
@@ -374,7 +328,7 @@ __global__ void __launch_bounds__(kSThreads, kSMinBlocks) bgmv_shrink_kernel(Bgm
       acc[2 * i] = acc2[i].x;
       acc[2 * i + 1] = acc2[i].y;
     }
-    const int off = reduce_scatter<NVAL, NV>(acc);
+    const int off = reduce_scatter<NVAL, NVE>(acc);
 #pragma unroll
     for (int i = 0; i < NKEEP; ++i) {
       const int idx = off + i, t = idx / VEC, e = idx % VEC;
@@ -400,6 +354,78 @@ __global__ void __launch_bounds__(kSThreads, kSMinBlocks) bgmv_shrink_kernel(Bgm
         rows[i] = a.mv.sorted_rows[u.start + nxt * kTT + i];
       __syncthreads();
       issue_x(nxt);
+    }
+  }
+}
+
+template <typename TW, int NV>
+__global__ void __launch_bounds__(kSThreads, kSMinBlocks) bgmv_shrink_kernel(BgmvArgs a) {
+  constexpr int VEC = Elem<TW>::kVec;
+  extern __shared__ __align__(16) unsigned char smem[];
+  const Geo &g = a.g;
+  const int kc = blockIdx.y;
+  const int rows_per = a.by_slot ? a.mv.num_slots - 1 : a.max_items;
+  const int slice = a.slice_order[blockIdx.x / rows_per];
+  int *rows = reinterpret_cast<int *>(smem + g.off_rows);
+  const int tid = threadIdx.x;
+  const int r_max = g.r_max;
+  const int k0 = kc * g.kchunk;
+  const int klen = min(g.kchunk, g.d_in - k0);
+  const int nst = (klen + g.sc - 1) / g.sc;  // stretches of this chunk (<= kStretches)
+  auto stA = [&](int b) { return reinterpret_cast<TW *>(smem + g.off_ring + b * (g.a_stage + g.x_stage)); };
+  // All A stretches of this chunk in flight at once, rank tail skipped.
+  auto issue_a = [&](int slot, int nva) {
+    const TW *Aslot = static_cast<const TW *>(a.A[slice]) + ((int64_t)slot * g.d_in + k0) * r_max;
+    for (int s = 0; s < nst; ++s) {
+      const int r0 = s * g.sc, nr = min(g.sc, klen - r0);
+      const uint4 *src = reinterpret_cast<const uint4 *>(Aslot + (int64_t)r0 * r_max);
+      uint4 *dst = reinterpret_cast<uint4 *>(stA(s));
+      for (int i = tid; i < nr * NV; i += kSThreads)
+        if ((i & (NV - 1)) < nva) cp_async16(dst + i, src + i);
+    }
+    cp_async_commit();
+  };
+  Unit u;
+  if (a.by_slot) {
+    // The slot table is complete before any kernel of this library starts
+    // (see pdl_wait), so this slot's A chunk streams in while the metadata
+    // kernel may still be running.
+    u.slot = 1 + (int)blockIdx.x % rows_per;
+    u.r_a = min(max(a.slot_rank[u.slot], 0), r_max);
+    u.scale = a.slot_scale[u.slot];
+    issue_a(u.slot, (u.r_a + VEC - 1) / VEC);
+    pdl_wait();
+    pdl_trigger();
+    // The slot-indexed copy of the slot's record: one load, no index lookup.
+    const int4 *rec = reinterpret_cast<const int4 *>(a.mv.work + WorkLists::by_slot(a.mv.num_slots) +
+                                                     u.slot * WorkLists::kRec);
+    const int4 h = rec[0], r = rec[1];
+    if (h.y < 0) {  // the slot has no tokens in this batch
+      cp_async_wait_upto(0);
+      return;
+    }
+    u.cnt = h.z;
+    u.start = h.w;
+    if (threadIdx.x < kTT)
+      rows[threadIdx.x] = threadIdx.x == 0 ? r.x : threadIdx.x == 1 ? r.y : threadIdx.x == 2 ? r.z : r.w;
+    __syncthreads();
+  } else {
+    pdl_wait();
+    pdl_trigger();
+    if (!load_unit(a, (int)blockIdx.x % rows_per, u, smem, rows)) return;
+    issue_a(u.slot, (u.r_a + VEC - 1) / VEC);
+  }
+  int nve = 1;  // lanes per A row this unit needs (a power of two <= NV)
+  while (nve < NV && nve * VEC < u.r_a) nve <<= 1;
+  if (nve >= NV) shrink_tiles<TW, NV>(a, smem, rows, u, slice, kc, k0, klen, nst);
+  else if constexpr (NV >= 2) {
+    if (nve * 2 >= NV) shrink_tiles<TW, (NV >= 2 ? NV / 2 : 1)>(a, smem, rows, u, slice, kc, k0, klen, nst);
+    else if constexpr (NV >= 4) {
+      if (nve * 4 >= NV) shrink_tiles<TW, (NV >= 4 ? NV / 4 : 1)>(a, smem, rows, u, slice, kc, k0, klen, nst);
+      else if constexpr (NV >= 8) {
+        if (nve * 8 >= NV) shrink_tiles<TW, (NV >= 8 ? NV / 8 : 1)>(a, smem, rows, u, slice, kc, k0, klen, nst);
+        else shrink_tiles<TW, (NV >= 16 ? NV / 16 : 1)>(a, smem, rows, u, slice, kc, k0, klen, nst);
+      }
     }
   }
 }
