@@ -74,6 +74,7 @@ struct BgmvArgs {
   MetaView mv;
   int list;      // int offset of the unit-record list inside the work lists
   int by_slot;   // shrink: grid rows are slots 1..S-1 (A prefetched before the wait)
+  int small_only;  // by_slot on the short-segment list: skip slots whose segment is long
   int pre;       // expand: runs right behind this library's shrink / reduce
   const int32_t *slot_rank;
   const float *slot_scale;
@@ -400,7 +401,7 @@ __global__ void __launch_bounds__(kSThreads, kSMinBlocks) bgmv_shrink_kernel(Bgm
     const int4 *rec = reinterpret_cast<const int4 *>(a.mv.work + WorkLists::by_slot(a.mv.num_slots) +
                                                      u.slot * WorkLists::kRec);
     const int4 h = rec[0], r = rec[1];
-    if (h.y < 0) {  // the slot has no tokens in this batch
+    if (h.y < 0 || (a.small_only && h.z >= LORA_SGMV_MIN_ROWS)) {  // no tokens here (or another family's)
       cp_async_wait_upto(0);
       return;
     }
@@ -616,9 +617,14 @@ Geo make_geo(const lora_layer_desc &d) {
 void fill_common(BgmvArgs &a, const lora_layer_desc &d, const MetaView &mv, ListSel sel) {
   a.list = WorkLists::list(mv.num_slots, sel);
   // Slot-indexed shrink CTAs (A prefetched before the metadata is known) when
-  // most slots are likely live: a whole batch of at least one token per slot.
-  // A sub-list (AUTO's short segments) may hold few of them.
-  a.by_slot = sel == kListAll && mv.num_tokens >= mv.num_slots - 1 ? 1 : 0;
+  // most slots are likely live in the list: a whole batch of at least one
+  // token per slot, or AUTO's short segments when the batch averages fewer
+  // than LORA_SGMV_MIN_ROWS tokens per slot (most slots are then short).
+  const int S1 = mv.num_slots - 1;
+  a.by_slot = (sel == kListAll && mv.num_tokens >= S1) ||
+                      (sel == kListSmall && mv.num_tokens >= S1 && mv.num_tokens <= LORA_SGMV_MIN_ROWS * S1)
+                  ? 1 : 0;
+  a.small_only = sel == kListSmall ? 1 : 0;
   a.n_slices = d.n_slices;
   a.max_items = std::min(mv.num_slots - 1, mv.num_tokens);
   a.mv = mv;
