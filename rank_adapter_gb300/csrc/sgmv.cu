@@ -133,19 +133,68 @@ __device__ __forceinline__ void tmem_alloc(uint32_t *slot, uint32_t ncols) {
 __device__ __forceinline__ void tmem_free(uint32_t taddr, uint32_t ncols) {
   asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
-// D[tmem] (+)= A[smem] * B[smem], bf16 operands, fp32 accumulator.
-__device__ __forceinline__ void mma_bf16(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
+// MMAs are issued by one elected lane of a converged warp, the way the
+// instruction wants its operands (warp-uniform values). A whole 64-deep K
+// block (four 16-deep steps) goes out from one asm block: its descriptors are
+// formed once and advanced in place, A by a_step and B by b_step (16-byte
+// units), so no other instruction sits between the MMAs and the tensor pipe
+// stays fed. Timed on this part: back-to-back issue like this keeps an
+// M=128 MMA at its pipe rate; with the descriptors rebuilt between MMAs by a
+// single divergent lane, issue alone took several times the MMA itself.
+// The first MMA accumulates when `acc` is non-zero; the others always do.
+// Every lane of the warp must call these.
+template <int kSteps>
+__device__ __forceinline__ void mma_run(uint32_t d, uint64_t ad, uint64_t bd, uint64_t a_step, uint64_t b_step,
+                                        uint32_t idesc, uint32_t acc) {
+  static_assert(kSteps == 1 || kSteps == 2 || kSteps == 4, "1, 2 or 4 steps");
+  if constexpr (kSteps == 1) {
+    asm volatile(
+        "{\n\t.reg .pred q, e;\n\t.reg .b32 r;\n\t"
+        "elect.sync r|e, 0xffffffff;\n\tsetp.ne.b32 q, %4, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, q;\n\t}"
+        ::"r"(d), "l"(ad), "l"(bd), "r"(idesc), "r"(acc), "l"(a_step), "l"(b_step)
+        : "memory");
+  } else if constexpr (kSteps == 2) {
+    asm volatile(
+        "{\n\t.reg .pred q, e, t;\n\t.reg .b32 r;\n\t.reg .b64 a1, b1;\n\t"
+        "elect.sync r|e, 0xffffffff;\n\tsetp.ne.b32 q, %4, 0;\n\tsetp.eq.b32 t, %3, %3;\n\t"
+        "add.s64 a1, %1, %5;\n\tadd.s64 b1, %2, %6;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, q;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, t;\n\t}"
+        ::"r"(d), "l"(ad), "l"(bd), "r"(idesc), "r"(acc), "l"(a_step), "l"(b_step)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred q, e, t;\n\t.reg .b32 r;\n\t.reg .b64 a1, a2, a3, b1, b2, b3;\n\t"
+        "elect.sync r|e, 0xffffffff;\n\tsetp.ne.b32 q, %4, 0;\n\tsetp.eq.b32 t, %3, %3;\n\t"
+        "add.s64 a1, %1, %5;\n\tadd.s64 a2, a1, %5;\n\tadd.s64 a3, a2, %5;\n\t"
+        "add.s64 b1, %2, %6;\n\tadd.s64 b2, b1, %6;\n\tadd.s64 b3, b2, %6;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, q;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, t;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a2, b2, %3, t;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a3, b3, %3, t;\n\t}"
+        ::"r"(d), "l"(ad), "l"(bd), "r"(idesc), "r"(acc), "l"(a_step), "l"(b_step)
+        : "memory");
+  }
+}
+// 1, 2 or 4 steps chosen at run time (a warp-uniform value).
+__device__ __forceinline__ void mma_steps(int steps, uint32_t d, uint64_t ad, uint64_t bd, uint64_t a_step,
+                                          uint64_t b_step, uint32_t idesc, uint32_t acc) {
+  if (steps >= 4) mma_run<4>(d, ad, bd, a_step, b_step, idesc, acc);
+  else if (steps == 2) mma_run<2>(d, ad, bd, a_step, b_step, idesc, acc);
+  else mma_run<1>(d, ad, bd, a_step, b_step, idesc, acc);
+}
+// D[tmem] (+)= A[smem] * B[smem] with bf16 operands and an fp32 accumulator
+// is what each MMA computes. tcgen05.commit, below, gives the barrier one
+// arrival once every MMA the committing lane issued so far is complete; it is
+// sent from the elected lane, the one that issued the MMAs.
+__device__ __forceinline__ void mma_commit_elect(uint64_t *bar) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-      ::"r"(d), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc)
-      : "memory");
+      "{\n\t.reg .pred e;\n\t.reg .b32 r;\n\telect.sync r|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}"
+      ::"r"(smem_addr(bar)) : "memory");
 }
-// The barrier receives one arrival once every MMA this thread issued so far is complete.
-__device__ __forceinline__ void mma_commit(uint64_t *bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
-               ::"r"(smem_addr(bar)) : "memory");
-}
+
 // 16 consecutive fp32 accumulator columns of this thread's TMEM lane.
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
   uint32_t r[16];
@@ -421,10 +470,16 @@ __global__ void __launch_bounds__(kShrinkThreads, 1)
       mbar_arrive(&acce[acc]);
       ++nitem;
     }
-  } else if (lane == 0) {
-    // ---- MMA issuer
-    const uint32_t idesc = idesc_bf16(kTileM, a.r_max);
+  } else {
+    // ---- MMA issuer: the whole warp walks the pipeline, one elected lane issues.
+    // The slices' A blocks sit side by side at one stride, so up to 256 columns
+    // (gsl slices) go into one MMA.
+    const int gsl = min(a.n_slices, max(1, 256 / a.r_max));
+    const int n_groups = (a.n_slices + gsl - 1) / gsl;
     const uint32_t sbo_w = 8u * a.box_n * 2, lbo_w = (uint32_t)kKB * a.box_n * 2;
+    const uint64_t b_step = (2u * sbo_w) >> 4;  // 16 K rows of the MN-major block
+    const uint32_t id_full = idesc_bf16(kTileM, gsl * a.r_max);
+    const uint32_t id_last = idesc_bf16(kTileM, (a.n_slices - (n_groups - 1) * gsl) * a.r_max);
     int consumed = 0, nitem = 0;
     bool ok = true;
     for (int p = 0; p < n_pieces && ok; ++p) {
@@ -432,35 +487,32 @@ __global__ void __launch_bounds__(kShrinkThreads, 1)
       const int kb0 = (int)(max(u0, (int64_t)tile * a.nb) - (int64_t)tile * a.nb);
       const int kb1 = (int)(min(u1, (int64_t)(tile + 1) * a.nb) - (int64_t)tile * a.nb);
       const int acc = nitem % a.n_acc;
-      if (!mbar_wait(&acce[acc], ((nitem / a.n_acc) & 1) ^ 1, a.err, kErrShrink)) break;
+      if (!mbar_wait_warp(&acce[acc], ((nitem / a.n_acc) & 1) ^ 1, a.err, kErrShrink)) break;
       tc_after_sync();
       const uint32_t d0 = tmem + (uint32_t)(acc * a.acc_cols);
       for (int kb = kb0; kb < kb1; ++kb) {
         const int s = consumed % a.stages;
-        if (!mbar_wait(&full[s], (consumed / a.stages) & 1, a.err, kErrShrink)) {
+        if (!mbar_wait_warp(&full[s], (consumed / a.stages) & 1, a.err, kErrShrink)) {
           ok = false;
           break;
         }
         tc_after_sync();
         const uint32_t xs = smem_addr(sm + s * a.stage_bytes);
-#pragma unroll
-        for (int kk = 0; kk < kKB / 16; ++kk) {
-          const uint64_t ad = smem_desc(xs + kk * 32, 16, 1024, kSw128);
-          for (int sl = 0; sl < a.n_slices; ++sl) {
-            const uint64_t bd = smem_desc(xs + kTileM * 128 + sl * a.w_bytes + kk * 2 * sbo_w, lbo_w, sbo_w,
-                                          a.w_layout);
-            mma_bf16(d0 + (uint32_t)(sl * a.r_max), ad, bd, idesc, (kb > kb0 || kk > 0) ? 1u : 0u);
-          }
+        const uint64_t ad = smem_desc(xs, 16, 1024, kSw128);
+        for (int g = 0; g < n_groups; ++g) {
+          const uint64_t bd = smem_desc(xs + kTileM * 128 + g * gsl * a.w_bytes, lbo_w, sbo_w, a.w_layout);
+          mma_run<kKB / 16>(d0 + (uint32_t)(g * gsl * a.r_max), ad, bd, 2, b_step, g + 1 < n_groups ? id_full : id_last,
+                            kb > kb0 ? 1u : 0u);
         }
-        mma_commit(&empty[s]);
+        mma_commit_elect(&empty[s]);
         ++consumed;
       }
       if (!ok) break;
-      mma_commit(&accf[acc]);
+      mma_commit_elect(&accf[acc]);
       ++nitem;
     }
-    mma_commit(fin);
-    mbar_wait(fin, 0, a.err, kErrShrink);  // every MMA is done before TMEM is freed
+    mma_commit_elect(fin);
+    mbar_wait_warp(fin, 0, a.err, kErrShrink);  // every MMA is done before TMEM is freed
   }
   tc_before_sync();
   __syncthreads();
@@ -587,10 +639,16 @@ struct SgExpandArgs {
 
 struct SgExpandMaps {
   CUtensorMap b[LORA_MAX_SLICES];  // B[s] as {out_s, r_max, slots}, boxes of 64 columns x r_max rows
-  CUtensorMap y;                   // y as {sum(out_sizes), T}, boxes of 128 bytes x 128 rows
+  CUtensorMap y;                   // y as {sum(out_sizes), T}, boxes of 128 bytes x 128 rows (loads)
+  CUtensorMap ys;                  // the same y, boxes of 128 bytes x 32 rows (an epilogue warp's store)
 };
 
 constexpr int kEpiWarps = 8;  // epilogue warps, a multiple of 4 (one group per TMEM lane quadrant); 8 measured best
+// Accumulators in the expand's ring: the MMA warp runs up to kExpandAcc - 1
+// items ahead of the epilogue, so neither waits on the other's latency (with
+// two, an item took the MMA time plus the epilogue's hand-off). 4 x 128
+// columns fill the 512 TMEM columns for a bf16 y.
+constexpr int kExpandAcc = 4;
 constexpr int kExpandThreads = 32 * (kEpiWarps + 6);  // + loaders (u rows, gathered y rows) x4, producer, MMA
 constexpr int kYHalf = kTileM * 128;  // one half (128 bytes per row) of a staged y tile
 constexpr int kYStage = 2 * kYHalf;   // a staged y tile: 128 rows x 256 bytes
@@ -637,6 +695,29 @@ struct TileRows {
   }
 };
 
+// One elected lane stores a box of the staged tile with a TMA tile copy and
+// closes it as a bulk group; the same lane later waits for the group's
+// shared-memory reads (the slot may then be refilled) or for its completion.
+__device__ __forceinline__ void tma_store_2d_elect(const CUtensorMap *map, const void *src, int c0, int c1) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t.reg .b32 r;\n\telect.sync r|e, 0xffffffff;\n\t"
+      "@e cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];\n\t"
+      "@e cp.async.bulk.commit_group;\n\t}"
+      ::"l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(src)), "r"(c0), "r"(c1)
+      : "memory");
+}
+template <int kPending>
+__device__ __forceinline__ void bulk_wait_read_elect() {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t.reg .b32 r;\n\telect.sync r|e, 0xffffffff;\n\t"
+      "@e cp.async.bulk.wait_group.read %0;\n\t}" ::"n"(kPending) : "memory");
+}
+__device__ __forceinline__ void bulk_wait_all_elect() {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t.reg .b32 r;\n\telect.sync r|e, 0xffffffff;\n\t"
+      "@e cp.async.bulk.wait_group 0;\n\t}" ::: "memory");
+}
+
 // The barrier receives this thread's arrival once its earlier cp.async copies are complete.
 __device__ __forceinline__ void cp_async_arrive(uint64_t *bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
@@ -664,8 +745,8 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
   uint64_t *yfull = bempty + a.b_stages;
   uint64_t *yempty = yfull + a.y_stages;
   uint64_t *accf = yempty + a.y_stages;
-  uint64_t *acce = accf + 2;
-  uint64_t *ufull = acce + 2;
+  uint64_t *acce = accf + kExpandAcc;
+  uint64_t *ufull = acce + kExpandAcc;
   uint64_t *uempty = ufull + 1;
   uint64_t *fin = uempty + 1;
   uint32_t *tslot = reinterpret_cast<uint32_t *>(fin + 1);
@@ -679,7 +760,7 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
       mbar_init(&yfull[s], 1 + 128);  // the producer + every loader thread
       mbar_init(&yempty[s], 32 * kEpiWarps);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kExpandAcc; ++i) {
       mbar_init(&accf[i], 1);
       mbar_init(&acce[i], 32 * kEpiWarps);
     }
@@ -690,7 +771,8 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
   }
   pdl_wait();
   pdl_trigger();
-  constexpr uint32_t kTmemCols = 2 * kN;
+  constexpr uint32_t kTmemCols = kExpandAcc * kN;
+  static_assert(kTmemCols <= 512, "accumulators exceed tensor memory");
   if (warp == kEpiWarps + 5) tmem_alloc(tslot, kTmemCols);
   tc_before_sync();
   __syncthreads();
@@ -711,6 +793,9 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
     const int row = q * 32 + lane;
     const int g0 = part * kPartChunks;  // first 16-byte chunk of this part
     int cur_tile = -1, tok = -1, nitem = 0;
+    int tok0 = 0;                 // first token of the tile when its rows are one run of tokens
+    bool whole_rows = false;      // ... and this warp's 32 rows are all tokens of it
+    int pend = -1;                // ring slot whose bulk store may still be reading it
     int stok[kStoreInsts];
 #pragma unroll
     for (int i = 0; i < kStoreInsts; ++i) stok[i] = -1;
@@ -724,11 +809,13 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
           const int r = 32 * q + kRowsPerInst * i + lane / kPartChunks;
           stok[i] = r < ti.rows ? a.sorted_rows[ti.pos0 + r] : -1;
         }
+        tok0 = a.sorted_rows[ti.pos0];
+        whole_rows = 32 * q + 32 <= ti.rows && a.sorted_rows[ti.pos0 + ti.rows - 1] - tok0 == ti.rows - 1;
         cur_tile = e.tile;
       }
-      const int acc = nitem & 1, ys = nitem % a.y_stages;
+      const int acc = nitem % kExpandAcc, ys = nitem % a.y_stages;
       const uint32_t par = (nitem / a.y_stages) & 1;
-      if (!mbar_wait_warp(&accf[acc], (nitem >> 1) & 1, a.err, kErrExpand)) break;
+      if (!mbar_wait_warp(&accf[acc], (nitem / kExpandAcc) & 1, a.err, kErrExpand)) break;
       tc_after_sync();
       float v[kPartCols];
       const uint32_t t0 = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kN + part * kPartCols);
@@ -771,23 +858,51 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
 #pragma unroll
         for (int g = 0; g < kPartChunks; ++g) *reinterpret_cast<uint4 *>(st + ychunk(row, g0 + g)) = w[g];
       }
-      __syncwarp();
-      // Store this warp's part of its 32 rows: lanes along the row,
-      // kRowsPerInst rows per instruction. Columns past the slice stay unstored.
-      const int gl = lane % kPartChunks;
-      if ((g0 + gl) * kVec < e.ncols) {
-        TY *ybase = y + a.out_off[e.slice] + e.n0 + (g0 + gl) * kVec;
-        uint4 w[kStoreInsts];
+      // Store this warp's part of its 32 rows. When the rows are 32
+      // consecutive tokens and the part lies inside the slice, one bulk tile
+      // store sends it straight from the staged (swizzled) tile; otherwise
+      // lanes along the row, kRowsPerInst rows per instruction, and columns
+      // past the slice stay unstored.
+      const bool bulk = whole_rows && part * kPartCols + kPartCols <= e.ncols;
+      if (bulk) {
+        fence_async_smem();  // this lane's staged writes, before the copy reads them
+        __syncwarp();
+        tma_store_2d_elect(&maps.ys, st + part * kYHalf + q * 32 * 128, a.out_off[e.slice] + e.n0 + part * kPartCols,
+                           tok0 + 32 * q);
+      } else {
+        __syncwarp();
+        const int gl = lane % kPartChunks;
+        if ((g0 + gl) * kVec < e.ncols) {
+          TY *ybase = y + a.out_off[e.slice] + e.n0 + (g0 + gl) * kVec;
+          uint4 w[kStoreInsts];
 #pragma unroll
-        for (int i = 0; i < kStoreInsts; ++i)
-          w[i] = *reinterpret_cast<const uint4 *>(st + ychunk(32 * q + kRowsPerInst * i + lane / kPartChunks, g0 + gl));
+          for (int i = 0; i < kStoreInsts; ++i)
+            w[i] = *reinterpret_cast<const uint4 *>(st + ychunk(32 * q + kRowsPerInst * i + lane / kPartChunks, g0 + gl));
 #pragma unroll
-        for (int i = 0; i < kStoreInsts; ++i)
-          if (stok[i] >= 0) *reinterpret_cast<uint4 *>(ybase + (int64_t)stok[i] * a.ldy) = w[i];
+          for (int i = 0; i < kStoreInsts; ++i)
+            if (stok[i] >= 0) *reinterpret_cast<uint4 *>(ybase + (int64_t)stok[i] * a.ldy) = w[i];
+        }
       }
-      mbar_arrive(&yempty[ys]);
+      // A slot goes back to the loaders once nothing reads it: at once after
+      // lane stores, one item later after a bulk store (its reads are done
+      // when at most the newest group is still pending).
+      if (pend >= 0) {
+        if (bulk) bulk_wait_read_elect<1>();
+        else bulk_wait_read_elect<0>();
+        __syncwarp();
+        mbar_arrive(&yempty[pend]);
+        pend = -1;
+      }
+      if (bulk) pend = ys;
+      else mbar_arrive(&yempty[ys]);
       ++nitem;
     }
+    if (pend >= 0) {
+      bulk_wait_read_elect<0>();
+      __syncwarp();
+      mbar_arrive(&yempty[pend]);
+    }
+    bulk_wait_all_elect();  // every bulk store has landed before the CTA exits
   } else if (warp < kEpiWarps + 4) {
     // ---- loaders: the u rows of each (tile, slice) (thread = row), and the
     // y rows of tiles that are not one run of tokens (16-byte cp.async,
@@ -888,43 +1003,43 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
       }
       ++nitem;
     }
-  } else if (lane == 0) {
-    // ---- MMA issuer: acc = u_hi B + u_lo B, K = r_max each
+  } else if (warp == kEpiWarps + 5) {
+    // ---- MMA issuer: acc = u_hi B + u_lo B, K = r_max each. The whole warp
+    // walks the items, one elected lane issues (a 64-deep K block per run).
     const uint32_t idesc = idesc_bf16(kTileM, kN);
     const uint32_t uhi = smem_addr(sU), ulo = uhi + (uint32_t)(a.nk * kUKRegion);
     const uint32_t lbo_b = (uint32_t)r_max * 128;
-    const int ksteps = r_max / 16;
+    const int steps = min(r_max, 64) / 16;  // 16-deep K steps per 64-deep block (r_max 16, 32: 1, 2)
     int cur_group = -1, g = 0, nitem = 0;
     for (int64_t it = it0; it < it1; ++it) {
       const ExpandItem e = expand_item(a, it, nbt, kN, n_slices);
       if (e.group != cur_group) {
-        if (cur_group >= 0) mma_commit(uempty);  // the previous u rows are free once its MMAs finish
-        if (!mbar_wait(ufull, g & 1, a.err, kErrExpand)) break;
+        if (cur_group >= 0) mma_commit_elect(uempty);  // the previous u rows are free once its MMAs finish
+        if (!mbar_wait_warp(ufull, g & 1, a.err, kErrExpand)) break;
         ++g;
         cur_group = e.group;
       }
-      const int acc = nitem & 1, bs = nitem % a.b_stages;
-      if (!mbar_wait(&acce[acc], ((nitem >> 1) & 1) ^ 1, a.err, kErrExpand)) break;
-      if (!mbar_wait(&bfull[bs], (nitem / a.b_stages) & 1, a.err, kErrExpand)) break;
+      const int acc = nitem % kExpandAcc, bs = nitem % a.b_stages;
+      if (!mbar_wait_warp(&acce[acc], ((nitem / kExpandAcc) & 1) ^ 1, a.err, kErrExpand)) break;
+      if (!mbar_wait_warp(&bfull[bs], (nitem / a.b_stages) & 1, a.err, kErrExpand)) break;
       tc_after_sync();
       const uint32_t d = tmem + (uint32_t)(acc * kN);
       const uint32_t bb = smem_addr(sB + bs * a.b_bytes);
-      for (int kk = 0; kk < ksteps; ++kk) {
-        const uint32_t ka = (uint32_t)((kk * 16) / 64 * kUKRegion + ((kk * 16) % 64) * 2);
-        const uint64_t bd = smem_desc(bb + kk * 2048, lbo_b, 1024, kSw128);
-        mma_bf16(d, smem_desc(uhi + ka, 16, 1024, kSw128), bd, idesc, kk > 0 ? 1u : 0u);
+      // K block c covers u columns [64c, 64c + 64): its own u region, B rows 64c on.
+      for (int c = 0; c < a.nk; ++c) {
+        const uint64_t bd = smem_desc(bb + c * 4 * 2048, lbo_b, 1024, kSw128);
+        mma_steps(steps, d, smem_desc(uhi + c * kUKRegion, 16, 1024, kSw128), bd, 2, 128, idesc, c > 0 ? 1u : 0u);
       }
-      for (int kk = 0; kk < ksteps; ++kk) {
-        const uint32_t ka = (uint32_t)((kk * 16) / 64 * kUKRegion + ((kk * 16) % 64) * 2);
-        const uint64_t bd = smem_desc(bb + kk * 2048, lbo_b, 1024, kSw128);
-        mma_bf16(d, smem_desc(ulo + ka, 16, 1024, kSw128), bd, idesc, 1u);
+      for (int c = 0; c < a.nk; ++c) {
+        const uint64_t bd = smem_desc(bb + c * 4 * 2048, lbo_b, 1024, kSw128);
+        mma_steps(steps, d, smem_desc(ulo + c * kUKRegion, 16, 1024, kSw128), bd, 2, 128, idesc, 1u);
       }
-      mma_commit(&bempty[bs]);
-      mma_commit(&accf[acc]);
+      mma_commit_elect(&bempty[bs]);
+      mma_commit_elect(&accf[acc]);
       ++nitem;
     }
-    mma_commit(fin);
-    mbar_wait(fin, 0, a.err, kErrExpand);  // every MMA is done before TMEM is freed
+    mma_commit_elect(fin);
+    mbar_wait_warp(fin, 0, a.err, kErrExpand);  // every MMA is done before TMEM is freed
   }
   tc_before_sync();
   __syncthreads();
@@ -979,16 +1094,16 @@ cudaError_t make_map(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1,
 }
 
 // 2-D tensor map of a row-major matrix {cols (contiguous), rows} with row
-// stride `ld` elements, boxes of box_cols columns (128 bytes) x 128 rows in the
-// 128-byte swizzle.
+// stride `ld` elements, boxes of box_cols columns (128 bytes) x box_rows rows
+// in the 128-byte swizzle.
 cudaError_t make_rows_map(CUtensorMap *m, const void *base, bool bf16, uint64_t cols, uint64_t rows, int64_t ld,
-                          uint32_t box_cols) {
+                          uint32_t box_cols, uint32_t box_rows = kTileM) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
   if (enc == nullptr) return cudaErrorNotSupported;
   const uint64_t es = bf16 ? 2 : 4;
   const cuuint64_t dims[2] = {cols, rows};
   const cuuint64_t strides[1] = {(cuuint64_t)ld * es};
-  const cuuint32_t box[2] = {box_cols, (cuuint32_t)kTileM};
+  const cuuint32_t box[2] = {box_cols, box_rows};
   const cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
                    const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -1120,6 +1235,9 @@ cudaError_t launch_sgmv_expand(const lora_layer_desc &d, const MetaView &mv, Lis
   }
   cudaError_t em = make_rows_map(&maps.y, y, y_dtype == LORA_BF16, (uint64_t)width, (uint64_t)mv.num_tokens, ldy,
                                  y_dtype == LORA_BF16 ? 64u : 32u);
+  if (em != cudaSuccess) return em;
+  em = make_rows_map(&maps.ys, y, y_dtype == LORA_BF16, (uint64_t)width, (uint64_t)mv.num_tokens, ldy,
+                     y_dtype == LORA_BF16 ? 64u : 32u, 32u);
   if (em != cudaSuccess) return em;
   SgExpandArgs a{};
   a.u.src = u_src;
