@@ -50,6 +50,8 @@ WORKLOADS = {
     "toy_fp32": "toy fp32: d=256, r=16, 8 slots, 6 requests (53 tokens)",
     "full_decode": "full-model decode step: 32 layers x {qkv, o, gate_up, down}, r=16, 100 resident adapters "
                    "(~84 MB each), 512 tokens uniform over them; one metadata pass, 128 lora_apply calls",
+    "logits_lm_head": "lm_head LoRA on sampled rows: hidden 4096 -> vocab 128256, r=16, 64 slots, "
+                      "256 sampled rows (one per request, 10% slot 0)",
 }
 
 
@@ -106,7 +108,7 @@ def algorithmic(inst, y_bytes_per_elem=2):
 
 def make_workload(name, seed_offset=0):
     import workloads as wl
-    base = {"toy_fp32": 0, "decode_qkv": 2, "prefill_gate_up": 3, "mixed_o_proj": 4}[name]
+    base = {"toy_fp32": 0, "decode_qkv": 2, "prefill_gate_up": 3, "mixed_o_proj": 4, "logits_lm_head": 6}[name]
     return wl.make_instance(name, seed=base + 1000 * seed_offset if seed_offset else None)
 
 

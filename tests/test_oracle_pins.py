@@ -364,3 +364,31 @@ def test_bf16_encoding_matches_torch():
     assert np.array_equal(ours, theirs)
     assert np.array_equal(wl.bf16_bits_to_f32(ours),
                           torch.from_numpy(v).to(torch.bfloat16).float().numpy())
+
+
+def test_sampled_rows_mapping_and_restriction():
+    """The lm_head LoRA's sampled rows are the last token of every request
+    (page "vLLM 源码完全拆解(十八): 多 LoRA 服务", section "lm_head / logits"), and
+    the oracle's delta on those rows alone equals its delta for the whole batch
+    restricted to them (each row's delta uses only its row and slot), to fp64
+    rounding: the matrix products may sum in another order for another row count."""
+    assert wl.sampled_rows([1, 1, 1]).tolist() == [0, 1, 2]
+    assert wl.sampled_rows([3, 1, 5, 2]).tolist() == [2, 3, 8, 10]
+    with pytest.raises(ValueError):
+        wl.sampled_rows([2, 0])
+    lengths = [5, 1, 3, 1, 7]
+    inst = wl.make_instance("logits_lm_head", req_lengths=lengths, out_sizes=[96], num_slots=4, d_in=64,
+                            dtype="f32")
+    ads = lo.adapters_f64(inst)
+    x = inst.to_f32(inst.x).astype(np.float64)
+    y_in = inst.to_f32(inst.y_in).astype(np.float64)
+    y_all = lo.apply_requests(x, y_in, ads, inst.out_sizes, inst.r_max, inst.req_lengths, inst.req_slots,
+                              inst.num_slots)
+    rows = wl.sampled_rows(inst.req_lengths)
+    y_s = lo.apply_requests(x[rows], y_in[rows], ads, inst.out_sizes, inst.r_max, np.ones(len(rows), np.int64),
+                            inst.req_slots, inst.num_slots)
+    assert np.allclose(y_s, y_all[rows], rtol=0, atol=1e-12 * np.abs(y_all).max())
+    live = inst.req_slots != 0
+    assert live.any()
+    assert not np.array_equal(y_s[live], y_in[rows][live])
+

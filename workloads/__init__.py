@@ -20,6 +20,10 @@ Workloads (sizes follow the Llama-3-8B-shaped projections the pages use):
                     1024 decode tokens + 4 prefill chunks of 512, 5% slot 0.
 * ``full_decode``   one decode step over 32 layers x {qkv, o, gate_up, down},
                     r=16, 100 resident adapters, 512 tokens.
+* ``logits_lm_head`` the lm_head LoRA on the rows sampled this step (page
+                    "vLLM 源码完全拆解(十八): 多 LoRA 服务", section
+                    "lm_head / logits"): hidden 4096 -> vocab 128256, r=16,
+                    64 slots, 256 sampled rows (one per request), 10% slot 0.
 
 Slot 0 is the reserved "no LoRA" slot; adapters live in slots 1..num_slots-1.
 bf16 tensors are produced as uint16 bit patterns so that every consumer sees
@@ -35,10 +39,11 @@ import numpy as np
 __all__ = [
     "bf16_bits_from_f32", "bf16_bits_to_f32", "Adapter", "Instance",
     "make_instance", "toy_page_instance", "zipf_probs", "full_decode_groups",
-    "CONFIG_NAMES", "split_requests",
+    "CONFIG_NAMES", "EXTRA_NAMES", "split_requests", "sampled_rows",
 ]
 
 CONFIG_NAMES = ("toy_fp32", "decode_qkv", "prefill_gate_up", "mixed_o_proj", "full_decode")
+EXTRA_NAMES = ("logits_lm_head",)   # widening beyond the five configurations
 
 _CHUNK = 1 << 24
 
@@ -193,7 +198,7 @@ def make_instance(name: str, seed: Optional[int] = None, *, num_tokens: Optional
     Config i uses seed i (``toy_fp32`` seed 0) unless ``seed`` is given.
     """
     default_seed = {"toy_fp32": 0, "decode_qkv": 2, "prefill_gate_up": 3,
-                    "mixed_o_proj": 4, "full_decode": 5}
+                    "mixed_o_proj": 4, "full_decode": 5, "logits_lm_head": 6}
     if name not in default_seed:
         raise ValueError(f"unknown workload {name!r}")
     rng = np.random.Generator(np.random.PCG64(default_seed[name] if seed is None else seed))
@@ -264,6 +269,22 @@ def make_instance(name: str, seed: Optional[int] = None, *, num_tokens: Optional
         scales = {k: 2.0 * ranks[k] / ranks[k] for k in range(1, S)}   # alpha/r with alpha = 2r
         adapters = _draw_adapters(rng, range(1, S), D, outs, ranks, scales, 64.0, 16.0, dt)
         x_inv, a_note = 1.0, "A~N/64, B~N/16"
+    elif name == "logits_lm_head":
+        # The sampled rows' hidden states and logits: one row per request (the
+        # last token of a prefill request, the token of a decode request).
+        dt = dtype or "bf16"
+        D = d_in or 4096
+        outs = list(out_sizes or [128256])
+        S = num_slots or 64
+        R = r_max or 16
+        n = num_tokens or 256
+        lengths = np.asarray(req_lengths if req_lengths is not None else np.ones(n), np.int64)
+        none = rng.random(len(lengths)) < 0.10
+        slots = np.where(none, 0, rng.integers(1, S, size=len(lengths))).astype(np.int32)
+        ranks = {k: R for k in range(1, S)}
+        scales = {k: 1.0 for k in range(1, S)}
+        adapters = _draw_adapters(rng, range(1, S), D, outs, ranks, scales, 64.0, 16.0, dt)
+        x_inv, a_note = 1.0, "A~N/64, B~N/16"
     else:  # full_decode: one (layer, group); see full_decode_groups for the whole step
         raise ValueError("full_decode is built per (layer, group) by full_decode_groups()")
 
@@ -312,6 +333,16 @@ def full_decode_groups(seed: int = 5, *, layers: int = 32, num_tokens: int = 512
                            out_sizes=list(outs), num_slots=S, r_max=rank, adapters=adapters,
                            req_lengths=lengths, req_slots=slots, x=x, y_in=y_in,
                            meta={"seed": seed, "layer": layer, "group": gname})
+
+
+def sampled_rows(req_lengths) -> np.ndarray:
+    """Batch indices of the rows sampled this step: the last token of every
+    request (for a one-token decode request, its only token), in request order.
+    The lm_head LoRA runs on these rows only, each with its request's slot."""
+    lengths = np.asarray(req_lengths, np.int64)
+    if (lengths < 1).any():
+        raise ValueError("every request has at least one token")
+    return (np.cumsum(lengths) - 1).astype(np.int64)
 
 
 def split_requests(req_lengths: np.ndarray, world_size: int, rank: int) -> np.ndarray:
