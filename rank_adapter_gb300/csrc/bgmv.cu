@@ -39,7 +39,12 @@ constexpr int kSMinBlocks = 5;
 constexpr int kTT = 4;               // tokens per tile
 constexpr int kAStageBytes = 16384;  // A bytes per stretch
 constexpr int kStretches = 2;        // stretches per shrink CTA (all in flight at once)
-constexpr int kBPassBytes = 32768;   // B bytes per expand CTA
+constexpr int kBPassBytes = 32768;   // B bytes per expand CTA (twice that for deep grids, see kWideGrid)
+// An expand grid of more CTAs than this at kBPassBytes (about 4.5 waves of
+// three CTAs per SM on 152 SMs) takes CTAs of twice the columns: for a
+// vocabulary-wide output that measured 110 -> 92 us, while shallow decode
+// grids are faster with the narrower CTAs (fewer CTAs would leave SMs idle).
+constexpr int kWideGrid = 2048;
 constexpr int kSmallTable = 256;     // slot tables up to this size: rank / scale copied whole
 constexpr int kRowsWin = 32;         // token rows of a unit kept in shared memory (a sliding window)
 constexpr int kKCReg = 16;           // expand: chunk partials of the next tile held in registers
@@ -573,7 +578,7 @@ __global__ void __launch_bounds__(kThreads, 3) bgmv_expand_kernel(BgmvArgs a) {
 int align16(int v) { return (v + 15) & ~15; }
 
 // Geometry of the shrink and expand CTAs for a layer.
-Geo make_geo(const lora_layer_desc &d) {
+Geo make_geo(const lora_layer_desc &d, bool wide = false) {
   Geo g{};
   const int es = d.dtype == LORA_BF16 ? 2 : 4;
   g.d_in = d.d_in;
@@ -585,7 +590,7 @@ Geo make_geo(const lora_layer_desc &d) {
   g.sc = sc;
   g.kchunk = kStretches * sc;
   g.kc_count = (d.d_in + g.kchunk - 1) / g.kchunk;
-  int pw = (kBPassBytes / row_bytes) & ~7;
+  int pw = ((wide ? 2 * kBPassBytes : kBPassBytes) / row_bytes) & ~7;
   if (pw < 8) pw = 8;
   int max_out = 0;
   for (int s = 0; s < d.n_slices; ++s) max_out = d.out_sizes[s] > max_out ? d.out_sizes[s] : max_out;
@@ -642,13 +647,16 @@ void fill_common(BgmvArgs &a, const lora_layer_desc &d, const MetaView &mv, List
       std::swap(a.slice_order[j], a.slice_order[j - 1]);
   a.slot_rank = d.slot_rank;
   a.slot_scale = d.slot_scale;
-  a.g = make_geo(d);
-  int chunks = 0;
-  for (int s = 0; s < d.n_slices; ++s) {
-    a.chunk_start[s] = chunks;
-    chunks += (d.out_sizes[s] + a.g.pw - 1) / a.g.pw;
+  for (int wide = 0; wide < 2; ++wide) {
+    a.g = make_geo(d, wide != 0);
+    int chunks = 0;
+    for (int s = 0; s < d.n_slices; ++s) {
+      a.chunk_start[s] = chunks;
+      chunks += (d.out_sizes[s] + a.g.pw - 1) / a.g.pw;
+    }
+    a.chunk_start[d.n_slices] = chunks;
+    if ((int64_t)chunks * a.max_items <= kWideGrid) break;  // a shallow expand grid keeps the narrow CTAs
   }
-  a.chunk_start[d.n_slices] = chunks;
 }
 
 template <typename TW, int NV>
