@@ -182,6 +182,8 @@ int lora_prepare_meta(const lora_meta *meta, lora_stream_t stream);
  * (lora_shrink / add_shrink of the vLLM page, section "shrink 核"; the scale
  * enters here as in section "PEFTHelper:认清 adapter 文件").
  *   x:   device, [num_tokens, d_in] with row stride ldx elements, desc->dtype
+ *        (a row-parallel shard's d_in columns of a wider x: x advanced by the
+ *        shard's first column, ldx the full width)
  *   buf: device fp32, [n_slices, num_tokens, r_max] contiguous; rows of
  *        slot-0 tokens are not written
  *   ws:  device scratch of at least lora_workspace_bytes(desc, num_tokens,
@@ -211,6 +213,10 @@ int lora_shrink(const lora_layer_desc *desc, const lora_meta *meta, const void *
  *   y:   device, [num_tokens, sum(out_sizes)] with row stride ldy elements,
  *        y_dtype (LORA_BF16 production; LORA_F32 for accuracy runs; an fp32
  *        table requires LORA_F32)
+ * To add into a column range of a wider output -- the offset_start of the
+ * fully-sharded variant (section "S-LoRA 式:把秩也切开"), where a shard's B
+ * holds only its output columns -- pass y advanced by the range's first
+ * column and ldy the full row width (16-byte alignment still applies).
  */
 int lora_expand(const lora_layer_desc *desc, const lora_meta *meta, const float *buf, void *y,
                 int64_t ldy, int32_t y_dtype, int32_t kind, lora_stream_t stream);
