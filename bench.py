@@ -52,6 +52,8 @@ WORKLOADS = {
                    "(~84 MB each), 512 tokens uniform over them; one metadata pass, 128 lora_apply calls",
     "logits_lm_head": "lm_head LoRA on sampled rows: hidden 4096 -> vocab 128256, r=16, 64 slots, "
                       "256 sampled rows (one per request, 10% slot 0)",
+    "embed_lookup": "embedding LoRA: vocab 128256 -> hidden 4096, r=16, 64 slots, 256 decode tokens "
+                    "(ids uniform over the vocabulary, 10% slot 0); lookup + expand",
 }
 
 
@@ -97,18 +99,25 @@ def algorithmic(inst, y_bytes_per_elem=2):
     w_a = int(sum(es * ranks[a] * n_s * d_in for a in active))
     w_b = int(sum(es * ranks[a] * d_out for a in active))
     x_b = es * T_L * d_in
+    if inst.token_ids is not None:
+        # embedding: the lookup reads one r-vector per distinct (slot, token id) and the ids
+        pairs = {(int(a), int(v)) for a, v in zip(ts[live], inst.token_ids[live])}
+        w_a = int(sum(es * ranks[a] for a, _ in pairs))
+        x_b = 4 * len(ts)
     y_b = 2 * y_bytes_per_elem * T_L * d_out
     buf_b = 4 * n_s * T_L * inst.r_max
-    flops = int(sum(2 * ranks[a] * (n_s * d_in + d_out) * int((ts == a).sum()) for a in active))
+    shrink_d = 0 if inst.token_ids is not None else n_s * d_in   # a lookup does no products
+    flops = int(sum(2 * ranks[a] * (shrink_d + d_out) * int((ts == a).sum()) for a in active))
     return dict(T=int(len(ts)), T_L=T_L, active=int(len(active)), shrink_bytes=w_a + x_b + buf_b,
                 expand_bytes=w_b + buf_b + y_b, step_bytes=w_a + w_b + x_b + y_b, flops=flops,
-                shrink_flops=int(sum(2 * ranks[a] * n_s * d_in * int((ts == a).sum()) for a in active)),
+                shrink_flops=int(sum(2 * ranks[a] * shrink_d * int((ts == a).sum()) for a in active)),
                 expand_flops=int(sum(2 * ranks[a] * d_out * int((ts == a).sum()) for a in active)))
 
 
 def make_workload(name, seed_offset=0):
     import workloads as wl
-    base = {"toy_fp32": 0, "decode_qkv": 2, "prefill_gate_up": 3, "mixed_o_proj": 4, "logits_lm_head": 6}[name]
+    base = {"toy_fp32": 0, "decode_qkv": 2, "prefill_gate_up": 3, "mixed_o_proj": 4, "logits_lm_head": 6,
+            "embed_lookup": 7}[name]
     return wl.make_instance(name, seed=base + 1000 * seed_offset if seed_offset else None)
 
 
@@ -207,8 +216,13 @@ def cpu_child(args):
     reps, t0 = 0, time.perf_counter()
     while True:
         oracle.prepare_meta(inst.token_slot, inst.num_slots)
-        oracle.apply_requests(x, y, ads, inst.out_sizes, inst.r_max, inst.req_lengths, inst.req_slots,
-                              inst.num_slots)
+        if inst.token_ids is not None:   # embedding: lookup, then expand
+            buf, _ = oracle.embed_requests(inst.token_ids, ads, inst.r_max, inst.req_lengths, inst.req_slots,
+                                           inst.num_slots)
+            oracle.expand_requests(buf, y, ads, inst.out_sizes, inst.req_lengths, inst.req_slots, inst.num_slots)
+        else:
+            oracle.apply_requests(x, y, ads, inst.out_sizes, inst.r_max, inst.req_lengths, inst.req_slots,
+                                  inst.num_slots)
         reps += 1
         el = time.perf_counter() - t0
         if el >= args.cpu_seconds:
@@ -281,6 +295,7 @@ class Replica:
         self.ws_bytes = self.ws.numel() * 4 if self.ws is not None else 0
         self.kind = kind
         self.ydt = ra.LORA_BF16 if self.y.dtype == torch.bfloat16 else ra.LORA_F32
+        self.embed = inst.token_ids is not None   # x holds token ids: the shrink is the embedding lookup
 
     def bytes(self):
         return self.table.nbytes() + self.x.numel() * self.x.element_size() + \
@@ -295,10 +310,15 @@ class Replica:
         if only is not None:
             if only == "meta":
                 ra.check(ra.lora_prepare_meta(self.meta.c, st), "prepare_meta")
+            elif only == "apply" and self.embed:
+                self._embed_step(ra, st)
             elif only == "apply":
                 ra.check(ra.lora_apply(self.table.desc, self.meta.c, self.x.data_ptr(), self.x.stride(0), 0,
                                        self.y.data_ptr(), self.y.stride(0), self.ydt, self.kind, self.ws_ptr,
                                        self.ws_bytes, st), "apply")
+            elif only == "shrink" and self.embed:
+                ra.check(ra.lora_embed_shrink(self.table.desc, self.meta.c, self.x.data_ptr(), self.buf.data_ptr(),
+                                              st), "embed_shrink")
             elif only == "shrink":
                 ra.check(ra.lora_shrink(self.table.desc, self.meta.c, self.x.data_ptr(), self.x.stride(0),
                                         self.buf.data_ptr(), self.kind, self.ws_ptr, self.ws_bytes, st), "shrink")
@@ -311,6 +331,16 @@ class Replica:
         ra.check(ra.lora_prepare_meta(self.meta.c, st), "prepare_meta")
         if ev is not None:
             ev[1].record()
+        if self.embed:  # both paths: the lookup, then the expand
+            ra.check(ra.lora_embed_shrink(self.table.desc, self.meta.c, self.x.data_ptr(), self.buf.data_ptr(),
+                                          st), "embed_shrink")
+            if ev is not None:
+                ev[2].record()
+            ra.check(ra.lora_expand(self.table.desc, self.meta.c, self.buf.data_ptr(), self.y.data_ptr(),
+                                    self.y.stride(0), self.ydt, self.kind, st), "expand")
+            if ev is not None:
+                ev[len(ev) - 1].record()
+            return
         if path == "fused":
             # The fused step keeps the rank-r intermediate in the workspace; no buf output is asked for.
             ra.check(ra.lora_apply(self.table.desc, self.meta.c, self.x.data_ptr(), self.x.stride(0), 0,
@@ -327,6 +357,13 @@ class Replica:
                                 self.y.stride(0), self.ydt, self.kind, st), "expand")
         if ev is not None:
             ev[3].record()
+
+
+    def _embed_step(self, ra, st):
+        ra.check(ra.lora_embed_shrink(self.table.desc, self.meta.c, self.x.data_ptr(), self.buf.data_ptr(), st),
+                 "embed_shrink")
+        ra.check(ra.lora_expand(self.table.desc, self.meta.c, self.buf.data_ptr(), self.y.data_ptr(),
+                                self.y.stride(0), self.ydt, self.kind, st), "expand")
 
 
 KERNELS = {"fused": ("meta", "apply"), "split": ("meta", "shrink", "expand")}
@@ -448,7 +485,7 @@ def run_ours(args):
     for k, ad in sorted(inst.adapters.items()):
         master.set_slot(k, ad.rank, ad.scale, [dev(a, inst.dtype) for a in ad.A], [dev(b, inst.dtype) for b in ad.B])
         torch.cuda.synchronize()
-    x0 = dev(inst.x, inst.dtype)
+    x0 = dev(inst.x, inst.dtype) if inst.token_ids is None else torch.from_numpy(inst.token_ids).cuda()
     y0 = dev(inst.y_in, inst.dtype)
     ts0 = torch.from_numpy(inst.token_slot).cuda()
 

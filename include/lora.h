@@ -59,8 +59,10 @@ typedef enum {
   LORA_EUNSUPPORTED = 4,  /* valid but not implemented (e.g. SGMV on fp32 tables) */
   LORA_ECUDA = 5,         /* a CUDA launch or copy failed; see lora_last_cuda_error() */
   LORA_EBADSLOT = 6,      /* lora_query_status: some token slot ids were out of range */
-  LORA_EDEVICE = 7        /* lora_query_status: a kernel gave up waiting on its own pipeline
+  LORA_EDEVICE = 7,       /* lora_query_status: a kernel gave up waiting on its own pipeline
                              (a fault it avoided); outputs since lora_prepare_meta are invalid */
+  LORA_EBADTOKEN = 8      /* lora_query_status: lora_embed_shrink met token ids outside the
+                             vocabulary; those rows got no delta, the rest are valid */
 } lora_status;
 
 typedef enum { LORA_F32 = 0, LORA_BF16 = 1 } lora_dtype;
@@ -249,10 +251,34 @@ size_t lora_meta_tiles_bytes(int32_t num_slots);
 /*
  * Synchronise `stream`, copy meta->status to *out (host) and return
  * LORA_EDEVICE if a kernel since the last lora_prepare_meta gave up waiting
- * on its own pipeline, else LORA_OK if *out is 0 and LORA_EBADSLOT if some
- * token ids were out of range.
+ * on its own pipeline, else LORA_EBADTOKEN if lora_embed_shrink met token ids
+ * outside the vocabulary, else LORA_OK if *out is 0 and LORA_EBADSLOT if some
+ * token slot ids were out of range.
  */
 int lora_query_status(const lora_meta *meta, int32_t *out, lora_stream_t stream);
+
+/*
+ * Embedding lookup: the shrink of an embedding layer's LoRA (page "vLLM 源码完全
+ * 拆解(十八): 多 LoRA 服务", section "embedding 的 LoRA 是一个查表增量"). With
+ * desc->d_in the vocabulary size and one slice, A[0] = [num_slots, vocab, r_max]
+ * holds slot a's r-vector for token id v at A[0][a, v, :] (the page's
+ * lora_a_stacked; it indexes the flattened table at v + a * vocab). For every
+ * token t whose slot a = meta->token_slot[t] != 0,
+ *   buf[0, t, k] = scale[a] * A[0][a, token_id[t], k]     (k < rank a)
+ *   buf[0, t, k] = 0                                       (rank a <= k < r_max)
+ * -- lora_shrink's result for the one-hot row of token_id[t] -- and rows of
+ * slot-0 tokens are not written. lora_expand with the layer's B then adds the
+ * delta into the embedding output. A token id outside [0, d_in) gives a zero
+ * row (no delta) and makes lora_query_status report LORA_EBADTOKEN; it never
+ * traps.
+ *   token_id: device int32 [num_tokens], batch order (the rows of meta)
+ *   buf:      device fp32 [1, num_tokens, r_max], 16-byte aligned
+ * Needs no metadata output (only meta->token_slot) and no workspace.
+ * Errors: LORA_EINVAL for null pointers, n_slices != 1 or a table / meta
+ * mismatch; LORA_EALIGN for a misaligned buf.
+ */
+int lora_embed_shrink(const lora_layer_desc *desc, const lora_meta *meta, const int32_t *token_id, float *buf,
+                      lora_stream_t stream);
 
 /*
  * Allocation-free shrink. The multi-LoRA pages have no counterpart to this

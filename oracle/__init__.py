@@ -15,5 +15,5 @@ brute force, and independent library routines).
 """
 from .lora_oracle import (  # noqa: F401
     prepare_meta, shrink_requests, expand_requests, apply_requests, adapters_f64,
-    requests_of_token_slots,
+    requests_of_token_slots, embed_requests,
 )

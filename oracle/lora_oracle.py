@@ -180,6 +180,35 @@ def expand_requests(buf: np.ndarray, y_in: np.ndarray, adapters: Dict[int, Adapt
     return y
 
 
+def embed_requests(token_ids, adapters: Dict[int, AdapterF64], r_max: int, req_lengths, req_slots,
+                   num_slots: int) -> Tuple[np.ndarray, np.ndarray]:
+    """buf[0, t, :] of an embedding layer's LoRA; returns (buf, written).
+
+    Page "vLLM 源码完全拆解(十八): 多 LoRA 服务", section "embedding 的 LoRA 是一个
+    查表增量": the r-vector of token id v under slot a is row v of a's A table, so
+        buf[0, t, k] = scale * A[token_ids[t], k]   (k < rank),  0 for the rank tail.
+    Rows of no-LoRA tokens are left NaN and not written. A token id outside
+    [0, vocab) gets a zero row (no delta): the pages do not say; this reading
+    lets one bad id spoil nothing else.
+    """
+    token_ids = np.asarray(token_ids)
+    T = int(token_ids.shape[0])
+    buf = np.full((1, T, r_max), np.nan, dtype=np.float64)
+    written = np.zeros(T, dtype=bool)
+    for (t0, t1), a in zip(_request_rows(req_lengths), req_slots):
+        ad = _live_adapter(adapters, int(a), num_slots)
+        if ad is None or t1 == t0:
+            continue
+        r, scale, A, _ = ad
+        buf[0, t0:t1, :] = 0.0
+        for t in range(t0, t1):
+            v = int(token_ids[t])
+            if r > 0 and 0 <= v < A[0].shape[0]:
+                buf[0, t, :r] = scale * A[0][v, :r]
+        written[t0:t1] = True
+    return buf, written
+
+
 def apply_requests(x: np.ndarray, y_in: np.ndarray, adapters: Dict[int, AdapterF64],
                    out_sizes: Sequence[int], r_max: int, req_lengths, req_slots,
                    num_slots: int) -> np.ndarray:

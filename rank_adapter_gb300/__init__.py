@@ -8,7 +8,7 @@ has not been built (``__graft_entry__.build()`` or
 
 Low-level functions carry the C names and return the C status codes
 (``lora_set_slot``, ``lora_reset_slot``, ``lora_prepare_meta``,
-``lora_shrink``, ``lora_expand``, ``lora_workspace_bytes``,
+``lora_shrink``, ``lora_expand``, ``lora_embed_shrink``, ``lora_workspace_bytes``,
 ``lora_meta_tiles_bytes``, ``lora_query_status``, ``lora_strerror``,
 ``lora_last_cuda_error``). ``SlotTable`` and ``TokenMeta`` own torch buffers
 laid out as the ABI wants and call those functions; ``shrink`` / ``expand``
@@ -22,17 +22,18 @@ from typing import Optional, Sequence
 
 __all__ = [
     "LORA_OK", "LORA_EINVAL", "LORA_ERANGE", "LORA_EALIGN", "LORA_EUNSUPPORTED", "LORA_ECUDA",
-    "LORA_EBADSLOT", "LORA_EDEVICE", "LORA_F32", "LORA_BF16", "LORA_AUTO", "LORA_BGMV", "LORA_SGMV",
+    "LORA_EBADSLOT", "LORA_EDEVICE", "LORA_EBADTOKEN", "LORA_F32", "LORA_BF16", "LORA_AUTO", "LORA_BGMV", "LORA_SGMV",
     "LORA_MAX_SLICES", "LORA_MAX_NUM_SLOTS", "LORA_MAX_RANK", "LORA_SGMV_MIN_ROWS", "LORA_SGMV_TILE_M",
     "LORA_AUTO_SGMV_MIN_TOKENS",
     "LayerDesc", "Meta", "LoraError", "lib_path", "exported_symbols",
     "lora_set_slot", "lora_reset_slot", "lora_prepare_meta", "lora_shrink", "lora_expand", "lora_apply",
-    "lora_shrink_noalloc", "lora_noalloc_scratch_bytes",
+    "lora_shrink_noalloc", "lora_noalloc_scratch_bytes", "lora_embed_shrink", "embed_shrink",
     "lora_workspace_bytes", "lora_meta_tiles_bytes", "lora_query_status", "lora_strerror",
     "lora_last_cuda_error", "lora_launch_count", "SlotTable", "TokenMeta", "shrink", "expand", "apply", "workspace", "check",
 ]
 
-LORA_OK, LORA_EINVAL, LORA_ERANGE, LORA_EALIGN, LORA_EUNSUPPORTED, LORA_ECUDA, LORA_EBADSLOT, LORA_EDEVICE = range(8)
+(LORA_OK, LORA_EINVAL, LORA_ERANGE, LORA_EALIGN, LORA_EUNSUPPORTED, LORA_ECUDA, LORA_EBADSLOT, LORA_EDEVICE,
+ LORA_EBADTOKEN) = range(9)
 LORA_F32, LORA_BF16 = 0, 1
 LORA_AUTO, LORA_BGMV, LORA_SGMV = 0, 1, 2
 LORA_MAX_SLICES = 4
@@ -95,6 +96,7 @@ _sig = {
     "lora_workspace_bytes": (ctypes.c_size_t, [_P(LayerDesc), _i32, _i32]),
     "lora_meta_tiles_bytes": (ctypes.c_size_t, [_i32]),
     "lora_query_status": (_i32, [_P(Meta), _P(_i32), _vp]),
+    "lora_embed_shrink": (_i32, [_P(LayerDesc), _P(Meta), _vp, _vp, _vp]),
     "lora_strerror": (ctypes.c_char_p, [_i32]),
     "lora_last_cuda_error": (_i32, []),
     "lora_launch_count": (ctypes.c_uint64, []),
@@ -167,6 +169,11 @@ def lora_apply(desc: LayerDesc, meta: Meta, x: int, ldx: int, buf: int, y: int, 
                kind: int = LORA_AUTO, ws: int = 0, ws_bytes: int = 0, stream=None) -> int:
     return _lib.lora_apply(ctypes.byref(desc), ctypes.byref(meta), x, ldx, buf or None, y, ldy, y_dtype, kind,
                            ws or None, ws_bytes, _stream(stream))
+
+
+def lora_embed_shrink(desc: LayerDesc, meta: Meta, token_id: int, buf: int, stream=None) -> int:
+    """Embedding lookup: buf[0, t] = scale * A[slot t][token_id[t]] for LoRA tokens."""
+    return _lib.lora_embed_shrink(ctypes.byref(desc), ctypes.byref(meta), token_id, buf, _stream(stream))
 
 
 def lora_shrink_noalloc(desc: LayerDesc, meta: Meta, x: int, ldx: int, buf: int, stream=None) -> int:
@@ -332,6 +339,11 @@ def shrink(table: SlotTable, meta: TokenMeta, x, buf, kind: int = LORA_AUTO, str
     wsp, wsb, _keep = _ws_args(table, meta, kind, ws)
     check(lora_shrink(table.desc, meta.c, x.data_ptr(), x.stride(0), buf.data_ptr(), kind, wsp, wsb, stream),
           "lora_shrink")
+
+
+def embed_shrink(table: SlotTable, meta: TokenMeta, token_id, buf, stream=None) -> None:
+    """buf[0, t, :] = scale * A[slot t][token_id[t], :] for LoRA tokens (see lora_embed_shrink)."""
+    check(lora_embed_shrink(table.desc, meta.c, token_id.data_ptr(), buf.data_ptr(), stream), "lora_embed_shrink")
 
 
 def expand(table: SlotTable, meta: TokenMeta, buf, y, kind: int = LORA_AUTO, stream=None) -> None:

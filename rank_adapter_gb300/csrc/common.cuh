@@ -142,7 +142,7 @@ __device__ __forceinline__ void cp_async_wait_upto(int n) {
 struct WorkLists {
   static constexpr int kHeader = 8;
   static constexpr int kRec = 8;
-  static constexpr int kErrWord = 7;
+  static constexpr int kErrWord = 7;  // device error bits; kErrBadToken marks a token id outside the vocabulary
   __host__ __device__ static inline size_t ints(int S) {
     return kHeader + 4 * (size_t)kRec * S + 2 * ((size_t)S + 1) + 3 * (size_t)S;
   }
@@ -154,6 +154,11 @@ struct WorkLists {
 };
 
 enum ListSel { kListAll = 0, kListSmall = 1, kListLarge = 2 };
+
+// Error bit of the embedding lookup in the work lists' device error word: a
+// token id was outside the vocabulary (its row got no delta). The other bits
+// are pipeline waits that ran out.
+constexpr int32_t kErrBadToken = 1 << 8;
 
 // Device-side view of the metadata used by the compute kernels.
 struct MetaView {
@@ -242,6 +247,9 @@ cudaError_t launch_bgmv_apply_shrink(const lora_layer_desc &d, const MetaView &m
                                      int64_t ldx, float *buf, float *ws, cudaStream_t st);
 cudaError_t launch_bgmv_apply_expand(const lora_layer_desc &d, const MetaView &mv, ListSel sel, const float *ws,
                                      void *y, int64_t ldy, int y_dtype, cudaStream_t st);
+// Embedding lookup (embed.cu): buf rows of the one-hot token ids, see lora_embed_shrink.
+cudaError_t launch_embed_shrink(const lora_layer_desc &d, const MetaView &mv, const int32_t *token_slot,
+                                const int32_t *token_id, float *buf, cudaStream_t st);
 // SGMV family (sgmv.cu, tcgen05). part: split partials, sgmv_workspace_bytes() bytes.
 bool sgmv_supported();
 size_t sgmv_workspace_bytes(const lora_layer_desc &d, int max_tokens);

@@ -146,6 +146,7 @@ const char *lora_strerror(int status) {
     case LORA_ECUDA: return "CUDA launch or copy failed (see lora_last_cuda_error)";
     case LORA_EBADSLOT: return "some token slot ids were outside [0, num_slots) and were treated as slot 0";
     case LORA_EDEVICE: return "a kernel stopped waiting on its own pipeline; the outputs since the last lora_prepare_meta are invalid";
+    case LORA_EBADTOKEN: return "some token ids were outside the embedding vocabulary; their rows got no delta";
     default: return "unknown lora_status";
   }
 }
@@ -320,8 +321,24 @@ int lora_query_status(const lora_meta *meta, int32_t *out, lora_stream_t stream)
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) return cuda_status(e);
   *out = v[0];
-  if (v[1] != 0) return LORA_EDEVICE;
+  if ((v[1] & ~ra::kErrBadToken) != 0) return LORA_EDEVICE;
+  if (v[1] != 0) return LORA_EBADTOKEN;
   return v[0] == 0 ? LORA_OK : LORA_EBADSLOT;
+}
+
+int lora_embed_shrink(const lora_layer_desc *desc, const lora_meta *meta, const int32_t *token_id, float *buf,
+                      lora_stream_t stream) {
+  clear_stale_error();
+  int st = check_desc(desc);
+  if (st != LORA_OK) return st;
+  st = check_meta(meta);
+  if (st != LORA_OK) return st;
+  if (meta->num_slots != desc->num_slots || desc->n_slices != 1) return LORA_EINVAL;
+  if (meta->num_tokens == 0) return LORA_OK;
+  if (token_id == nullptr || buf == nullptr) return LORA_EINVAL;
+  if (!aligned16(buf) || reinterpret_cast<uintptr_t>(token_id) % sizeof(int32_t) != 0) return LORA_EALIGN;
+  return cuda_status(ra::launch_embed_shrink(*desc, view_of(meta), meta->token_slot, token_id, buf,
+                                             (cudaStream_t)stream));
 }
 
 }  // extern "C"

@@ -41,18 +41,20 @@ def test_header_constants_match_binding(ra):
         m = re.search(rf"#define {name} (\d+)", src)
         assert m and int(m.group(1)) == getattr(ra, name), name
     for i, name in enumerate(["LORA_OK", "LORA_EINVAL", "LORA_ERANGE", "LORA_EALIGN", "LORA_EUNSUPPORTED",
-                              "LORA_ECUDA", "LORA_EBADSLOT", "LORA_EDEVICE"]):
+                              "LORA_ECUDA", "LORA_EBADSLOT", "LORA_EDEVICE", "LORA_EBADTOKEN"]):
         assert re.search(rf"{name} = {i}\b", src) and getattr(ra, name) == i
 
 
 def test_strerror_and_sizes(ra):
-    for s in range(8):
+    for s in range(9):
         assert ra.lora_strerror(s) and "unknown" not in ra.lora_strerror(s)
     assert "unknown" in ra.lora_strerror(99)
     assert ra.lora_meta_tiles_bytes(0) == 0
     assert ra.lora_meta_tiles_bytes(64) == (8 + 4 * 8 * 64 + 2 * 65 + 3 * 64) * 4
     assert ra.lora_last_cuda_error() == 0
-    assert ra.lora_launch_count() == 0      # nothing launched on a host-only run
+    import torch
+    if not torch.cuda.is_available():       # nothing can launch on a host-only run
+        assert ra.lora_launch_count() == 0
 
 
 def _desc(ra, **kw):
@@ -111,6 +113,18 @@ def test_meta_validation(ra):
     m = _meta(ra)
     m.tiles = 0x4002
     assert ra.lora_prepare_meta(m, 0) == ra.LORA_EALIGN
+
+
+def test_embed_shrink_validation(ra):
+    one = _desc(ra, n_slices=1)
+    m = _meta(ra)
+    assert ra.lora_embed_shrink(_desc(ra), m, 0x9000, 0x6000, 0) == ra.LORA_EINVAL   # an embedding has one slice
+    assert ra.lora_embed_shrink(one, m, 0, 0x6000, 0) == ra.LORA_EINVAL              # no token ids
+    assert ra.lora_embed_shrink(one, m, 0x9000, 0, 0) == ra.LORA_EINVAL              # no buf
+    assert ra.lora_embed_shrink(one, m, 0x9000, 0x6008, 0) == ra.LORA_EALIGN         # buf not 16-byte aligned
+    assert ra.lora_embed_shrink(one, m, 0x9002, 0x6000, 0) == ra.LORA_EALIGN         # ids not int-aligned
+    assert ra.lora_embed_shrink(one, _meta(ra, S=5), 0x9000, 0x6000, 0) == ra.LORA_EINVAL  # slot count mismatch
+    assert ra.lora_embed_shrink(one, _meta(ra, T=0), 0, 0, 0) == ra.LORA_OK          # T = 0: no-op
 
 
 def test_shrink_expand_validation(ra):

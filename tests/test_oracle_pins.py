@@ -392,3 +392,41 @@ def test_sampled_rows_mapping_and_restriction():
     assert live.any()
     assert not np.array_equal(y_s[live], y_in[rows][live])
 
+
+def test_embedding_lookup_is_the_one_hot_shrink():
+    """The embedding lookup (page "vLLM 源码完全拆解(十八): 多 LoRA 服务", section
+    "embedding 的 LoRA 是一个查表增量") equals the linear shrink applied to each
+    token's one-hot row, exactly, and reads the row the page's flattened table
+    gives at token id + slot * vocab; an id outside the vocabulary gives a zero row."""
+    vocab = 50
+    inst = wl.make_instance("embed_lookup", num_tokens=30, d_in=vocab, out_sizes=[24], num_slots=5, r_max=16,
+                            dtype="f32")
+    for k, (r, s) in zip(sorted(inst.adapters), [(16, 2.0), (3, 0.5), (9, 1.0), (1, 4.0)]):
+        ad = inst.adapters[k]
+        inst.adapters[k] = wl.Adapter(r, s, [ad.A[0][:, :r].copy()], [ad.B[0][:r].copy()])
+    ids = inst.token_ids.copy()
+    ids[3] = vocab + 7          # outside the vocabulary
+    ids[4] = -1
+    ads = lo.adapters_f64(inst)
+    L, Sl, S, R = inst.req_lengths, inst.req_slots, inst.num_slots, inst.r_max
+    buf, written = lo.embed_requests(ids, ads, R, L, Sl, S)
+    onehot = np.zeros((inst.num_tokens, vocab))
+    ok = (ids >= 0) & (ids < vocab)
+    onehot[np.arange(inst.num_tokens)[ok], ids[ok]] = 1.0
+    ref, w_ref = lo.shrink_requests(onehot, ads, 1, R, L, Sl, S)
+    assert np.array_equal(written, w_ref)
+    assert np.array_equal(np.nan_to_num(buf, nan=-9.0), np.nan_to_num(ref, nan=-9.0))
+    # the page's flattened table: row v + a * vocab of A stacked over all slots
+    a_2d = np.zeros((S * vocab, R))
+    for a, (r, s, A, _) in ads.items():
+        a_2d[a * vocab:(a + 1) * vocab, :r] = A[0][:, :r]
+    ts = inst.token_slot
+    for t in range(inst.num_tokens):
+        a = int(ts[t])
+        if a == 0:
+            assert not written[t]
+        elif ok[t]:
+            assert np.array_equal(buf[0, t], ads[a][1] * a_2d[ids[t] + a * vocab])
+        else:
+            assert np.all(buf[0, t] == 0.0)
+

@@ -20,6 +20,10 @@ Workloads (sizes follow the Llama-3-8B-shaped projections the pages use):
                     1024 decode tokens + 4 prefill chunks of 512, 5% slot 0.
 * ``full_decode``   one decode step over 32 layers x {qkv, o, gate_up, down},
                     r=16, 100 resident adapters, 512 tokens.
+* ``embed_lookup``  the embedding layer's LoRA (page "vLLM 源码完全拆解(十八):
+                    多 LoRA 服务", section "embedding 的 LoRA 是一个查表增量"):
+                    vocab 128256 -> hidden 4096, r=16, 64 slots, 256 decode
+                    tokens with ids uniform over the vocabulary, 10% slot 0.
 * ``logits_lm_head`` the lm_head LoRA on the rows sampled this step (page
                     "vLLM 源码完全拆解(十八): 多 LoRA 服务", section
                     "lm_head / logits"): hidden 4096 -> vocab 128256, r=16,
@@ -43,7 +47,7 @@ __all__ = [
 ]
 
 CONFIG_NAMES = ("toy_fp32", "decode_qkv", "prefill_gate_up", "mixed_o_proj", "full_decode")
-EXTRA_NAMES = ("logits_lm_head",)   # widening beyond the five configurations
+EXTRA_NAMES = ("logits_lm_head", "embed_lookup")   # widening beyond the five configurations
 
 _CHUNK = 1 << 24
 
@@ -106,6 +110,7 @@ class Instance:
     x: np.ndarray                   # [T, d_in] (uint16 bits or float32)
     y_in: np.ndarray                # [T, sum(out_sizes)]
     meta: dict = field(default_factory=dict)
+    token_ids: Optional[np.ndarray] = None   # int32 [T]: an embedding layer's input (x is then empty)
 
     @property
     def num_tokens(self) -> int:
@@ -198,7 +203,7 @@ def make_instance(name: str, seed: Optional[int] = None, *, num_tokens: Optional
     Config i uses seed i (``toy_fp32`` seed 0) unless ``seed`` is given.
     """
     default_seed = {"toy_fp32": 0, "decode_qkv": 2, "prefill_gate_up": 3,
-                    "mixed_o_proj": 4, "full_decode": 5, "logits_lm_head": 6}
+                    "mixed_o_proj": 4, "full_decode": 5, "logits_lm_head": 6, "embed_lookup": 7}
     if name not in default_seed:
         raise ValueError(f"unknown workload {name!r}")
     rng = np.random.Generator(np.random.PCG64(default_seed[name] if seed is None else seed))
@@ -285,6 +290,28 @@ def make_instance(name: str, seed: Optional[int] = None, *, num_tokens: Optional
         scales = {k: 1.0 for k in range(1, S)}
         adapters = _draw_adapters(rng, range(1, S), D, outs, ranks, scales, 64.0, 16.0, dt)
         x_inv, a_note = 1.0, "A~N/64, B~N/16"
+    elif name == "embed_lookup":
+        # d_in is the vocabulary: A[a] holds one r-vector per token id.
+        dt = dtype or "bf16"
+        D = d_in or 128256
+        outs = list(out_sizes or [4096])
+        S = num_slots or 64
+        R = r_max or 16
+        n = num_tokens or 256
+        lengths = np.asarray(req_lengths if req_lengths is not None else np.ones(n), np.int64)
+        none = rng.random(len(lengths)) < 0.10
+        slots = np.where(none, 0, rng.integers(1, S, size=len(lengths))).astype(np.int32)
+        ranks = {k: R for k in range(1, S)}
+        scales = {k: 1.0 for k in range(1, S)}
+        adapters = _draw_adapters(rng, range(1, S), D, outs, ranks, scales, 1.0, 16.0, dt)
+        T = int(lengths.sum())
+        ids = rng.integers(0, D, size=T).astype(np.int32)
+        x = np.zeros((T, 0), np.uint16 if dt == "bf16" else np.float32)
+        y_in = _normal(rng, (T, int(sum(outs))), 1.0, dt)
+        return Instance(name=name, dtype=dt, d_in=D, out_sizes=outs, num_slots=S, r_max=R, adapters=adapters,
+                        req_lengths=lengths, req_slots=slots, x=x, y_in=y_in, token_ids=ids,
+                        meta={"seed": default_seed[name] if seed is None else seed,
+                              "values": "token ids U[0, vocab), y_in~N(0,1), A~N(0,1), B~N/16"})
     else:  # full_decode: one (layer, group); see full_decode_groups for the whole step
         raise ValueError("full_decode is built per (layer, group) by full_decode_groups()")
 
