@@ -17,7 +17,9 @@
 //   scaled rank-r rows u = s * x A directly).
 // * expand: one CTA per (segment, slice, column chunk of 32 KB of B). It
 //   forms u by summing the chunk partials in chunk order (or reads u), then
-//   adds u B into y with packed FMAs over pairs of rank indices.
+//   adds u B into y with packed FMAs over pairs of rank indices. Where the
+//   chunk is narrower than the block (high ranks), thread groups take
+//   several token tiles of a unit at once.
 // * reduce: for the split path, turns the partials into the u buffer with
 //   the same arithmetic, so shrink + expand and the fused apply (shrink +
 //   expand-from-partials, two launches) give bitwise identical results.
@@ -48,6 +50,8 @@ constexpr int kWideGrid = 2048;
 constexpr int kSmallTable = 256;     // slot tables up to this size: rank / scale copied whole
 constexpr int kRowsWin = 32;         // token rows of a unit kept in shared memory (a sliding window)
 constexpr int kKCReg = 16;           // expand: chunk partials of the next tile held in registers
+constexpr int kExpandNG = 4;         // expand: most token tiles of a unit run side by side
+constexpr int kReach = kThreads * 4; // expand: columns one tile pass of the whole block covers
 
 struct Geo {
   int d_in, r_max;
@@ -213,13 +217,13 @@ __device__ __forceinline__ void issue_b(TW *Bs, int pw, const TW *Bslot, int out
 // y[rows[t], col_base + c] += sum_k u[t][k] B[k][c] for tokens t < nt and
 // columns [0, pcn) of a staged pass. Bs holds B rows 0..r_pad-1 (r_pad = r_a
 // rounded up to even; an extra row is zero); us is u as [kTT][r_max] with the
-// rank tail and absent tokens zero. One thread per 4 columns; pairs of k in
-// the two lanes of packed FMAs.
-template <typename TW, typename TY>
+// rank tail and absent tokens zero. Thread lt of a group of GS threads takes
+// columns 4 lt, 4 (lt + GS), ...; pairs of k in the two lanes of packed FMAs.
+template <typename TW, typename TY, int GS>
 __device__ __forceinline__ void expand_pass(const TW *Bs, int pw, const float *us, int r_max, int r_pad,
                                             const int *rows, int rbase, int nt, TY *y, int64_t ldy, int col_base,
-                                            int pcn) {
-  for (int cq = threadIdx.x * 4; cq < pcn; cq += kThreads * 4) {
+                                            int pcn, int lt) {
+  for (int cq = lt * 4; cq < pcn; cq += GS * 4) {
     float2 acc[kTT][4];
 #pragma unroll
     for (int t = 0; t < kTT; ++t)
@@ -463,9 +467,88 @@ __global__ void __launch_bounds__(kThreads) bgmv_reduce_kernel(BgmvArgs a) {
   }
 }
 
+// The token passes of one expand unit of several tiles: a pass takes NG
+// tiles (kTT * NG tokens) at once, tile q of the pass on thread group q of
+// kThreads / NG threads; u of a pass is [kTT * NG][r_max] in shared memory,
+// zero past the unit.
+template <typename TW, typename TY, int NG>
+__device__ __forceinline__ void expand_passes(const BgmvArgs &a, const Unit &u, int s, int *rows, float *us,
+                                              const TW *Bs, TY *y, int col_base, int pcn, int r_pad) {
+  const Geo &g = a.g;
+  const int r_max = g.r_max;
+  // u of token t (of the unit) and rank index k: the partials summed in chunk
+  // order and scaled, or the u buffer. A tile's values go to one of two buffers.
+  auto u_val = [&](int tok, int k) -> float {
+    if (k >= u.r_a) return 0.f;
+    if (a.u_parts) return u_from_partials(a, s, u.start + tok, k, u);
+    return a.u_in[((int64_t)s * a.mv.num_tokens + rows[tok % kRowsWin]) * r_max + k];
+  };
+  constexpr int GS = kThreads / NG;
+  const int tpp = kTT * NG;
+  const int grp = (int)threadIdx.x / GS, lt = (int)threadIdx.x - grp * GS;
+  auto fill = [&](int pass, float *dst) {
+    const int n = min(tpp, u.cnt - pass * tpp);
+    for (int i = threadIdx.x; i < tpp * r_max; i += kThreads) {
+      const int t = i / r_max, k = i - t * r_max;
+      dst[i] = t < n ? u_val(pass * tpp + t, k) : 0.f;
+    }
+  };
+  // The next pass's partials are loaded into registers before this pass's
+  // products and summed after them, so their latency is hidden.
+  const bool overlap = a.u_parts && g.kc_count <= kKCReg && tpp * r_max <= kThreads;
+  const int npass = (u.cnt + tpp - 1) / tpp;
+  fill(0, us);
+  for (int pass = 0; pass < npass; ++pass) {
+    float *cur = us + (pass & 1) * tpp * r_max, *nxt_us = us + ((pass + 1) & 1) * tpp * r_max;
+    cp_async_wait_upto(0);
+    __syncthreads();  // the B chunk, this pass's u and token rows are in shared memory
+    const int nxt = pass + 1;
+    const bool next_in_window = nxt < npass && (nxt * tpp) % kRowsWin != 0;
+    float pref[kKCReg];
+    const int i = threadIdx.x, pt = i / r_max, pk = i - pt * r_max;
+    const bool mine = overlap && next_in_window && i < tpp * r_max && pt < min(tpp, u.cnt - nxt * tpp) &&
+                      pk < u.r_a;
+    if (mine) {
+      const float *p = a.u_in + (((int64_t)s * a.mv.num_tokens + u.start + nxt * tpp + pt) * g.kc_count) * r_max + pk;
+#pragma unroll
+      for (int c = 0; c < kKCReg; ++c)
+        if (c < g.kc_count) pref[c] = p[c * r_max];
+    }
+    const int tok0 = pass * tpp + grp * kTT, nt = min(kTT, u.cnt - tok0);
+    if (nt > 0)
+      expand_pass<TW, TY, GS>(Bs, g.pw, cur + grp * kTT * r_max, r_max, r_pad, rows, tok0, nt, y, a.ldy, col_base,
+                              pcn, lt);
+    if (nxt < npass) {
+      if (!next_in_window) {  // a new window of token rows
+        __syncthreads();
+        for (int j = threadIdx.x; j < kRowsWin && nxt * tpp + j < u.cnt; j += kThreads)
+          rows[j] = a.mv.sorted_rows[u.start + nxt * tpp + j];
+        __syncthreads();
+        if ((int)threadIdx.x < min(u.cnt - nxt * tpp, kRowsWin))
+          prefetch_l2(y + (int64_t)rows[threadIdx.x] * a.ldy + col_base, (uint32_t)(pcn * sizeof(TY)));
+        fill(nxt, nxt_us);
+      } else if (overlap) {
+        if (i < tpp * r_max) {
+          float v = 0.f;
+          if (mine) {  // same order and arithmetic as u_from_partials
+            float sum = 0.f;
+#pragma unroll
+            for (int c = 0; c < kKCReg; ++c)
+              if (c < g.kc_count) sum += pref[c];
+            v = u.scale * sum;
+          }
+          nxt_us[i] = v;
+        }
+      } else {
+        fill(nxt, nxt_us);
+      }
+    }
+  }
+}
+
 // Expand: one CTA per (segment, slice, column chunk of pw). Grid: (chunks over all slices, max_items).
 // u comes from the chunk partials (u_parts) or from the u buffer.
-template <typename TW, typename TY>
+template <typename TW, typename TY, bool GROUPS>
 __global__ void __launch_bounds__(kThreads, 3) bgmv_expand_kernel(BgmvArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
   // Behind this library's shrink (or reduce), the metadata and the slot
@@ -510,7 +593,19 @@ __global__ void __launch_bounds__(kThreads, 3) bgmv_expand_kernel(BgmvArgs a) {
     pdl_wait();
     pdl_trigger();
   }
-  // u of token t (of the unit) and rank index k: the partials summed in chunk
+  // A chunk narrower than half the block's reach (4 columns per thread)
+  // would leave threads idle (GROUPS), so a unit of several tiles runs up to
+  // that many tiles at once, tile q of a pass on thread group q. Every output
+  // takes the same arithmetic for any group count. Wider chunks keep one tile
+  // at a time: there, running tiles side by side measured slower.
+  if constexpr (GROUPS) {
+    const int ng_geo = g.pw * 4 <= kReach ? 4 : 2;
+    const int nt_all = (u.cnt + kTT - 1) / kTT;
+    const int ng = min(ng_geo, nt_all >= 3 ? 4 : nt_all);
+    if (ng == 4) return expand_passes<TW, TY, 4>(a, u, s, rows, us, Bs, y, col_base, pcn, r_pad);
+    if (ng == 2) return expand_passes<TW, TY, 2>(a, u, s, rows, us, Bs, y, col_base, pcn, r_pad);
+  }
+  // One tile at a time. u of token t (of the unit) and rank index k: the partials summed in chunk
   // order and scaled, or the u buffer. A tile's values go to one of two buffers.
   auto u_val = [&](int tok, int k) -> float {
     if (k >= u.r_a) return 0.f;
@@ -546,7 +641,8 @@ __global__ void __launch_bounds__(kThreads, 3) bgmv_expand_kernel(BgmvArgs a) {
       for (int c = 0; c < kKCReg; ++c)
         if (c < g.kc_count) pref[c] = p[c * r_max];
     }
-    expand_pass<TW, TY>(Bs, g.pw, cur, r_max, r_pad, rows, tile * kTT, nt, y, a.ldy, col_base, pcn);
+    expand_pass<TW, TY, kThreads>(Bs, g.pw, cur, r_max, r_pad, rows, tile * kTT, nt, y, a.ldy, col_base,
+                                    pcn, (int)threadIdx.x);
     if (nxt < ntiles) {
       if (!next_in_window) {  // a new window of token rows
         __syncthreads();
@@ -603,8 +699,6 @@ Geo make_geo(const lora_layer_desc &d, bool wide = false) {
   off += align16(2 * kSmallTable * 4);
   g.off_rows = off;
   off += align16(kRowsWin * 4);
-  g.off_u = off;
-  off += align16(2 * kTT * d.r_max * 4);  // two tiles of u (expand)
   const int common = off;
   // shrink: ring + reduction buffer
   g.off_ring = off;
@@ -612,9 +706,12 @@ Geo make_geo(const lora_layer_desc &d, bool wide = false) {
   g.off_red = off;
   off += align16(kSWarps * kTT * d.r_max * 4);
   g.smem_shrink = off;
-  // expand: one B chunk (+ the zero partner row of an odd rank)
-  g.off_b = common;
-  g.smem_expand = common + align16((d.r_max + 1) * pw * es);
+  // expand: u of two passes (of up to kExpandNG tiles where the chunk is
+  // narrow enough for tiles side by side), one B chunk (+ the zero partner
+  // row of an odd rank)
+  g.off_u = common;
+  g.off_b = common + align16(2 * (pw * 2 <= kReach ? kExpandNG : 1) * kTT * d.r_max * 4);
+  g.smem_expand = g.off_b + align16((d.r_max + 1) * pw * es);
   g.smem_reduce = common;
   return g;
 }
@@ -694,9 +791,14 @@ cudaError_t dispatch_shrink(const BgmvArgs &a, cudaStream_t st) {
 
 cudaError_t launch_expand(const BgmvArgs &a, int dtype, int y_dtype, cudaStream_t st) {
   void (*k)(BgmvArgs);
-  if (dtype == LORA_BF16 && y_dtype == LORA_BF16) k = bgmv_expand_kernel<__nv_bfloat16, __nv_bfloat16>;
-  else if (dtype == LORA_BF16) k = bgmv_expand_kernel<__nv_bfloat16, float>;
-  else k = bgmv_expand_kernel<float, float>;
+  const bool groups = a.g.pw * 2 <= kReach;  // column chunks that leave threads idle: tiles side by side
+  if (dtype == LORA_BF16 && y_dtype == LORA_BF16)
+    k = groups ? bgmv_expand_kernel<__nv_bfloat16, __nv_bfloat16, true>
+               : bgmv_expand_kernel<__nv_bfloat16, __nv_bfloat16, false>;
+  else if (dtype == LORA_BF16)
+    k = groups ? bgmv_expand_kernel<__nv_bfloat16, float, true> : bgmv_expand_kernel<__nv_bfloat16, float, false>;
+  else
+    k = groups ? bgmv_expand_kernel<float, float, true> : bgmv_expand_kernel<float, float, false>;
   cudaError_t e = set_max_dynamic_smem((const void *)k, a.g.smem_expand);
   if (e != cudaSuccess) return e;
   return launch_pdl(k, dim3((unsigned)a.chunk_start[a.n_slices], (unsigned)a.max_items), dim3(kThreads),

@@ -533,7 +533,11 @@ struct URowArgs {
 
 // u[k] for 16 consecutive k (k0 multiple of 16) of one row: scale * the
 // tile's pieces summed in CTA order (masked to the slot's rank), or the
-// buffer. All loads of one piece are issued together.
+// buffer. The loads of FB pieces are issued together, then summed in order,
+// so a row waits for one round trip per FB pieces (the reduce kernel takes
+// FB = 4; the expand's loader warps keep FB = 1, which leaves the registers
+// its epilogue warps need).
+template <int FB>
 __device__ __forceinline__ void u_row16(const URowArgs &u, int tile, int slice, int row, int tok, int k0, int r_a,
                                         float scale, float (&v)[16]) {
 #pragma unroll
@@ -541,21 +545,52 @@ __device__ __forceinline__ void u_row16(const URowArgs &u, int tile, int slice, 
   if (k0 >= r_a) return;
   if (u.parts) {
     const int c0 = u.sp.cta_of((int64_t)tile * u.sp.nb), c1 = u.sp.cta_of((int64_t)(tile + 1) * u.sp.nb - 1);
-    for (int c = c0; c <= c1; ++c) {
-      const int64_t cu0 = u.sp.u0(c);
-      if (u.sp.u0(c + 1) == cu0) continue;  // fewer units than CTAs: this CTA has none
-      const int j = tile - (int)(cu0 / u.sp.nb);
-      const float4 *p = reinterpret_cast<const float4 *>(
-          u.src + ((((int64_t)c * u.sp.maxp + j) * u.n_slices + slice) * kTileM + row) * u.r_max + k0);
-      float4 q[4];
+    if constexpr (FB == 1) {
+      for (int c = c0; c <= c1; ++c) {
+        const int64_t cu0 = u.sp.u0(c);
+        if (u.sp.u0(c + 1) == cu0) continue;  // fewer units than CTAs: this CTA has none
+        const int j = tile - (int)(cu0 / u.sp.nb);
+        const float4 *p = reinterpret_cast<const float4 *>(
+            u.src + ((((int64_t)c * u.sp.maxp + j) * u.n_slices + slice) * kTileM + row) * u.r_max + k0);
+        float4 q[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) q[i] = p[i];
+        for (int i = 0; i < 4; ++i) q[i] = p[i];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        v[4 * i] += q[i].x;
-        v[4 * i + 1] += q[i].y;
-        v[4 * i + 2] += q[i].z;
-        v[4 * i + 3] += q[i].w;
+        for (int i = 0; i < 4; ++i) {
+          v[4 * i] += q[i].x;
+          v[4 * i + 1] += q[i].y;
+          v[4 * i + 2] += q[i].z;
+          v[4 * i + 3] += q[i].w;
+        }
+      }
+    } else {
+      for (int cb = c0; cb <= c1; cb += FB) {
+        float4 q[FB][4];
+        bool have[FB];
+#pragma unroll
+        for (int b = 0; b < FB; ++b) {
+          const int c = cb + b;
+          const int64_t cu0 = c <= c1 ? u.sp.u0(c) : 0;
+          have[b] = c <= c1 && u.sp.u0(c + 1) != cu0;  // fewer units than CTAs: a CTA may have none
+          if (have[b]) {
+            const int j = tile - (int)(cu0 / u.sp.nb);
+            const float4 *p = reinterpret_cast<const float4 *>(
+                u.src + ((((int64_t)c * u.sp.maxp + j) * u.n_slices + slice) * kTileM + row) * u.r_max + k0);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) q[b][i] = p[i];
+          }
+        }
+#pragma unroll
+        for (int b = 0; b < FB; ++b) {
+          if (!have[b]) continue;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            v[4 * i] += q[b][i].x;
+            v[4 * i + 1] += q[b][i].y;
+            v[4 * i + 2] += q[b][i].z;
+            v[4 * i + 3] += q[b][i].w;
+          }
+        }
       }
     }
 #pragma unroll
@@ -609,7 +644,7 @@ __global__ void __launch_bounds__(kTileM) sgmv_reduce_kernel(const SgReduceArgs 
     float *dst = a.buf + ((int64_t)slice * u.T + tok) * u.r_max;
     for (int k0 = 0; k0 < u.r_max; k0 += 16) {
       float v[16];
-      u_row16(u, tile, slice, row, tok, k0, r_a, scale, v);
+      u_row16<4>(u, tile, slice, row, tok, k0, r_a, scale, v);
 #pragma unroll
       for (int i = 0; i < 4; ++i)
         reinterpret_cast<float4 *>(dst + k0)[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
@@ -933,7 +968,7 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
         if (!mbar_wait_warp(uempty, (g & 1) ^ 1, a.err, kErrExpand)) break;
         for (int k0 = 0; k0 < r_max; k0 += 16) {
           float v[16];
-          u_row16(u, e.tile, e.slice, lt, tok, k0, r_a, scale, v);
+          u_row16<1>(u, e.tile, e.slice, lt, tok, k0, r_a, scale, v);
 #pragma unroll
           for (int hc = 0; hc < 2; ++hc) {  // two 16-byte chunks of 8 k values
             uint4 hi, lo;

@@ -154,6 +154,27 @@ def test_deterministic_and_permutation_invariant(lib):
     assert np.array_equal(b3, b1[:, perm], equal_nan=True)
 
 
+def test_high_rank_rows_independent_of_slot_sharing(lib):
+    """A high-rank layer (r_max 64: expand column chunks narrower than the block, so a
+    slot's token tiles run side by side, up to four at once): each token's y row is
+    bitwise the row it gets in a batch where its slot holds far fewer tokens."""
+    lengths = [1] * 9 + [14, 6, 23, 2, 9, 40]
+    full = wl.make_instance("mixed_o_proj", req_lengths=lengths, d_in=1024, out_sizes=[256], num_slots=6)
+    t = load_table(full)
+    for path in ("apply", "split"):
+        _, y_all, _ = run_gpu(full, table=t, kind=lib.LORA_BGMV, y_dtype="f32", path=path)
+        rows = np.arange(0, full.num_tokens, 3)
+        solo = wl.make_instance("mixed_o_proj", req_lengths=[1] * len(rows), d_in=1024, out_sizes=[256],
+                                num_slots=6)
+        solo.adapters = full.adapters
+        solo.req_slots = full.token_slot[rows].copy()
+        solo.x = full.x[rows].copy()
+        solo.y_in = full.y_in[rows].copy()
+        assert np.bincount(solo.token_slot).max() < np.bincount(full.token_slot).max()
+        _, y_s, _ = run_gpu(solo, table=t, kind=lib.LORA_BGMV, y_dtype="f32", path=path)
+        assert np.array_equal(y_s.view(np.uint32), y_all[rows].view(np.uint32)), path
+
+
 # ----------------------------------------------------------------------------- fused lora_apply
 
 APPLY_CASES = {
