@@ -510,43 +510,72 @@ def run_ours(args):
     other_steps = min(args.steps, 20 * G)
     o_ms, o_avg, _, _ = time_path(torch, ra, reps, stream, other, other_steps, G)
 
-    # End to end: the same step through the ABI with pinned host buffers and copies in / out.
+    # End to end: every step copies its inputs in from pinned host memory, runs through the ABI and
+    # copies its result back to pinned host memory. A serving loop double-buffers: two replicas on two
+    # streams alternate, so one step's copies overlap the other's kernels; each step is one replay of
+    # a CUDA graph holding its copies and library calls (no per-call host overhead).
     h_x = torch.empty_like(x0, device="cpu").pin_memory()
     h_x.copy_(x0)
     h_y = torch.empty_like(y0, device="cpu").pin_memory()
     h_y.copy_(y0)
     h_ts = torch.empty_like(ts0, device="cpu").pin_memory()
     h_ts.copy_(ts0)
-    h_out = torch.empty_like(y0, device="cpu").pin_memory()
-    e2e_rep = reps[0]
+    pair = [reps[0], reps[1 % R]]
+    nbuf = 2 if R > 1 else 1
+    h_out = [torch.empty_like(y0, device="cpu").pin_memory() for _ in range(nbuf)]
     h2d = h_x.numel() * h_x.element_size() + h_y.numel() * h_y.element_size() + h_ts.numel() * 4
-    d2h = h_out.numel() * h_out.element_size()
+    d2h = h_out[0].numel() * h_out[0].element_size()
     ne = max(3, args.e2e_steps)
     T = inst.num_tokens
+    streams = [stream] + [torch.cuda.Stream() for _ in range(nbuf - 1)]
 
-    def e2e_step(i):
-        e2e_rep.x.copy_(h_x, non_blocking=True)
-        e2e_rep.y.copy_(h_y, non_blocking=True)
-        e2e_rep.meta.token_slot[:T].copy_(h_ts, non_blocking=True)
-        e2e_rep.launch(ra, i, path=args.path)
-        h_out.copy_(e2e_rep.y, non_blocking=True)
+    def e2e_step(j):
+        rep = pair[j]
+        rep.x.copy_(h_x, non_blocking=True)
+        rep.y.copy_(h_y, non_blocking=True)
+        rep.meta.token_slot[:T].copy_(h_ts, non_blocking=True)
+        rep.launch(ra, j, path=args.path)
+        h_out[j].copy_(rep.y, non_blocking=True)
 
-    with torch.cuda.stream(stream):
-        for i in range(3):
-            e2e_step(i)
-    stream.synchronize()
+    e2e_graphs = []
+    for j in range(nbuf):
+        with torch.cuda.stream(streams[j]):
+            e2e_step(j)  # warm (eager) before capture
+        streams[j].synchronize()
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=streams[j]):
+            e2e_step(j)
+        e2e_graphs.append(gr)
+    for i in range(3 * nbuf):
+        with torch.cuda.stream(streams[i % nbuf]):
+            e2e_graphs[i % nbuf].replay()
+    torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    joins = [torch.cuda.Event() for _ in range(nbuf)]
     t0 = time.perf_counter()
-    with torch.cuda.stream(stream):
+    with torch.cuda.stream(streams[0]):
         e0.record()
-        for i in range(ne):
-            e2e_step(i)
+    for j in range(1, nbuf):
+        streams[j].wait_event(e0)
+    for i in range(ne):
+        with torch.cuda.stream(streams[i % nbuf]):
+            e2e_graphs[i % nbuf].replay()
+    for j in range(1, nbuf):
+        joins[j].record(streams[j])
+        streams[0].wait_event(joins[j])
+    with torch.cuda.stream(streams[0]):
         e1.record()
-    stream.synchronize()
+    streams[0].synchronize()
     e2e_wall = time.perf_counter() - t0
     e2e_ms = e0.elapsed_time(e1)
+    torch.cuda.synchronize()
+    # The result the last step brought back is the full step's result (checked against a device step).
+    last = (ne - 1) % nbuf
+    ref_y = pair[last].y.cpu()
+    if not torch.equal(h_out[last], ref_y):
+        raise RuntimeError("end-to-end step: the host copy of y differs from the device result")
 
     elapsed_ms, e2e_ms, total_TL = reduce_over_ranks(torch, dist, elapsed_ms, e2e_ms, alg["T_L"], "cuda")
     launches = int(round(per_step * args.steps))  # counted by the library while capturing the step graph
@@ -586,7 +615,8 @@ def run_ours(args):
             "clocks": clocks.summary(),
             "e2e": {"value": total_TL * ne / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / ne, "wall_s": e2e_wall,
-                    "path": "pinned host x, y_in, token_slot -> device; one step; y -> host"},
+                    "path": f"per step: pinned host x, y_in, token_slot -> device; one step; y -> host; "
+                            f"{nbuf} replica(s) on {nbuf} stream(s) alternating, each step one CUDA-graph replay"},
         }
         if world == 1 and not args.no_cpu_baseline:
             line["cpu_baseline"] = run_cpu_baseline(args)
@@ -723,11 +753,17 @@ def run_full_decode(args):
     with torch.cuda.stream(stream):
         e2e_step()
     stream.synchronize()
+    e2e_graph = torch.cuda.CUDAGraph()  # the step's copies and calls, replayed as one graph per step
+    with torch.cuda.graph(e2e_graph, stream=stream):
+        e2e_step()
+    with torch.cuda.stream(stream):
+        e2e_graph.replay()
+    stream.synchronize()
     f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         f0.record()
         for _ in range(ne):
-            e2e_step()
+            e2e_graph.replay()
         f1.record()
     stream.synchronize()
     e2e_ms = f0.elapsed_time(f1)
@@ -754,7 +790,8 @@ def run_full_decode(args):
             "clocks": clocks.summary(),
             "e2e": {"value": total_TL * ne / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / ne,
-                    "path": "pinned host token slots and every group's x, y_in -> device; one step; every y -> host"},
+                    "path": "pinned host token slots and every group's x, y_in -> device; one step; every y -> host; "
+                            "each step one CUDA-graph replay"},
         }
         if world == 1 and not args.no_cpu_baseline:
             cores = len(os.sched_getaffinity(0))
