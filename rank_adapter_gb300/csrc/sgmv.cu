@@ -415,13 +415,23 @@ __global__ void __launch_bounds__(kShrinkThreads, 1)
           break;
         }
         unsigned char *st = sm + s * a.stage_bytes;
-        if (tid == 0) {
-          mbar_arrive_tx(&full[s], (uint32_t)(a.n_slices * a.w_bytes + (contiguous ? kTileM * 128 : 0)));
-          for (int sl = 0; sl < a.n_slices; ++sl)
-            for (int bx = 0; bx * a.box_n < a.r_max; ++bx)
-              tma_load_3d(st + kTileM * 128 + sl * a.w_bytes + bx * (kKB * a.box_n * 2), &maps.m[sl],
-                          bx * a.box_n, kb * kKB, ti.slot, &full[s]);
-          if (contiguous) tma_load_2d(st, &maps.x, kb * kKB, tok0, &full[s]);
+        // One thread's tensor copies complete one after another (about half a
+        // microsecond each, whatever their size), so a stage's copies go out
+        // from separate lanes, and the lanes rotate with the stage over eight
+        // groups of 16: the group's first lane posts the stage's bytes, then
+        // copies x; the next lanes copy one A box each.
+        const int grp = issued & 7;
+        if (warp == (grp >> 1)) {
+          const int l = lane - (grp & 1) * 16;
+          if (l == 0) mbar_arrive_tx(&full[s], (uint32_t)(a.n_slices * a.w_bytes + (contiguous ? kTileM * 128 : 0)));
+          __syncwarp();
+          const int nbx = (a.r_max + a.box_n - 1) / a.box_n;
+          if (l == 0 && contiguous) tma_load_2d(st, &maps.x, kb * kKB, tok0, &full[s]);
+          if (l >= 1 && l <= a.n_slices * nbx) {
+            const int sl = (l - 1) / nbx, bx = (l - 1) - sl * nbx;
+            tma_load_3d(st + kTileM * 128 + sl * a.w_bytes + bx * (kKB * a.box_n * 2), &maps.m[sl], bx * a.box_n,
+                        kb * kKB, ti.slot, &full[s]);
+          }
         }
         if (!contiguous) {
           const int col = kb * kKB + chunk * 8;
