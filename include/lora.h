@@ -33,7 +33,11 @@
  *   table through lora_set_slot / lora_reset_slot (they end with a launch
  *   that waits for the write to be visible); a table written any other way
  *   needs one more kernel, an event wait or a copy between the write and the
- *   next call of this library.
+ *   next call of this library. lora_prepare_meta likewise reads
+ *   meta->token_slot before waiting (it sorts while the previous kernel
+ *   drains and writes its outputs after the wait): write token_slot with a
+ *   copy, or with a kernel that has written it before it triggers its
+ *   dependents (any kernel launched without programmatic dependent launch).
  * - Grid sizes depend only on host-known bounds (num_tokens, num_slots,
  *   shapes), never on device data, so a sequence of calls can be captured in
  *   a CUDA graph once it has run eagerly once.

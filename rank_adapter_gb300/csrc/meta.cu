@@ -87,8 +87,10 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_meta_kernel(MetaArgs a) {
   __shared__ int tmp[7 * kWarps];
   __shared__ int s_bad;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  pdl_wait();
-  pdl_trigger();
+  // Everything up to the merged scan reads only token_slot (complete when
+  // this call was enqueued) and writes only shared memory, so it runs before
+  // the wait, beside the tail of the previous kernel; the outputs, which
+  // earlier kernels may still be reading, are written after it.
 
   for (int i = tid; i < kWarps * hs; i += kThreads) hist[i] = 0;
   if (tid == 0) s_bad = 0;
@@ -150,13 +152,17 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_meta_kernel(MetaArgs a) {
 
   int32_t *W = a.work;
   if (tid < S) {
-    W[WorkLists::slot_rec(S, kListAll) + tid] = lora ? ex[2] : -1;
-    W[WorkLists::slot_rec(S, kListSmall) + tid] = small ? ex[3] : -1;
-    W[WorkLists::slot_rec(S, kListLarge) + tid] = large ? ex[4] : -1;
     base_s[tid] = base;
     rec_a[tid] = lora ? WorkLists::list(S, kListAll) + ex[2] * R : -1;
     rec_k[tid] = small ? WorkLists::list(S, kListSmall) + ex[3] * R
                : large ? WorkLists::list(S, kListLarge) + ex[4] * R : -1;
+  }
+  pdl_wait();
+  pdl_trigger();
+  if (tid < S) {
+    W[WorkLists::slot_rec(S, kListAll) + tid] = lora ? ex[2] : -1;
+    W[WorkLists::slot_rec(S, kListSmall) + tid] = small ? ex[3] : -1;
+    W[WorkLists::slot_rec(S, kListLarge) + tid] = large ? ex[4] : -1;
   }
   if (present) {
     a.seg_slot[seg_idx] = tid;
