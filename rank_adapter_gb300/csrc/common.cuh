@@ -180,12 +180,16 @@ struct MetaView {
 // * every slot write is followed by a fence kernel that waits for it and
 //   never triggers early, so the slot table (A, B, ranks, scales) is complete
 //   and visible whenever a later kernel starts;
-// * other kernels trigger their successor only after their own wait, so when
-//   a kernel starts, everything older than its immediate predecessor is
-//   complete;
+// * every kernel waits before it exits, so a kernel's completion implies the
+//   completion of everything before it on the stream;
+// * the metadata kernel triggers its successor at once (it only sorts in
+//   shared memory before its wait); the other kernels trigger only after
+//   their own wait, so when a kernel other than the metadata kernel's
+//   immediate successor starts, everything older than its immediate
+//   predecessor is complete;
 // * a kernel reads before its wait only the slot table, and (the expand when
-//   launched right behind its own shrink) the metadata that is two launches
-//   old.
+//   launched behind this library's shrink, itself behind the metadata
+//   kernel) the metadata, which is then complete.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 

@@ -90,7 +90,10 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_meta_kernel(MetaArgs a) {
   // Everything up to the merged scan reads only token_slot (complete when
   // this call was enqueued) and writes only shared memory, so it runs before
   // the wait, beside the tail of the previous kernel; the outputs, which
-  // earlier kernels may still be reading, are written after it.
+  // earlier kernels may still be reading, are written after it. The
+  // successor is released at once: before its own wait it reads only the
+  // slot table (a shrink starts streaming its A chunk).
+  pdl_trigger();
 
   for (int i = tid; i < kWarps * hs; i += kThreads) hist[i] = 0;
   if (tid == 0) s_bad = 0;
@@ -158,7 +161,6 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_meta_kernel(MetaArgs a) {
                : large ? WorkLists::list(S, kListLarge) + ex[4] * R : -1;
   }
   pdl_wait();
-  pdl_trigger();
   if (tid < S) {
     W[WorkLists::slot_rec(S, kListAll) + tid] = lora ? ex[2] : -1;
     W[WorkLists::slot_rec(S, kListSmall) + tid] = small ? ex[3] : -1;
