@@ -183,13 +183,14 @@ struct MetaView {
 // * every kernel waits before it exits, so a kernel's completion implies the
 //   completion of everything before it on the stream;
 // * the metadata kernel triggers its successor at once (it only sorts in
-//   shared memory before its wait); the other kernels trigger only after
-//   their own wait, so when a kernel other than the metadata kernel's
-//   immediate successor starts, everything older than its immediate
-//   predecessor is complete;
-// * a kernel reads before its wait only the slot table, and (the expand when
-//   launched behind this library's shrink, itself behind the metadata
-//   kernel) the metadata, which is then complete.
+//   shared memory before its wait); an SGMV kernel launched right behind
+//   this library's BGMV kernel of the same call triggers at once too and
+//   waits just before it exits (the families touch disjoint rows and
+//   workspace parts, and everything older than the BGMV kernel is complete
+//   when it starts); every other kernel triggers only after its own wait;
+// * apart from those SGMV kernels, a kernel reads before its wait only the
+//   slot table, and (the expand launched behind this library's shrink) the
+//   metadata, which is then complete.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
@@ -257,12 +258,14 @@ cudaError_t launch_embed_shrink(const lora_layer_desc &d, const MetaView &mv, co
 // SGMV family (sgmv.cu, tcgen05). part: split partials, sgmv_workspace_bytes() bytes.
 bool sgmv_supported();
 size_t sgmv_workspace_bytes(const lora_layer_desc &d, int max_tokens);
+// behind: launched right behind this library's BGMV kernel(s) of the same
+// call over the other segments (the kernel then works before its wait).
 cudaError_t launch_sgmv_shrink(const lora_layer_desc &d, const MetaView &mv, ListSel sel, const void *x,
-                               int64_t ldx, float *part, cudaStream_t st);
+                               int64_t ldx, float *part, cudaStream_t st, bool behind = false);
 cudaError_t launch_sgmv_reduce(const lora_layer_desc &d, const MetaView &mv, ListSel sel, const float *part,
                                float *buf, cudaStream_t st);
 // u_parts: u_src holds the shrink's split partials (else the u buffer [n_slices, T, r_max]).
 cudaError_t launch_sgmv_expand(const lora_layer_desc &d, const MetaView &mv, ListSel sel, const float *u_src,
-                               int u_parts, void *y, int64_t ldy, int y_dtype, cudaStream_t st);
+                               int u_parts, void *y, int64_t ldy, int y_dtype, cudaStream_t st, bool behind = false);
 
 }  // namespace ra

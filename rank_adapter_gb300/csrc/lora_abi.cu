@@ -225,7 +225,7 @@ int lora_shrink(const lora_layer_desc *desc, const lora_meta *meta, const void *
     st = cuda_status(ra::launch_bgmv_shrink(*desc, mv, ra::kListSmall, x, ldx, buf, wb, s));
     if (st != LORA_OK) return st;
   }
-  st = cuda_status(ra::launch_sgmv_shrink(*desc, mv, sel, x, ldx, wsg, s));
+  st = cuda_status(ra::launch_sgmv_shrink(*desc, mv, sel, x, ldx, wsg, s, p.split));
   if (st != LORA_OK) return st;
   return cuda_status(ra::launch_sgmv_reduce(*desc, mv, sel, wsg, buf, s));
 }
@@ -257,7 +257,7 @@ int lora_expand(const lora_layer_desc *desc, const lora_meta *meta, const float 
     if (st != LORA_OK) return st;
   }
   return cuda_status(ra::launch_sgmv_expand(*desc, mv, p.split ? ra::kListLarge : ra::kListAll, buf, 0, y, ldy,
-                                            y_dtype, s));
+                                            y_dtype, s, p.split));
 }
 
 int lora_apply(const lora_layer_desc *desc, const lora_meta *meta, const void *x, int64_t ldx, float *buf,
@@ -297,7 +297,7 @@ int lora_apply(const lora_layer_desc *desc, const lora_meta *meta, const void *x
     st = cuda_status(ra::launch_bgmv_apply_shrink(*desc, mv, ra::kListSmall, x, ldx, buf, wb, s));
     if (st != LORA_OK) return st;
   }
-  st = cuda_status(ra::launch_sgmv_shrink(*desc, mv, sel, x, ldx, wsg, s));
+  st = cuda_status(ra::launch_sgmv_shrink(*desc, mv, sel, x, ldx, wsg, s, p.split));
   if (st != LORA_OK) return st;
   if (buf != nullptr) {
     st = cuda_status(ra::launch_sgmv_reduce(*desc, mv, sel, wsg, buf, s));
@@ -307,7 +307,7 @@ int lora_apply(const lora_layer_desc *desc, const lora_meta *meta, const void *x
     st = cuda_status(ra::launch_bgmv_apply_expand(*desc, mv, ra::kListSmall, wb, y, ldy, y_dtype, s));
     if (st != LORA_OK) return st;
   }
-  return cuda_status(ra::launch_sgmv_expand(*desc, mv, sel, wsg, 1, y, ldy, y_dtype, s));
+  return cuda_status(ra::launch_sgmv_expand(*desc, mv, sel, wsg, 1, y, ldy, y_dtype, s, p.split));
 }
 
 int lora_query_status(const lora_meta *meta, int32_t *out, lora_stream_t stream) {

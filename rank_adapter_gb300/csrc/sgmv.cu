@@ -336,10 +336,25 @@ struct SgShrinkArgs {
   uint32_t w_layout;          // its swizzle
   int stages, lag, stage_bytes, w_bytes;
   int acc_cols, n_acc, tmem_cols;
+  int behind;                 // launched behind this library's BGMV kernel of the same call (see sg_enter)
 };
 
 constexpr int kShrinkProducers = 128;  // warps 0-3
 constexpr int kShrinkThreads = 288;    // + epilogue warps 4-7 + MMA warp 8
+
+// Entry and exit of an SGMV kernel. Launched behind this library's BGMV
+// kernel of the same call (`behind`), it starts work at once: everything
+// older than that kernel is complete when it starts (the BGMV kernel releases
+// its successor only after its own wait), the two families touch disjoint
+// rows and workspace parts, and it waits just before it exits, so its
+// completion still implies the BGMV kernel's. Otherwise it waits first.
+__device__ __forceinline__ void sg_enter(int behind) {
+  if (!behind) pdl_wait();
+  pdl_trigger();
+}
+__device__ __forceinline__ void sg_exit(int behind) {
+  if (behind) pdl_wait();
+}
 
 __global__ void __launch_bounds__(kShrinkThreads, 1)
     sgmv_shrink_kernel(const __grid_constant__ SgMaps maps, const SgShrinkArgs a) {
@@ -364,8 +379,7 @@ __global__ void __launch_bounds__(kShrinkThreads, 1)
     mbar_init(fin, 1);
     fence_mbar_init();
   }
-  pdl_wait();
-  pdl_trigger();
+  sg_enter(a.behind);
   if (warp == 8) tmem_alloc(tslot, (uint32_t)a.tmem_cols);
   const int n_tiles = a.work[a.L.hdr_tiles];
   const int n_list = a.work[a.L.hdr_segs];
@@ -530,6 +544,7 @@ __global__ void __launch_bounds__(kShrinkThreads, 1)
     tc_after_sync();
     tmem_free(tmem, (uint32_t)a.tmem_cols);
   }
+  sg_exit(a.behind);
 }
 
 // ------------------------------------------------------------------ u rows (expand and reduce)
@@ -680,6 +695,7 @@ struct SgExpandArgs {
   int nb_start[LORA_MAX_SLICES + 1];  // column blocks per slice (cumulative)
   int nk;                             // 64-wide K regions of the u operand (1 or 2)
   int b_stages, y_stages, b_bytes;
+  int behind;                         // launched behind this library's BGMV kernel of the same call
 };
 
 struct SgExpandMaps {
@@ -814,8 +830,7 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
     mbar_init(fin, 1);
     fence_mbar_init();
   }
-  pdl_wait();
-  pdl_trigger();
+  sg_enter(a.behind);
   constexpr uint32_t kTmemCols = kExpandAcc * kN;
   static_assert(kTmemCols <= 512, "accumulators exceed tensor memory");
   if (warp == kEpiWarps + 5) tmem_alloc(tslot, kTmemCols);
@@ -1092,6 +1107,7 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
     tc_after_sync();
     tmem_free(tmem, kTmemCols);
   }
+  sg_exit(a.behind);
 }
 
 // ------------------------------------------------------------------ host side
@@ -1195,7 +1211,7 @@ size_t sgmv_workspace_bytes(const lora_layer_desc &d, int max_tokens) {
 }
 
 cudaError_t launch_sgmv_shrink(const lora_layer_desc &d, const MetaView &mv, ListSel sel, const void *x, int64_t ldx,
-                               float *part, cudaStream_t st) {
+                               float *part, cudaStream_t st, bool behind) {
   if (mv.num_tokens <= 0 || mv.num_slots <= 1) return cudaSuccess;
   SgMaps maps;
   memset(&maps, 0, sizeof(maps));
@@ -1216,6 +1232,7 @@ cudaError_t launch_sgmv_shrink(const lora_layer_desc &d, const MetaView &mv, Lis
   a.x = static_cast<const __nv_bfloat16 *>(x);
   a.ldx = ldx;
   a.part = part;
+  a.behind = behind ? 1 : 0;
   a.work = mv.work;
   a.sorted_rows = mv.sorted_rows;
   a.err = const_cast<int32_t *>(mv.work) + WorkLists::kErrWord;
@@ -1266,7 +1283,7 @@ cudaError_t launch_sgmv_reduce(const lora_layer_desc &d, const MetaView &mv, Lis
 }
 
 cudaError_t launch_sgmv_expand(const lora_layer_desc &d, const MetaView &mv, ListSel sel, const float *u_src,
-                               int u_parts, void *y, int64_t ldy, int y_dtype, cudaStream_t st) {
+                               int u_parts, void *y, int64_t ldy, int y_dtype, cudaStream_t st, bool behind) {
   if (mv.num_tokens <= 0 || mv.num_slots <= 1) return cudaSuccess;
   const int kN = y_dtype == LORA_BF16 ? YCols<__nv_bfloat16>::kN : YCols<float>::kN;
   SgExpandMaps maps;
@@ -1285,6 +1302,7 @@ cudaError_t launch_sgmv_expand(const lora_layer_desc &d, const MetaView &mv, Lis
                      y_dtype == LORA_BF16 ? 64u : 32u, 32u);
   if (em != cudaSuccess) return em;
   SgExpandArgs a{};
+  a.behind = behind ? 1 : 0;
   a.u.src = u_src;
   a.u.parts = u_parts;
   a.u.n_slices = d.n_slices;
