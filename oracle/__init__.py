@@ -17,3 +17,4 @@ from .lora_oracle import (  # noqa: F401
     prepare_meta, shrink_requests, expand_requests, apply_requests, adapters_f64,
     requests_of_token_slots, embed_requests,
 )
+from .moe_oracle import moe_pair_slots, gathered_apply, moe_lora_w13, moe_lora_w2  # noqa: F401
