@@ -102,7 +102,8 @@ typedef enum { LORA_AUTO = 0, LORA_BGMV = 1, LORA_SGMV = 2 } lora_kind;
  * Slot 0 is reserved (kept zero, rank 0). Constraints: dtype in lora_dtype;
  * 1 <= n_slices <= LORA_MAX_SLICES; d_in and every out_sizes[s] positive
  * multiples of 8; r_max a power of two in [8, LORA_MAX_RANK];
- * 1 <= num_slots <= LORA_MAX_NUM_SLOTS. The library only reads this struct.
+ * 1 <= num_slots <= LORA_MAX_NUM_SLOTS; x_row_div >= 0. The library only
+ * reads this struct.
  */
 typedef struct {
   int32_t dtype;
@@ -115,6 +116,10 @@ typedef struct {
   void *B[LORA_MAX_SLICES];
   int32_t *slot_rank;
   float *slot_scale;
+  int32_t x_row_div;  /* LoRA row i of a call reads x row i / x_row_div (0 or 1: row i).
+                         A mixture-of-experts w13 layer, whose LoRA rows are the
+                         (token, choice) pairs of lora_moe_pair_slots, sets topk:
+                         a token's hidden state serves its top-k pairs. */
 } lora_layer_desc;
 
 /*
@@ -251,6 +256,41 @@ size_t lora_workspace_bytes(const lora_layer_desc *desc, int32_t max_tokens, int
 
 /* Bytes the meta->tiles work-list buffer needs for a table of num_slots slots. */
 size_t lora_meta_tiles_bytes(int32_t num_slots);
+
+/*
+ * Mixture-of-experts LoRA (page "vLLM 源码完全拆解(十八): 多 LoRA 服务", section
+ * "MoE 的 LoRA:按专家挂载、融合 kernel 与 EP 切片"): every expert has its own
+ * low-rank pair per adapter, applied after w13 (before the activation) and
+ * after w2 (before the top-k sum). This call gives each (token, choice) pair,
+ * token-major (pair p = t * topk + k), the composite slot of its (adapter,
+ * local expert):
+ *   pair_slot[p] = 1 + (a - 1) * local_experts + expert_map[e]
+ * with a = token_slot[t], e = topk_ids[t * topk + k]; 0 (no delta) when a is 0
+ * or expert_map[e] < 0 (an expert another expert-parallel rank holds); -1
+ * (counted as a bad id by lora_prepare_meta) when a is outside [0, num_loras],
+ * e outside [0, num_experts) or expert_map[e] >= local_experts. expert_map
+ * NULL means every expert is local (e itself). The composite table then has
+ * 1 + num_loras * local_experts slots: slot 1 + (a - 1) * local_experts + j
+ * holds adapter a's pair for local expert j. lora_prepare_meta over pair_slot
+ * groups the pairs by (adapter, expert), which is what the pages'
+ * moe_lora_align_block_size does; the w13 application is then lora_apply
+ * (or shrink / expand) on the w13 table with x_row_div = topk and the token
+ * rows as x, the w2 application the same on the w2 table with the pairs'
+ * rows, both with the pairs' metadata.
+ *   token_slot [num_tokens], topk_ids [num_tokens * topk], expert_map
+ *   [num_experts] (or NULL), pair_slot [num_tokens * topk]: device int32,
+ *   4-byte aligned, caller-owned. It waits for the previous kernel before it
+ *   reads and releases its successor only when done (lora_prepare_meta reads
+ *   pair_slot before waiting).
+ * Errors: a null array (other than expert_map) -> LORA_EINVAL; num_tokens
+ * outside [0, LORA_MAX_TOKENS / topk], topk outside [1, 64], num_loras < 0,
+ * num_experts < 1, local_experts outside [1, num_experts], or a composite
+ * table above LORA_MAX_NUM_SLOTS slots -> LORA_ERANGE; misaligned arrays ->
+ * LORA_EALIGN. num_tokens == 0 is a no-op.
+ */
+int lora_moe_pair_slots(const int32_t *token_slot, const int32_t *topk_ids, int32_t num_tokens, int32_t topk,
+                        int32_t num_loras, int32_t num_experts, int32_t local_experts, const int32_t *expert_map,
+                        int32_t *pair_slot, lora_stream_t stream);
 
 /*
  * Synchronise `stream`, copy meta->status to *out (host) and return

@@ -28,6 +28,7 @@ __all__ = [
     "LayerDesc", "Meta", "LoraError", "lib_path", "exported_symbols",
     "lora_set_slot", "lora_reset_slot", "lora_prepare_meta", "lora_shrink", "lora_expand", "lora_apply",
     "lora_shrink_noalloc", "lora_noalloc_scratch_bytes", "lora_embed_shrink", "embed_shrink",
+    "lora_moe_pair_slots", "moe_pair_slots",
     "lora_workspace_bytes", "lora_meta_tiles_bytes", "lora_query_status", "lora_strerror",
     "lora_last_cuda_error", "lora_launch_count", "SlotTable", "TokenMeta", "shrink", "expand", "apply", "workspace", "check",
 ]
@@ -68,7 +69,7 @@ class LayerDesc(ctypes.Structure):
         ("dtype", _i32), ("d_in", _i32), ("n_slices", _i32),
         ("out_sizes", _i32 * LORA_MAX_SLICES), ("num_slots", _i32), ("r_max", _i32),
         ("A", _vp * LORA_MAX_SLICES), ("B", _vp * LORA_MAX_SLICES),
-        ("slot_rank", _vp), ("slot_scale", _vp),
+        ("slot_rank", _vp), ("slot_scale", _vp), ("x_row_div", _i32),
     ]
 
 
@@ -97,6 +98,7 @@ _sig = {
     "lora_meta_tiles_bytes": (ctypes.c_size_t, [_i32]),
     "lora_query_status": (_i32, [_P(Meta), _P(_i32), _vp]),
     "lora_embed_shrink": (_i32, [_P(LayerDesc), _P(Meta), _vp, _vp, _vp]),
+    "lora_moe_pair_slots": (_i32, [_vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp]),
     "lora_strerror": (ctypes.c_char_p, [_i32]),
     "lora_last_cuda_error": (_i32, []),
     "lora_launch_count": (ctypes.c_uint64, []),
@@ -176,6 +178,13 @@ def lora_embed_shrink(desc: LayerDesc, meta: Meta, token_id: int, buf: int, stre
     return _lib.lora_embed_shrink(ctypes.byref(desc), ctypes.byref(meta), token_id, buf, _stream(stream))
 
 
+def lora_moe_pair_slots(token_slot: int, topk_ids: int, num_tokens: int, topk: int, num_loras: int,
+                        num_experts: int, local_experts: int, expert_map: int, pair_slot: int, stream=None) -> int:
+    """Composite (adapter, local expert) slot of every (token, choice) pair (see the header)."""
+    return _lib.lora_moe_pair_slots(token_slot, topk_ids, num_tokens, topk, num_loras, num_experts, local_experts,
+                                    expert_map, pair_slot, _stream(stream))
+
+
 def lora_shrink_noalloc(desc: LayerDesc, meta: Meta, x: int, ldx: int, buf: int, stream=None) -> int:
     """lora_shrink (BGMV family) with its scratch in the library's fixed device array; allocates nothing."""
     return _lib.lora_shrink_noalloc(ctypes.byref(desc), ctypes.byref(meta), x, ldx, buf, _stream(stream))
@@ -229,7 +238,7 @@ class SlotTable:
     """
 
     def __init__(self, d_in: int, out_sizes: Sequence[int], num_slots: int, r_max: int,
-                 dtype: int = LORA_BF16, device="cuda"):
+                 dtype: int = LORA_BF16, device="cuda", x_row_div: int = 1):
         import torch
         td = _torch_dtype(dtype)
         self.dtype, self.d_in, self.out_sizes = dtype, d_in, list(out_sizes)
@@ -246,6 +255,7 @@ class SlotTable:
             d.B[i] = self.B[i].data_ptr()
         d.num_slots, d.r_max = num_slots, r_max
         d.slot_rank, d.slot_scale = self.slot_rank.data_ptr(), self.slot_scale.data_ptr()
+        d.x_row_div = x_row_div   # LoRA row i reads x row i // x_row_div (an MoE w13 layer: topk)
         self.desc = d
 
     @property
@@ -344,6 +354,20 @@ def shrink(table: SlotTable, meta: TokenMeta, x, buf, kind: int = LORA_AUTO, str
 def embed_shrink(table: SlotTable, meta: TokenMeta, token_id, buf, stream=None) -> None:
     """buf[0, t, :] = scale * A[slot t][token_id[t], :] for LoRA tokens (see lora_embed_shrink)."""
     check(lora_embed_shrink(table.desc, meta.c, token_id.data_ptr(), buf.data_ptr(), stream), "lora_embed_shrink")
+
+
+def moe_pair_slots(token_slot, topk_ids, num_loras: int, num_experts: int, local_experts: int, expert_map=None,
+                   pair_slot=None, stream=None):
+    """pair_slot [T * topk] int32 (allocated when omitted) for token_slot [T] and topk_ids [T, topk]."""
+    import torch
+    T, topk = int(topk_ids.shape[0]), int(topk_ids.shape[1])
+    if pair_slot is None:
+        pair_slot = torch.empty(T * topk, dtype=torch.int32, device=topk_ids.device)
+    check(lora_moe_pair_slots(token_slot.data_ptr() if T else 0, topk_ids.data_ptr() if T else 0, T, topk,
+                              num_loras, num_experts, local_experts,
+                              expert_map.data_ptr() if expert_map is not None else 0,
+                              pair_slot.data_ptr() if T else 0, stream), "lora_moe_pair_slots")
+    return pair_slot
 
 
 def expand(table: SlotTable, meta: TokenMeta, buf, y, kind: int = LORA_AUTO, stream=None) -> None:

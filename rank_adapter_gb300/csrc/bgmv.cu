@@ -66,6 +66,7 @@ struct Geo {
 struct BgmvArgs {
   const void *x;
   int64_t ldx;
+  int x_div;            // LoRA row i reads x row i / x_div
   const void *A[LORA_MAX_SLICES];
   const void *B[LORA_MAX_SLICES];
   float *buf;           // shrink (to_parts == 0) and reduce: receives u rows
@@ -291,7 +292,8 @@ __device__ __forceinline__ void shrink_tiles(const BgmvArgs &a, unsigned char *s
       const int upr = nr / VEC;
       TW *xs = stX(s);
       for (int t = warp; t < nt; t += kSWarps) {
-        const TW *xsrc = x + (int64_t)rows[(tile * kTT + t) % kRowsWin] * a.ldx + k0 + r0;
+        const int row = rows[(tile * kTT + t) % kRowsWin];
+        const TW *xsrc = x + (int64_t)(a.x_div == 1 ? row : row / a.x_div) * a.ldx + k0 + r0;
         for (int c = tid & 31; c < upr; c += 32) cp_async16(xs + t * g.sc + c * VEC, xsrc + c * VEC);
       }
     }
@@ -727,6 +729,7 @@ void fill_common(BgmvArgs &a, const lora_layer_desc &d, const MetaView &mv, List
                       (sel == kListSmall && mv.num_tokens >= S1 && mv.num_tokens <= LORA_SGMV_MIN_ROWS * S1)
                   ? 1 : 0;
   a.small_only = sel == kListSmall ? 1 : 0;
+  a.x_div = d.x_row_div > 1 ? d.x_row_div : 1;
   a.n_slices = d.n_slices;
   a.max_items = std::min(mv.num_slots - 1, mv.num_tokens);
   a.mv = mv;

@@ -253,6 +253,10 @@ cudaError_t launch_bgmv_apply_shrink(const lora_layer_desc &d, const MetaView &m
 cudaError_t launch_bgmv_apply_expand(const lora_layer_desc &d, const MetaView &mv, ListSel sel, const float *ws,
                                      void *y, int64_t ldy, int y_dtype, cudaStream_t st);
 // Embedding lookup (embed.cu): buf rows of the one-hot token ids, see lora_embed_shrink.
+// Mixture-of-experts (moe.cu): composite slot of every (token, choice) pair.
+cudaError_t launch_moe_pair_slots(const int32_t *token_slot, const int32_t *topk_ids, int T, int topk, int num_loras,
+                                  int num_experts, int local_experts, const int32_t *expert_map, int32_t *pair_slot,
+                                  cudaStream_t st);
 cudaError_t launch_embed_shrink(const lora_layer_desc &d, const MetaView &mv, const int32_t *token_slot,
                                 const int32_t *token_id, float *buf, cudaStream_t st);
 // SGMV family (sgmv.cu, tcgen05). part: split partials, sgmv_workspace_bytes() bytes.

@@ -68,6 +68,7 @@ int check_desc(const lora_layer_desc *d) {
   if (d->slot_rank == nullptr || d->slot_scale == nullptr) return LORA_EINVAL;
   if ((reinterpret_cast<uintptr_t>(d->slot_rank) & 3u) || (reinterpret_cast<uintptr_t>(d->slot_scale) & 3u))
     return LORA_EALIGN;
+  if (d->x_row_div < 0) return LORA_EINVAL;
   return LORA_OK;
 }
 
@@ -339,6 +340,23 @@ int lora_embed_shrink(const lora_layer_desc *desc, const lora_meta *meta, const 
   if (!aligned16(buf) || reinterpret_cast<uintptr_t>(token_id) % sizeof(int32_t) != 0) return LORA_EALIGN;
   return cuda_status(ra::launch_embed_shrink(*desc, view_of(meta), meta->token_slot, token_id, buf,
                                              (cudaStream_t)stream));
+}
+
+int lora_moe_pair_slots(const int32_t *token_slot, const int32_t *topk_ids, int32_t num_tokens, int32_t topk,
+                        int32_t num_loras, int32_t num_experts, int32_t local_experts, const int32_t *expert_map,
+                        int32_t *pair_slot, lora_stream_t stream) {
+  clear_stale_error();
+  if (topk < 1 || topk > 64 || num_tokens < 0 || (int64_t)num_tokens * topk > LORA_MAX_TOKENS) return LORA_ERANGE;
+  if (num_loras < 0 || num_experts < 1 || local_experts < 1 || local_experts > num_experts) return LORA_ERANGE;
+  if (1 + (int64_t)num_loras * local_experts > LORA_MAX_NUM_SLOTS) return LORA_ERANGE;
+  if (num_tokens == 0) return LORA_OK;
+  if (token_slot == nullptr || topk_ids == nullptr || pair_slot == nullptr) return LORA_EINVAL;
+  auto misaligned = [](const void *p) { return reinterpret_cast<uintptr_t>(p) % sizeof(int32_t) != 0; };
+  if (misaligned(token_slot) || misaligned(topk_ids) || misaligned(pair_slot) ||
+      (expert_map != nullptr && misaligned(expert_map)))
+    return LORA_EALIGN;
+  return cuda_status(ra::launch_moe_pair_slots(token_slot, topk_ids, num_tokens, topk, num_loras, num_experts,
+                                               local_experts, expert_map, pair_slot, (cudaStream_t)stream));
 }
 
 }  // extern "C"

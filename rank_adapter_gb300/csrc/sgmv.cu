@@ -337,6 +337,7 @@ struct SgShrinkArgs {
   int stages, lag, stage_bytes, w_bytes;
   int acc_cols, n_acc, tmem_cols;
   int behind;                 // launched behind this library's BGMV kernel of the same call (see sg_enter)
+  int x_div;                  // LoRA row i reads x row i / x_div (> 1: x rows are gathered, never tiled)
 };
 
 constexpr int kShrinkProducers = 128;  // warps 0-3
@@ -413,12 +414,13 @@ __global__ void __launch_bounds__(kShrinkThreads, 1)
       // A tile of consecutive tokens comes by one TMA tile copy per K block,
       // already in the swizzled operand layout; others are gathered.
       const int tok0 = pi.tok0;
-      const bool contiguous = pi.contiguous != 0;
+      const bool contiguous = pi.contiguous != 0 && a.x_div == 1;
       int tok[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int r = (tid >> 3) + 16 * i;
         tok[i] = (!contiguous && r < ti.rows) ? a.sorted_rows[ti.pos0 + r] : -1;
+        if (a.x_div != 1 && tok[i] >= 0) tok[i] /= a.x_div;  // the x row of this LoRA row
       }
       const int kb0 = (int)(max(u0, (int64_t)tile * a.nb) - (int64_t)tile * a.nb);
       const int kb1 = (int)(min(u1, (int64_t)(tile + 1) * a.nb) - (int64_t)tile * a.nb);
@@ -1225,8 +1227,10 @@ cudaError_t launch_sgmv_shrink(const lora_layer_desc &d, const MetaView &mv, Lis
                              (uint32_t)a.box_n, (uint32_t)kKB, sw);
     if (e != cudaSuccess) return e;
   }
+  a.x_div = d.x_row_div > 1 ? d.x_row_div : 1;
   {
-    cudaError_t e = make_rows_map(&maps.x, x, true, (uint64_t)d.d_in, (uint64_t)mv.num_tokens, ldx, kKB);
+    const uint64_t x_rows = ((uint64_t)mv.num_tokens + a.x_div - 1) / a.x_div;
+    cudaError_t e = make_rows_map(&maps.x, x, true, (uint64_t)d.d_in, x_rows, ldx, kKB);
     if (e != cudaSuccess) return e;
   }
   a.x = static_cast<const __nv_bfloat16 *>(x);

@@ -127,6 +127,24 @@ def test_embed_shrink_validation(ra):
     assert ra.lora_embed_shrink(one, _meta(ra, T=0), 0, 0, 0) == ra.LORA_OK          # T = 0: no-op
 
 
+def test_moe_pair_slots_validation(ra):
+    f = lambda *a: ra.lora_moe_pair_slots(*a, 0)   # noqa: E731
+    P = 0x1000
+    assert f(0, 0, 0, 2, 1, 4, 4, 0, 0) == ra.LORA_OK                  # no tokens: no-op
+    assert f(P, P, 5, 0, 1, 4, 4, 0, P) == ra.LORA_ERANGE              # topk < 1
+    assert f(P, P, 5, 65, 1, 4, 4, 0, P) == ra.LORA_ERANGE             # topk > 64
+    assert f(P, P, 5, 2, 1, 4, 5, 0, P) == ra.LORA_ERANGE              # more local experts than experts
+    assert f(P, P, 5, 2, 2000, 4, 4, 0, P) == ra.LORA_ERANGE           # composite table too large
+    assert f(P, P, 5, 2, -1, 4, 4, 0, P) == ra.LORA_ERANGE
+    assert f(0, P, 5, 2, 1, 4, 4, 0, P) == ra.LORA_EINVAL              # no token slots
+    assert f(P, P, 5, 2, 1, 4, 4, 0, 0) == ra.LORA_EINVAL              # no output
+    assert f(P + 2, P, 5, 2, 1, 4, 4, 0, P) == ra.LORA_EALIGN
+    assert f(P, P, 5, 2, 1, 4, 4, P + 1, P) == ra.LORA_EALIGN          # expert map misaligned
+    d = _desc(ra)
+    d.x_row_div = -1
+    assert ra.lora_reset_slot(d, 1, 0) == ra.LORA_EINVAL
+
+
 def test_shrink_expand_validation(ra):
     d, m = _desc(ra), _meta(ra)
     assert ra.lora_shrink(d, m, 0x5000, 64, 0x6000, 9, 0, 0, 0) == ra.LORA_EINVAL       # kind

@@ -24,6 +24,13 @@ Workloads (sizes follow the Llama-3-8B-shaped projections the pages use):
                     多 LoRA 服务", section "embedding 的 LoRA 是一个查表增量"):
                     vocab 128256 -> hidden 4096, r=16, 64 slots, 256 decode
                     tokens with ids uniform over the vocabulary, 10% slot 0.
+* ``moe_decode``    one mixture-of-experts layer's LoRA (page "vLLM 源码完全拆解
+                    (十八): 多 LoRA 服务", section "MoE 的 LoRA:按专家挂载、融合 kernel
+                    与 EP 切片"), shaped like its DeepSeek-V3 memory example:
+                    hidden 7168, expert intermediate 2048, 256 experts with
+                    8-way expert parallelism (32 local, rank 0), top-8 routing,
+                    r=64, 4 adapters, 256 decode tokens (10% slot 0); the w13
+                    (gate, up) and w2 applications over the (token, choice) pairs.
 * ``logits_lm_head`` the lm_head LoRA on the rows sampled this step (page
                     "vLLM 源码完全拆解(十八): 多 LoRA 服务", section
                     "lm_head / logits"): hidden 4096 -> vocab 128256, r=16,
@@ -43,11 +50,11 @@ import numpy as np
 __all__ = [
     "bf16_bits_from_f32", "bf16_bits_to_f32", "Adapter", "Instance",
     "make_instance", "toy_page_instance", "zipf_probs", "full_decode_groups",
-    "CONFIG_NAMES", "EXTRA_NAMES", "split_requests", "sampled_rows",
+    "CONFIG_NAMES", "EXTRA_NAMES", "split_requests", "sampled_rows", "MoEInstance", "make_moe_instance",
 ]
 
 CONFIG_NAMES = ("toy_fp32", "decode_qkv", "prefill_gate_up", "mixed_o_proj", "full_decode")
-EXTRA_NAMES = ("logits_lm_head", "embed_lookup")   # widening beyond the five configurations
+EXTRA_NAMES = ("logits_lm_head", "embed_lookup", "moe_decode")   # widening beyond the five configurations
 
 _CHUNK = 1 << 24
 
@@ -402,3 +409,93 @@ def toy_page_instance():
     x = torch.randn(sum(lengths), 256, generator=g)
     return dict(W=W.numpy(), A=A.numpy(), B=B.numpy(), x=x.numpy(), lengths=lengths,
                 adapters=adapters, scale=2.0)
+
+
+@dataclass
+class MoEInstance:
+    """One mixture-of-experts layer's LoRA inputs.
+
+    ``w13`` and ``w2`` are the two applications as dense-layer instances over
+    the (token, choice) pairs (p = t * topk + k): their slot tables hold the
+    composite (adapter, local expert) slots 1 + (a - 1) * local_experts + j,
+    their requests are the pairs (one row each, slot = the pair's composite
+    slot), ``w2.x`` is the per-pair input h2 and ``w2.y_in`` / ``w13.y_in``
+    the pairs' base outputs. ``w13.x`` holds the token rows [T, hidden]: the
+    w13 LoRA row of pair p reads token row p // topk.
+    """
+    name: str
+    hidden: int
+    inter: int
+    num_experts: int
+    local_experts: int
+    ep_rank: int
+    topk: int
+    num_loras: int
+    token_slot: np.ndarray          # int32 [T]: adapter slot of every token (0 = none)
+    topk_ids: np.ndarray            # int32 [T, topk]: chosen global expert ids
+    expert_map: Optional[np.ndarray]  # int32 [num_experts]: local index or -1 (None: all local)
+    pair_slot: np.ndarray           # int32 [T * topk]: composite slot of every pair
+    w13: Instance
+    w2: Instance
+
+    @property
+    def num_tokens(self) -> int:
+        return int(self.token_slot.size)
+
+
+def make_moe_instance(name: str = "moe_decode", seed: Optional[int] = None, *, num_tokens: Optional[int] = None,
+                      hidden: Optional[int] = None, inter: Optional[int] = None,
+                      num_experts: Optional[int] = None, local_experts: Optional[int] = None, ep_rank: int = 0,
+                      topk: Optional[int] = None, num_loras: Optional[int] = None,
+                      r_max: Optional[int] = None) -> MoEInstance:
+    """A seeded MoE-layer instance; keyword overrides shrink it for tests.
+
+    Tokens: slot 0 with probability 10%, else uniform over adapters 1..num_loras.
+    Routing: each token's topk distinct experts uniform over all experts.
+    Expert parallelism: rank ep_rank holds experts [ep_rank * L, (ep_rank + 1) * L).
+    Weights: A ~ N(0,1)/64, B ~ N(0,1)/16 (seeded windows of a N(0,1) pool),
+    every composite slot rank r_max, scale 1.0; x, h2 and base outputs ~ N(0,1).
+    """
+    if name != "moe_decode":
+        raise ValueError(f"unknown MoE workload {name!r}")
+    rng = np.random.Generator(np.random.PCG64(8 if seed is None else seed))
+    T = num_tokens or 256
+    H, I = hidden or 7168, inter or 2048
+    E = num_experts or 256
+    L = local_experts or 32
+    K = topk or 8
+    NL = num_loras or 4
+    R = r_max or 64
+    dt = "bf16"
+    ts = rng.integers(1, NL + 1, size=T).astype(np.int32)
+    ts[rng.random(T) < 0.10] = 0
+    ids = np.argsort(rng.random((T, E)), axis=1)[:, :K].astype(np.int32)
+    start = ep_rank * L
+    emap = None
+    if L < E:
+        emap = np.full(E, -1, dtype=np.int32)
+        emap[start:start + L] = np.arange(L, dtype=np.int32)
+    # composite slots, restated here from the layout rule (the oracle keeps its own copy)
+    pair = np.zeros(T * K, dtype=np.int32)
+    for t in range(T):
+        for k in range(K):
+            e = int(ids[t, k])
+            el = e - start if start <= e < start + L else -1
+            if ts[t] > 0 and el >= 0:
+                pair[t * K + k] = 1 + (int(ts[t]) - 1) * L + el
+    S = 1 + NL * L
+    pool = _Pool(rng, min(1 << 26, max(1 << 20, 4 * S * R * (2 * H + I + 2 * I + H))), dt)
+    ranks = {k: R for k in range(1, S)}
+    scales = {k: 1.0 for k in range(1, S)}
+    ad13 = _draw_adapters(rng, range(1, S), H, [I, I], ranks, scales, 64.0, 16.0, dt, pool=pool)
+    ad2 = _draw_adapters(rng, range(1, S), I, [H], ranks, scales, 64.0, 16.0, dt, pool=pool)
+    ones = np.ones(T * K, np.int64)
+    x = pool.take((T, H), 1.0)
+    w13 = Instance(name=f"{name}/w13", dtype=dt, d_in=H, out_sizes=[I, I], num_slots=S, r_max=R, adapters=ad13,
+                   req_lengths=ones, req_slots=pair.copy(), x=x, y_in=pool.take((T * K, 2 * I), 1.0),
+                   meta={"x_row_div": K})
+    w2 = Instance(name=f"{name}/w2", dtype=dt, d_in=I, out_sizes=[H], num_slots=S, r_max=R, adapters=ad2,
+                  req_lengths=ones, req_slots=pair.copy(), x=pool.take((T * K, I), 1.0),
+                  y_in=pool.take((T * K, H), 1.0))
+    return MoEInstance(name=name, hidden=H, inter=I, num_experts=E, local_experts=L, ep_rank=ep_rank, topk=K,
+                       num_loras=NL, token_slot=ts, topk_ids=ids, expert_map=emap, pair_slot=pair, w13=w13, w2=w2)
