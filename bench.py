@@ -54,6 +54,9 @@ WORKLOADS = {
                       "256 sampled rows (one per request, 10% slot 0)",
     "embed_lookup": "embedding LoRA: vocab 128256 -> hidden 4096, r=16, 64 slots, 256 decode tokens "
                     "(ids uniform over the vocabulary, 10% slot 0); lookup + expand",
+    "moe_decode": "MoE layer LoRA: hidden 7168, expert inter 2048, 256 experts / EP8 (32 local), top-8, r=64, "
+                  "4 adapters (128 composite slots, ~457 MB), 256 decode tokens (10% slot 0); pair slots + metadata "
+                  "over the 2048 pairs + w13 (gate, up; x rows shared by a token's pairs) + w2",
 }
 
 
@@ -255,7 +258,7 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
-    batch = 512 if args.workload == "full_decode" else make_workload(args.workload).num_tokens
+    batch = {"full_decode": 512, "moe_decode": 256}.get(args.workload) or make_workload(args.workload).num_tokens
     cfg = {"workload": args.workload, "desc": WORKLOADS[args.workload], "global_batch": batch,
            "n_gpus_ignored": args.gpus}
     cpu = run_cpu_baseline(argparse.Namespace(workload=args.workload,
@@ -812,11 +815,210 @@ def run_full_decode(args):
     return 0
 
 
+def moe_algorithmic(m):
+    """Bytes of one MoE-layer step: every active composite slot's w13 and w2 weights once, the token
+    rows x of tokens with a live pair once, h2 of live pairs once, h1 and h3 of live pairs read and
+    written once (bf16), and the routing ints."""
+    import numpy as np
+    live = m.pair_slot > 0
+    active = np.unique(m.pair_slot[live])
+    r = m.w13.r_max
+    w = int(len(active)) * 2 * r * (2 * m.hidden + 2 * m.inter + m.inter + m.hidden)
+    tok = int(np.unique(np.nonzero(live)[0] // m.topk).size)
+    P_L = int(live.sum())
+    act = 2 * tok * m.hidden + 2 * P_L * m.inter + 2 * 2 * P_L * 2 * m.inter + 2 * 2 * P_L * m.hidden
+    ints = 4 * m.num_tokens * (1 + 2 * m.topk)
+    return dict(step_bytes=w + act + ints, T_L=int((m.token_slot > 0).sum()), pairs_live=P_L, active=int(len(active)))
+
+
+def moe_cpu(args):
+    """The oracle on the MoE-layer step (pair slots, metadata, w13, w2); one JSON line."""
+    import numpy as np
+    import oracle
+    import workloads as wl
+    m = wl.make_moe_instance()
+    a13, a2 = oracle.adapters_f64(m.w13), oracle.adapters_f64(m.w2)
+    x = m.w13.to_f32(m.w13.x).astype(np.float64)
+    h1 = m.w13.to_f32(m.w13.y_in).astype(np.float64)
+    h2 = m.w2.to_f32(m.w2.x).astype(np.float64)
+    h3 = m.w2.to_f32(m.w2.y_in).astype(np.float64)
+    S = m.w13.num_slots
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        pair = oracle.moe_pair_slots(m.token_slot, m.topk_ids, m.num_loras, m.num_experts, m.local_experts,
+                                     m.expert_map)
+        oracle.prepare_meta(pair, S)
+        oracle.moe_lora_w13(x, h1, pair, m.topk, a13, m.w13.out_sizes, S)
+        oracle.moe_lora_w2(h2, h3, pair, a2, m.hidden, S)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= args.cpu_seconds:
+            break
+    T_L = int((m.token_slot > 0).sum())
+    print(json.dumps({"value": reps * T_L / el, "seconds": el, "reps": reps, "sec_per_step": el / reps}))
+
+
+def run_moe(args):
+    """One mixture-of-experts layer's LoRA per step: the pairs' composite slots, the metadata over the
+    pairs, the w13 application (x rows shared by a token's top-k pairs) and the w2 application."""
+    import numpy as np
+    import torch
+    import workloads as wl
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    import rank_adapter_gb300 as ra
+    kind = {"auto": ra.LORA_AUTO, "bgmv": ra.LORA_BGMV, "sgmv": ra.LORA_SGMV}[args.kind]
+    m = wl.make_moe_instance(seed=8 + 1000 * rank)
+    alg = moe_algorithmic(m)
+
+    def dev(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
+
+    def table(layer, x_row_div):
+        t = ra.SlotTable(layer.d_in, layer.out_sizes, layer.num_slots, layer.r_max, ra.LORA_BF16,
+                         x_row_div=x_row_div)
+        for k, ad in sorted(layer.adapters.items()):
+            t.set_slot(k, ad.rank, ad.scale, [dev(w) for w in ad.A], [dev(w) for w in ad.B])
+        return t
+
+    t13, t2 = table(m.w13, m.topk), table(m.w2, 1)
+    T, K, S = m.num_tokens, m.topk, m.w13.num_slots
+    P = T * K
+    ts = torch.from_numpy(m.token_slot).cuda()
+    ids = torch.from_numpy(np.ascontiguousarray(m.topk_ids)).cuda()
+    emap = torch.from_numpy(m.expert_map).cuda() if m.expert_map is not None else None
+    x, h1, h2, h3 = dev(m.w13.x), dev(m.w13.y_in), dev(m.w2.x), dev(m.w2.y_in)
+    meta = ra.TokenMeta(P, S)
+    meta.set_num_tokens(P)
+    ws = ra.workspace(max((t13, t2), key=lambda t: ra.lora_workspace_bytes(t.desc, P, kind)), P, kind)
+    ws_ptr, ws_bytes = (ws.data_ptr(), ws.numel() * 4) if ws is not None else (0, 0)
+    torch.cuda.synchronize()
+
+    def step(st):
+        ra.check(ra.lora_moe_pair_slots(ts.data_ptr(), ids.data_ptr(), T, K, m.num_loras, m.num_experts,
+                                        m.local_experts, emap.data_ptr() if emap is not None else 0,
+                                        meta.token_slot.data_ptr(), st), "moe_pair_slots")
+        ra.check(ra.lora_prepare_meta(meta.c, st), "prepare_meta")
+        ra.check(ra.lora_apply(t13.desc, meta.c, x.data_ptr(), x.stride(0), 0, h1.data_ptr(), h1.stride(0),
+                               ra.LORA_BF16, kind, ws_ptr, ws_bytes, st), "apply w13")
+        ra.check(ra.lora_apply(t2.desc, meta.c, h2.data_ptr(), h2.stride(0), 0, h3.data_ptr(), h3.stride(0),
+                               ra.LORA_BF16, kind, ws_ptr, ws_bytes, st), "apply w2")
+
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            step(None)
+    stream.synchronize()
+    n0 = ra.lora_launch_count()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step(None)
+    per_step = ra.lora_launch_count() - n0
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            graph.replay()
+    stream.synchronize()
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    clocks = ClockSampler(vis.split(",")[local].strip() if vis else str(local))
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record()
+        for _ in range(args.steps):
+            graph.replay()
+        e1.record()
+    stream.synchronize()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.stop()
+    elapsed_ms = e0.elapsed_time(e1)
+
+    # End to end: routing, x and the base outputs h1, h2, h3 in from pinned host memory, h1 and h3 out;
+    # each step one CUDA-graph replay of its copies and calls.
+    pin = lambda t: torch.empty_like(t, device="cpu").pin_memory().copy_(t)   # noqa: E731
+    h_in = [(d, pin(d)) for d in (ts, ids, x, h1, h2, h3)]
+    h_out = [(d, torch.empty_like(d, device="cpu").pin_memory()) for d in (h1, h3)]
+    h2d = sum(h.numel() * h.element_size() for _, h in h_in)
+    d2h = sum(h.numel() * h.element_size() for _, h in h_out)
+
+    def e2e_step():
+        for d, h in h_in:
+            d.copy_(h, non_blocking=True)
+        step(None)
+        for d, h in h_out:
+            h.copy_(d, non_blocking=True)
+
+    ne = max(3, args.e2e_steps)
+    with torch.cuda.stream(stream):
+        e2e_step()
+    stream.synchronize()
+    e2e_graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(e2e_graph, stream=stream):
+        e2e_step()
+    with torch.cuda.stream(stream):
+        e2e_graph.replay()
+    stream.synchronize()
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        f0.record()
+        for _ in range(ne):
+            e2e_graph.replay()
+        f1.record()
+    stream.synchronize()
+    e2e_ms = f0.elapsed_time(f1)
+    elapsed_ms, e2e_ms, total_TL = reduce_over_ranks(torch, dist, elapsed_ms, e2e_ms, alg["T_L"], "cuda")
+    if rank == 0:
+        hbm, _, src = load_peaks()
+        step_ms = elapsed_ms / args.steps
+        ach = alg["step_bytes"] / (step_ms * 1e-3) / 1e9
+        line = {
+            "metric": METRIC, "value": total_TL * args.steps / (elapsed_ms * 1e-3), "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": "moe_decode", "desc": WORKLOADS["moe_decode"], "kind": args.kind,
+                       "path": "fused", "global_batch": T * world, "lora_tokens_per_gpu": alg["T_L"],
+                       "pairs": P, "live_pairs": alg["pairs_live"], "active_composite_slots": alg["active"],
+                       "parallelism": f"dp{world}",
+                       "l2": f"{alg['step_bytes'] / 2**20:.0f} MiB touched per step (> L2)",
+                       "timing": "CUDA-graph replays of one step (library launches only), CUDA events"},
+            "gpu_launches": per_step * args.steps,
+            "step_algorithmic_bytes": alg["step_bytes"],
+            "roofline": {"bound": "hbm", "kernel": "step (pair slots + metadata + w13 and w2 lora_apply)",
+                         "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm, "peak_source": src,
+                         "algorithmic_bytes_per_launch": alg["step_bytes"], "traffic": None},
+            "clocks": clocks.summary(),
+            "e2e": {"value": total_TL * ne / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / ne,
+                    "path": "pinned host token slots, top-k ids, x, h1, h2, h3 -> device; one step; h1, h3 -> host; "
+                            "each step one CUDA-graph replay"},
+        }
+        if world == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = run_cpu_baseline(args)
+        print(json.dumps(line))
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.cpu_child:
         if args.workload == "full_decode":
             full_decode_cpu(args)
+        elif args.workload == "moe_decode":
+            moe_cpu(args)
         else:
             cpu_child(args)
         return 0
@@ -824,6 +1026,8 @@ def main(argv=None):
         return run_reference(args)
     if args.workload == "full_decode":
         return run_full_decode(args)
+    if args.workload == "moe_decode":
+        return run_moe(args)
     return run_ours(args)
 
 
