@@ -22,7 +22,7 @@ and the token metadata of section "LoRAKernelMeta:先按槽位排序" (a stable 
 of token indices by slot, the slots present in ascending order, per-slot counts
 and start offsets with a leading 0).
 
-Readings where the pages leave a step open (each is listed in the design doc):
+Readings where the pages leave a step open:
 * slot 0 is the reserved no-LoRA slot (vLLM marks it -1; it sorts first either way);
 * the per-slot scale multiplies the shrink result (vLLM page, section
   "PEFTHelper:认清 adapter 文件": the scale is applied in the shrink step);

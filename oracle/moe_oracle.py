@@ -23,7 +23,7 @@ for w13 and pair p itself for w2. Expert-parallel ranks hold only their local
 experts (subsection "EP 下只装载本地专家的权重"): a pair whose expert is not
 local gets no delta on that rank.
 
-Readings (each listed in the design doc):
+Readings where the pages leave a step open:
 * adapter slot 0 is "no LoRA", as for the dense layers; adapters are slots
   1..num_loras;
 * pairs are numbered token-major, p = t * topk + k (the layout of
