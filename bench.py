@@ -815,13 +815,14 @@ def run_full_decode(args):
     return 0
 
 
-def moe_algorithmic(m):
+def moe_algorithmic(m, pair_slot):
     """Bytes of one MoE-layer step: every active composite slot's w13 and w2 weights once, the token
     rows x of tokens with a live pair once, h2 of live pairs once, h1 and h3 of live pairs read and
-    written once (bf16), and the routing ints."""
+    written once (bf16), and the routing ints. pair_slot: the pairs' composite slots (from the step)."""
     import numpy as np
-    live = m.pair_slot > 0
-    active = np.unique(m.pair_slot[live])
+    pair_slot = np.asarray(pair_slot)
+    live = pair_slot > 0
+    active = np.unique(pair_slot[live])
     r = m.w13.r_max
     w = int(len(active)) * 2 * r * (2 * m.hidden + 2 * m.inter + m.inter + m.hidden)
     tok = int(np.unique(np.nonzero(live)[0] // m.topk).size)
@@ -875,7 +876,6 @@ def run_moe(args):
     import rank_adapter_gb300 as ra
     kind = {"auto": ra.LORA_AUTO, "bgmv": ra.LORA_BGMV, "sgmv": ra.LORA_SGMV}[args.kind]
     m = wl.make_moe_instance(seed=8 + 1000 * rank)
-    alg = moe_algorithmic(m)
 
     def dev(a):
         return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
@@ -915,6 +915,7 @@ def run_moe(args):
         for _ in range(max(3, args.warmup)):
             step(None)
     stream.synchronize()
+    alg = moe_algorithmic(m, meta.token_slot[:P].cpu().numpy())   # the pairs' slots as the step computed them
     n0 = ra.lora_launch_count()
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=stream):

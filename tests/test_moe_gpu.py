@@ -86,31 +86,32 @@ def test_moe_layer_matches_oracle(lib, case, kind, path):
     k = getattr(lib, f"LORA_{kind}")
     pair = oracle.moe_pair_slots(inst.token_slot, inst.topk_ids, inst.num_loras, inst.num_experts,
                                  inst.local_experts, inst.expert_map)
-    assert np.array_equal(pair, inst.pair_slot)
     S = inst.w13.num_slots
     # w13: the pairs read their token's row of x
     y13 = _run_layer(lib, inst, inst.w13, inst.w13.x, inst.topk, k, path)
     ref13 = oracle.moe_lora_w13(inst.w13.to_f32(inst.w13.x).astype(np.float64),
                                 inst.w13.to_f32(inst.w13.y_in).astype(np.float64), pair, inst.topk,
                                 oracle.adapters_f64(inst.w13), inst.w13.out_sizes, S)
-    _check(inst.w13, y13, ref13)
+    _check(inst.routed(inst.w13, pair), y13, ref13)
     # w2: one input row per pair
     y2 = _run_layer(lib, inst, inst.w2, inst.w2.x, 1, k, path)
     ref2 = oracle.moe_lora_w2(inst.w2.to_f32(inst.w2.x).astype(np.float64),
                               inst.w2.to_f32(inst.w2.y_in).astype(np.float64), pair,
                               oracle.adapters_f64(inst.w2), inst.hidden, S)
-    _check(inst.w2, y2, ref2)
+    _check(inst.routed(inst.w2, pair), y2, ref2)
 
 
 def test_moe_sgmv_family_and_bad_ids(lib):
     """The w13 application on the tensor-core family alone, and pairs with bad ids
     (an adapter outside the table) counted by the metadata and left untouched."""
     inst = wl.make_moe_instance(seed=33, **MOE_CASES["all_local"])
+    pair = oracle.moe_pair_slots(inst.token_slot, inst.topk_ids, inst.num_loras, inst.num_experts,
+                                 inst.local_experts, inst.expert_map)
     y13 = _run_layer(lib, inst, inst.w13, inst.w13.x, inst.topk, lib.LORA_SGMV, "apply")
     ref13 = oracle.moe_lora_w13(inst.w13.to_f32(inst.w13.x).astype(np.float64),
-                                inst.w13.to_f32(inst.w13.y_in).astype(np.float64), inst.pair_slot, inst.topk,
+                                inst.w13.to_f32(inst.w13.y_in).astype(np.float64), pair, inst.topk,
                                 oracle.adapters_f64(inst.w13), inst.w13.out_sizes, inst.w13.num_slots)
-    _check(inst.w13, y13, ref13)
+    _check(inst.routed(inst.w13, pair), y13, ref13)
     ts = inst.token_slot.copy()
     ts[:5] = inst.num_loras + 1
     pair = lib.moe_pair_slots(_i32(ts), _i32(inst.topk_ids), inst.num_loras, inst.num_experts, inst.local_experts)

@@ -413,15 +413,16 @@ def toy_page_instance():
 
 @dataclass
 class MoEInstance:
-    """One mixture-of-experts layer's LoRA inputs.
+    """One mixture-of-experts layer's LoRA inputs (routing, tables, activations).
 
     ``w13`` and ``w2`` are the two applications as dense-layer instances over
     the (token, choice) pairs (p = t * topk + k): their slot tables hold the
     composite (adapter, local expert) slots 1 + (a - 1) * local_experts + j,
-    their requests are the pairs (one row each, slot = the pair's composite
-    slot), ``w2.x`` is the per-pair input h2 and ``w2.y_in`` / ``w13.y_in``
-    the pairs' base outputs. ``w13.x`` holds the token rows [T, hidden]: the
-    w13 LoRA row of pair p reads token row p // topk.
+    ``w2.x`` is the per-pair input h2 and ``w2.y_in`` / ``w13.y_in`` the
+    pairs' base outputs; ``w13.x`` holds the token rows [T, hidden] (the w13
+    LoRA row of pair p reads token row p // topk). The pairs' composite slots
+    are not computed here: ``routed(layer, pair_slot)`` gives a layer whose
+    requests are the pairs with the slots the caller computed.
     """
     name: str
     hidden: int
@@ -434,13 +435,20 @@ class MoEInstance:
     token_slot: np.ndarray          # int32 [T]: adapter slot of every token (0 = none)
     topk_ids: np.ndarray            # int32 [T, topk]: chosen global expert ids
     expert_map: Optional[np.ndarray]  # int32 [num_experts]: local index or -1 (None: all local)
-    pair_slot: np.ndarray           # int32 [T * topk]: composite slot of every pair
-    w13: Instance
+    w13: Instance                   # requests: the pairs, all with slot 0 until routed()
     w2: Instance
 
     @property
     def num_tokens(self) -> int:
         return int(self.token_slot.size)
+
+    @staticmethod
+    def routed(layer: Instance, pair_slot: np.ndarray) -> Instance:
+        """The layer with one request per pair carrying the given composite slot."""
+        return Instance(name=layer.name, dtype=layer.dtype, d_in=layer.d_in, out_sizes=layer.out_sizes,
+                        num_slots=layer.num_slots, r_max=layer.r_max, adapters=layer.adapters,
+                        req_lengths=layer.req_lengths, req_slots=np.asarray(pair_slot, np.int32).copy(),
+                        x=layer.x, y_in=layer.y_in, meta=dict(layer.meta))
 
 
 def make_moe_instance(name: str = "moe_decode", seed: Optional[int] = None, *, num_tokens: Optional[int] = None,
@@ -475,15 +483,8 @@ def make_moe_instance(name: str = "moe_decode", seed: Optional[int] = None, *, n
     if L < E:
         emap = np.full(E, -1, dtype=np.int32)
         emap[start:start + L] = np.arange(L, dtype=np.int32)
-    # composite slots, restated here from the layout rule (the oracle keeps its own copy)
-    pair = np.zeros(T * K, dtype=np.int32)
-    for t in range(T):
-        for k in range(K):
-            e = int(ids[t, k])
-            el = e - start if start <= e < start + L else -1
-            if ts[t] > 0 and el >= 0:
-                pair[t * K + k] = 1 + (int(ts[t]) - 1) * L + el
     S = 1 + NL * L
+    none = np.zeros(T * K, dtype=np.int32)
     pool = _Pool(rng, min(1 << 26, max(1 << 20, 4 * S * R * (2 * H + I + 2 * I + H))), dt)
     ranks = {k: R for k in range(1, S)}
     scales = {k: 1.0 for k in range(1, S)}
@@ -492,10 +493,10 @@ def make_moe_instance(name: str = "moe_decode", seed: Optional[int] = None, *, n
     ones = np.ones(T * K, np.int64)
     x = pool.take((T, H), 1.0)
     w13 = Instance(name=f"{name}/w13", dtype=dt, d_in=H, out_sizes=[I, I], num_slots=S, r_max=R, adapters=ad13,
-                   req_lengths=ones, req_slots=pair.copy(), x=x, y_in=pool.take((T * K, 2 * I), 1.0),
+                   req_lengths=ones, req_slots=none.copy(), x=x, y_in=pool.take((T * K, 2 * I), 1.0),
                    meta={"x_row_div": K})
     w2 = Instance(name=f"{name}/w2", dtype=dt, d_in=I, out_sizes=[H], num_slots=S, r_max=R, adapters=ad2,
-                  req_lengths=ones, req_slots=pair.copy(), x=pool.take((T * K, I), 1.0),
+                  req_lengths=ones, req_slots=none.copy(), x=pool.take((T * K, I), 1.0),
                   y_in=pool.take((T * K, H), 1.0))
     return MoEInstance(name=name, hidden=H, inter=I, num_experts=E, local_experts=L, ep_rank=ep_rank, topk=K,
-                       num_loras=NL, token_slot=ts, topk_ids=ids, expert_map=emap, pair_slot=pair, w13=w13, w2=w2)
+                       num_loras=NL, token_slot=ts, topk_ids=ids, expert_map=emap, w13=w13, w2=w2)
