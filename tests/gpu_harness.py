@@ -18,7 +18,6 @@ import torch
 
 import oracle
 import rank_adapter_gb300 as ra
-import workloads as wl
 
 TOL_BF16 = 1e-2
 TOL_F32 = 1e-5

@@ -10,7 +10,7 @@ import torch
 
 import oracle
 import workloads as wl
-from gpu_harness import (TOL_BF16, TOL_F32, check_parity, load_table, oracle_ref, parity, run_gpu, to_dev)
+from gpu_harness import load_table, oracle_ref, parity, run_gpu, to_dev
 
 pytestmark = pytest.mark.gpu
 
