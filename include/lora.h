@@ -194,7 +194,9 @@ int lora_prepare_meta(const lora_meta *meta, lora_stream_t stream);
  * enters here as in section "PEFTHelper:认清 adapter 文件").
  *   x:   device, [num_tokens, d_in] with row stride ldx elements, desc->dtype
  *        (a row-parallel shard's d_in columns of a wider x: x advanced by the
- *        shard's first column, ldx the full width)
+ *        shard's first column, ldx the full width); with desc->x_row_div > 1,
+ *        [ceil(num_tokens / x_row_div), d_in] and row i of the batch reads x
+ *        row i / x_row_div (lora_apply reads x the same way)
  *   buf: device fp32, [n_slices, num_tokens, r_max] contiguous; rows of
  *        slot-0 tokens are not written
  *   ws:  device scratch of at least lora_workspace_bytes(desc, num_tokens,
