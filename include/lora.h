@@ -339,7 +339,10 @@ int lora_embed_shrink(const lora_layer_desc *desc, const lora_meta *meta, const 
  * library holds that array until the process exits.
  * - The first call on a device looks up the array's device address (with
  *   that device current) and caches it; make that first call before any
- *   stream capture.
+ *   stream capture. The cached address belongs to that device's context:
+ *   after cudaDeviceReset (or anything else that destroys and recreates
+ *   the device's primary context) it is stale, so do not call this entry
+ *   point again in that process.
  * - All calls share the one array and it keeps the last call's contents.
  *   Nothing in it needs to start at zero. Calls whose kernels overlap on the
  *   GPU (on different streams, or from different threads without ordering)

@@ -119,3 +119,27 @@ def test_moe_sgmv_family_and_bad_ids(lib):
     meta.prepare(pair)
     torch.cuda.synchronize()
     assert lib.lora_query_status(meta.c) == (lib.LORA_EBADSLOT, 5 * inst.topk)
+
+
+@pytest.mark.parametrize("kind", ["BGMV", "SGMV", "AUTO"])
+def test_moe_layer_workload_shape(lib, kind):
+    """The MoE workload's own layer (hidden 7168, expert intermediate 2048, 256 experts with 8-way
+    expert parallelism, top-8, r = 64, 4 adapters), reduced only in token count: 160 tokens give
+    1280 pairs, above AUTO's token threshold. The w13 shrink runs 112 K blocks of 64 over d_in 7168,
+    the w2 expand 7168-wide outputs. SGMV takes every (adapter, expert) group on the tensor cores."""
+    inst = wl.make_moe_instance(seed=35, num_tokens=160)
+    assert (inst.hidden, inst.inter, inst.num_experts, inst.local_experts, inst.topk) == (7168, 2048, 256, 32, 8)
+    k = getattr(lib, f"LORA_{kind}")
+    pair = oracle.moe_pair_slots(inst.token_slot, inst.topk_ids, inst.num_loras, inst.num_experts,
+                                 inst.local_experts, inst.expert_map)
+    S = inst.w13.num_slots
+    y13 = _run_layer(lib, inst, inst.w13, inst.w13.x, inst.topk, k, "apply")
+    ref13 = oracle.moe_lora_w13(inst.w13.to_f32(inst.w13.x).astype(np.float64),
+                                inst.w13.to_f32(inst.w13.y_in).astype(np.float64), pair, inst.topk,
+                                oracle.adapters_f64(inst.w13), inst.w13.out_sizes, S)
+    _check(inst.routed(inst.w13, pair), y13, ref13)
+    y2 = _run_layer(lib, inst, inst.w2, inst.w2.x, 1, k, "apply")
+    ref2 = oracle.moe_lora_w2(inst.w2.to_f32(inst.w2.x).astype(np.float64),
+                              inst.w2.to_f32(inst.w2.y_in).astype(np.float64), pair,
+                              oracle.adapters_f64(inst.w2), inst.hidden, S)
+    _check(inst.routed(inst.w2, pair), y2, ref2)

@@ -5,7 +5,7 @@ over d_in, hi + lo bf16 expand). The cases cover tiles that end inside a
 segment and segments shorter than a tile, d_in and output widths that are not
 multiples of the K block or the column block, every supported r_max, one to
 four packed slices, padded leading dimensions, heterogeneous ranks with a
-scale, the full-size prefill batch (on sampled rows) and the full mixed batch
+scale, the full-size prefill batch (every row) and the full mixed batch
 under AUTO. Tolerances are those of the BGMV tests."""
 import numpy as np
 import pytest
@@ -150,12 +150,15 @@ def test_auto_small_batches_stay_on_bgmv(lib):
     _status_ok(lib, meta)
 
 
-def test_sgmv_prefill_full_size_sampled(lib):
-    """The full prefill batch (gate_up 4096 -> 2 x 14336, r = 64, ~17k tokens) through
-    lora_apply with AUTO and a bf16 y, checked on sampled rows against the oracle run
-    on those rows alone (a token's delta depends only on its own row and slot)."""
+def test_sgmv_prefill_full_size_every_row(lib):
+    """The full prefill batch (gate_up 4096 -> 2 x 14336, r = 64, ~14k tokens) through
+    lora_apply with AUTO and a bf16 y, every row and column checked against the oracle.
+    The oracle runs one request at a time on that request's rows (a token's delta
+    depends only on its own row and slot), so the host never holds more than one
+    request's fp64 rows; the bound is the stated one over the whole batch's delta."""
     inst = wl.make_instance("prefill_gate_up")
     T, W = inst.num_tokens, inst.d_out_total
+    assert W == 28672
     t = load_table(inst)
     x = to_dev(inst.x, "bf16")
     y = to_dev(inst.y_in, "bf16")
@@ -164,20 +167,23 @@ def test_sgmv_prefill_full_size_sampled(lib):
     lib.apply(t, meta, x, y, kind=lib.LORA_AUTO)
     torch.cuda.synchronize()
     _status_ok(lib, meta)
-    rng = np.random.default_rng(17)
-    rows = np.sort(rng.choice(T, size=128, replace=False))
-    rows[:2] = [0, T - 1]
-    y_gpu = y[torch.from_numpy(rows).cuda()].float().cpu().numpy().astype(np.float64)
-    ts = inst.token_slot[rows]
-    lengths, slots = oracle.requests_of_token_slots(ts)
+    y_gpu_all = y.float().cpu().numpy()
     ads = oracle.adapters_f64(inst)
-    x64 = inst.to_f32(inst.x[rows]).astype(np.float64)
-    y64 = inst.to_f32(inst.y_in[rows]).astype(np.float64)
-    buf, written = oracle.shrink_requests(x64, ads, inst.n_slices, inst.r_max, lengths, slots, inst.num_slots)
-    y_ref = oracle.expand_requests(buf, y64, ads, inst.out_sizes, lengths, slots, inst.num_slots)
-    assert written.all()
-    delta = y_ref - y64
-    rms = np.sqrt(np.mean(delta ** 2))
-    excess = np.abs(y_gpu - y_ref) - (TOL_BF16 * rms + bf16_half_ulp(y_ref))
-    assert excess.max() <= 0, f"max excess {excess.max():.3e} (RMS delta {rms:.3e})"
-    assert W == 28672
+    starts = np.concatenate([[0], np.cumsum(inst.req_lengths)])
+    sq_sum, n, worst = 0.0, 0, []
+    for i, slot in enumerate(inst.req_slots):
+        t0, t1 = int(starts[i]), int(starts[i + 1])
+        x64 = inst.to_f32(inst.x[t0:t1]).astype(np.float64)
+        y64 = inst.to_f32(inst.y_in[t0:t1]).astype(np.float64)
+        lengths, slots = np.asarray([t1 - t0], np.int64), np.asarray([slot], np.int64)
+        buf, written = oracle.shrink_requests(x64, ads, inst.n_slices, inst.r_max, lengths, slots, inst.num_slots)
+        y_ref = oracle.expand_requests(buf, y64, ads, inst.out_sizes, lengths, slots, inst.num_slots)
+        assert written.all()
+        delta = y_ref - y64
+        sq_sum += float(np.sum(delta ** 2))
+        n += delta.size
+        err = np.abs(y_gpu_all[t0:t1].astype(np.float64) - y_ref)
+        # per request: the largest error beyond half a bf16 ulp of the reference value
+        worst.append(float(np.max(err - bf16_half_ulp(y_ref))))
+    rms = np.sqrt(sq_sum / n)
+    assert max(worst) <= TOL_BF16 * rms, f"max excess {max(worst):.3e} > 1e-2 x RMS {rms:.3e}"

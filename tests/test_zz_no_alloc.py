@@ -50,6 +50,27 @@ def test_noalloc_shrink_matches_workspace_shrink_twice(lib):
         assert np.array_equal(np.isnan(got), np.isnan(ref)), "rows written differ"
         err = float(np.max(np.abs(got[:, written] - ref[:, written])))
         assert err <= TOL_BF16 * rms, f"max err {err:.3e} > {TOL_BF16} x RMS {rms:.3e}"
+        # same kernels, same arithmetic: the header promises the same results, bit for bit
+        assert np.array_equal(got, ref, equal_nan=True)
+
+
+def test_noalloc_shrink_allocates_nothing(lib):
+    """After a first call (which looks up the array's address), further calls leave the
+    device's free memory unchanged."""
+    inst = wl.make_instance("decode_qkv", seed=13, num_tokens=128, d_in=4096, out_sizes=[512, 128], num_slots=9)
+    table = load_table(inst)
+    meta = lib.TokenMeta(inst.num_tokens, inst.num_slots)
+    meta.prepare(torch.from_numpy(inst.token_slot).cuda())
+    x = to_dev(inst.x, "bf16")
+    buf = torch.zeros(2, inst.num_tokens, table.r_max, dtype=torch.float32, device="cuda")
+    lib.check(lib.lora_shrink_noalloc(table.desc, meta.c, x.data_ptr(), x.stride(0), buf.data_ptr()), "warm-up")
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    for _ in range(5):
+        lib.check(lib.lora_shrink_noalloc(table.desc, meta.c, x.data_ptr(), x.stride(0), buf.data_ptr()), "call")
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0
 
 
 def test_noalloc_shrink_after_a_different_layer(lib):
@@ -79,5 +100,7 @@ def test_noalloc_shrink_refuses_oversized_scratch(lib):
     assert lib.lora_workspace_bytes(table.desc, T) > lib.lora_noalloc_scratch_bytes()
     x = torch.zeros(T, 14336, dtype=torch.bfloat16, device="cuda")
     buf = torch.zeros(1, T, 128, device="cuda")
+    n0 = lib.lora_launch_count()
     st = lib.lora_shrink_noalloc(table.desc, meta.c, x.data_ptr(), x.stride(0), buf.data_ptr())
     assert st == lib.LORA_ERANGE
+    assert lib.lora_launch_count() == n0, "a refused call launched a kernel"

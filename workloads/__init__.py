@@ -171,12 +171,19 @@ class _Pool:
         self.vals = rng.standard_normal(size, dtype=np.float32)
         self.dtype = dtype
         self.rng = rng
+        self._bf16 = {}     # inv_scale -> the whole pool divided by it, encoded once
 
     def take(self, shape, inv_scale: float) -> np.ndarray:
         n = int(np.prod(shape))
         off = int(self.rng.integers(0, self.vals.size - n + 1))
-        v = self.vals[off:off + n].reshape(shape) / np.float32(inv_scale)
-        return bf16_bits_from_f32(v) if self.dtype == "bf16" else v.astype(np.float32)
+        if self.dtype == "bf16":
+            # Encoding the scaled pool once and copying windows of it gives the
+            # same bits as encoding each scaled window.
+            enc = self._bf16.get(inv_scale)
+            if enc is None:
+                enc = self._bf16[inv_scale] = bf16_bits_from_f32(self.vals / np.float32(inv_scale))
+            return enc[off:off + n].reshape(shape).copy()
+        return (self.vals[off:off + n].reshape(shape) / np.float32(inv_scale)).astype(np.float32)
 
 
 def _draw_adapters(rng, slots: Sequence[int], d_in: int, out_sizes: Sequence[int],
