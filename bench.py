@@ -10,13 +10,21 @@ is quoted on: qkv_proj d_in=4096, packed slices [4096,1024,1024], r=16,
 Timing: the step's inputs (slot table, x, y, token slots, metadata) are
 replicated on the device R times so that the rotation touches more than
 3x the 129 MB L2 between visits to a replica ("inputs larger than L2").
-Warm-up steps run eagerly; the K timed steps are CUDA-graph replays
-bracketed by CUDA events on the launching stream, with a barrier and
-torch.cuda.synchronize() on both sides; the value is the max over ranks.
+Warm-up steps run eagerly; a timed region is exactly K steps as CUDA-graph
+replays bracketed by CUDA events on the launching stream. Regions repeat
+back to back until at least --min-seconds of device time has been timed
+(so the clock sampler sees the load), with a barrier and
+torch.cuda.synchronize() on both sides of the whole set; the value is the
+median region (min and max reported beside it), max over ranks.
 Per-call durations come from graphs of G launches of one call alone (on
 inputs the steps prepared), timed around their replays. The end-to-end figure repeats the step through
 the same ABI with pinned host buffers: the copies in and out are inside its
 timed region.
+
+The default run (decode batch, one GPU) also measures the other workloads of
+the same family -- the toy fp32 batch, the prefill batch, the mixed batch and
+the 32-layer decode step -- and reports them under "configs" with their own
+roofline fractions and oracle baselines.
 
 Multi-GPU (torchrun): data parallel over independent batches, one replica of
 the slot table per rank, no collective on the data path ("scaling": "weak").
@@ -29,6 +37,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -75,6 +84,13 @@ def parse_args(argv=None):
     p.add_argument("--e2e-steps", type=int, default=200)
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--min-seconds", type=float, default=0.5,
+                   help="device time to accumulate over repeated K-step regions")
+    p.add_argument("--no-configs", action="store_true",
+                   help="skip the other workloads' sub-records of the default run")
+    p.add_argument("--sub-cpu-seconds", type=float, default=4.0,
+                   help="oracle time per sub-record's cpu_baseline")
+    p.add_argument("--cpu-threads", type=int, default=0, help=argparse.SUPPRESS)
     p.add_argument("--cpu-child", action="store_true", help=argparse.SUPPRESS)
     return p.parse_args(argv)
 
@@ -211,6 +227,8 @@ def cpu_child(args):
     """Time the oracle as it stands on this host's cores; prints one JSON line."""
     import numpy as np
     import oracle
+    if args.cpu_threads == 1:   # the single-thread figure: one core
+        os.sched_setaffinity(0, {sorted(os.sched_getaffinity(0))[0]})
     inst = make_workload(args.workload)
     alg = algorithmic(inst)
     ads = oracle.adapters_f64(inst)
@@ -231,39 +249,68 @@ def cpu_child(args):
         if el >= args.cpu_seconds:
             break
     print(json.dumps({"value": reps * alg["T_L"] / el, "seconds": el, "reps": reps,
-                      "sec_per_step": el / reps}))
+                      "sec_per_step": el / reps, "T_L": alg["T_L"], "active": alg["active"],
+                      "T": alg["T"]}))
 
 
-def run_cpu_baseline(args):
-    cores = len(os.sched_getaffinity(0))
+def run_cpu_baseline(workload, seconds, threads=None):
+    """The oracle on this host's cores (all of them, or one) in a child process; a cpu_baseline record."""
+    cores = len(os.sched_getaffinity(0)) if threads is None else threads
     env = dict(os.environ)
     for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
         env[v] = str(cores)
-    cmd = [sys.executable, os.path.abspath(__file__), "--cpu-child", "--workload", args.workload,
-           "--cpu-seconds", str(args.cpu_seconds)]
+    cmd = [sys.executable, os.path.abspath(__file__), "--cpu-child", "--workload", workload,
+           "--cpu-seconds", str(seconds), "--cpu-threads", str(threads or 0)]
     p = subprocess.run(cmd, capture_output=True, text=True, env=env, cwd=ROOT)
     if p.returncode != 0:
         return {"value": None, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                 "error": p.stderr.strip().splitlines()[-1:] }
     r = json.loads(p.stdout.strip().splitlines()[-1])
-    return {"value": r["value"], "unit": "tokens/s", "cores": cores, "kind": "oracle",
-            "sample": (f"{r['reps']} x one layer (4 groups) of the full-model step, scaled x32 " if
-                       args.workload == "full_decode" else f"{r['reps']} full steps of the {args.workload} batch ") +
-                      "(fp64 per-request loop, "
-                      f"numpy BLAS with {cores} threads), {r['seconds']:.1f} s",
-            "sec_per_step": r["sec_per_step"]}
+    what = {"full_decode": f"{r['reps']} x one layer (4 groups) of the full-model step, scaled x32 ",
+            "moe_decode": f"{r['reps']} full MoE-layer steps (pair slots, metadata, w13, w2) "}.get(
+        workload, f"{r['reps']} full steps of the {workload} batch ")
+    rec = {"value": r["value"], "unit": "tokens/s", "cores": cores, "kind": "oracle",
+           "sample": what + f"(fp64 per-request loop, numpy BLAS with {cores} thread{'s' if cores > 1 else ''}), "
+                            f"{r['seconds']:.1f} s",
+           "sec_per_step": r["sec_per_step"]}
+    for k in ("T_L", "active", "T", "pairs", "live_pairs", "active_composite_slots"):
+        if k in r:
+            rec[k] = r[k]
+    return rec
+
+
+def workload_config(name, kind, path, world, T, T_L, active=None, extra=None):
+    """The config dict both arms print for a workload (the same keys and values on both)."""
+    cfg = {"workload": name, "desc": WORKLOADS[name], "kind": kind, "path": path, "global_batch": T * world,
+           "lora_tokens_per_gpu": T_L, "parallelism": f"dp{world}"}
+    if active is not None:
+        cfg["active_adapters"] = active
+    cfg["l2"] = L2_NOTES.get(name, "inputs larger than L2: device replicas of the step's inputs, "
+                                   "rotated so that > 3x the 129 MiB L2 lies between visits to one")
+    if extra:
+        cfg.update(extra)
+    return cfg
+
+
+L2_NOTES = {
+    "full_decode": "inputs larger than L2: ~12 GB of distinct weights and activations touched per step",
+    "moe_decode": "inputs larger than L2: ~377 MB touched per step, tables of 457 MB",
+}
 
 
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
-    batch = {"full_decode": 512, "moe_decode": 256}.get(args.workload) or make_workload(args.workload).num_tokens
-    cfg = {"workload": args.workload, "desc": WORKLOADS[args.workload], "global_batch": batch,
-           "n_gpus_ignored": args.gpus}
-    cpu = run_cpu_baseline(argparse.Namespace(workload=args.workload,
-                                              cpu_seconds=max(1.0, args.cpu_seconds)))
+    cpu = run_cpu_baseline(args.workload, max(1.0, args.cpu_seconds))
     v = cpu.get("value")
+    T = cpu.get("T") or {"full_decode": 512, "moe_decode": 256}.get(args.workload, 0)
+    path = "fused" if args.workload in ("full_decode", "moe_decode") else args.path
+    if args.workload == "moe_decode":
+        cfg = workload_config(args.workload, args.kind, path, args.gpus, T, cpu.get("T_L"), None,
+                              {k: cpu.get(k) for k in ("pairs", "live_pairs", "active_composite_slots")})
+    else:
+        cfg = workload_config(args.workload, args.kind, path, args.gpus, T, cpu.get("T_L"), cpu.get("active"))
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": cfg,
@@ -372,32 +419,63 @@ class Replica:
 KERNELS = {"fused": ("meta", "apply"), "split": ("meta", "shrink", "expand")}
 
 
-def time_path(torch, ra, reps, stream, path, steps, G, clocks=None, dist=None):
-    """Time `steps` steps of one path as replays of a CUDA graph of G steps (rotating replicas).
+def time_regions(torch, stream, run_region, min_seconds, min_regions=3):
+    """Device time of repeated regions, each one call of run_region() (which enqueues exactly K
+    steps) between its own CUDA events on `stream`; regions run back to back until at least
+    min_seconds of device time is covered. Returns the regions' durations in ms."""
+    def batch(n):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        with torch.cuda.stream(stream):
+            for e0, e1 in evs:
+                e0.record()
+                run_region()
+                e1.record()
+        stream.synchronize()
+        return [e0.elapsed_time(e1) for e0, e1 in evs]
+    first = batch(1)
+    n = int(math.ceil(min_seconds * 1e3 / max(first[0], 1e-3)))
+    n = min(max(n, min_regions) - 1, 200000)
+    return first + batch(n) if n > 0 else first
 
-    The timed graph holds only the library's launches. Per-call durations come
-    afterwards from graphs of G launches of one call alone. Returns (elapsed_ms
-    over all steps, per-call mean ms, how, kernels launched per step).
+
+def region_stats(ms):
+    return {"median_ms": statistics.median(ms), "min_ms": min(ms), "max_ms": max(ms), "regions": len(ms),
+            "timed_s": sum(ms) * 1e-3}
+
+
+def time_path(torch, ra, reps, stream, path, steps, G, min_seconds, clocks=None, dist=None):
+    """Time regions of exactly `steps` steps of one path as replays of CUDA graphs of G steps (rotating
+    replicas), repeated until min_seconds of device time; see time_regions.
+
+    The timed graphs hold only the library's launches. Per-call durations come
+    afterwards from graphs of G launches of one call alone. Returns (region durations in ms, per-call
+    mean ms, how, kernels launched per step).
     """
     R = len(reps)
     names = KERNELS[path]
 
-    def capture(n, with_events):
+    def capture(n):
         gr = torch.cuda.CUDAGraph()
         with torch.cuda.graph(gr, stream=stream):
             for i in range(n):
                 reps[i % R].launch(ra, i, path=path)
-        return gr, None
+        return gr
 
     n0 = ra.lora_launch_count()
-    graph, _ = capture(G, False)
+    graph = capture(G)
     per_step = (ra.lora_launch_count() - n0) / G  # kernels the library launches per step
     tail = steps % G
-    graph_tail = capture(tail, False)[0] if tail else None
+    graph_tail = capture(tail) if tail else None
     with torch.cuda.stream(stream):
         for _ in range(2):
             graph.replay()
     stream.synchronize()
+
+    def region():
+        for _ in range(steps // G):
+            graph.replay()
+        if graph_tail is not None:
+            graph_tail.replay()
 
     if dist is not None:
         dist.barrier()
@@ -405,21 +483,12 @@ def time_path(torch, ra, reps, stream, path, steps, G, clocks=None, dist=None):
     if clocks is not None:
         clocks.start()
         time.sleep(0.3)
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        start.record()
-        for _ in range(steps // G):
-            graph.replay()
-        if graph_tail is not None:
-            graph_tail.replay()
-        end.record()
-    stream.synchronize()
+    ms = time_regions(torch, stream, region, min_seconds)
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
     if clocks is not None:
         clocks.stop()
-    elapsed_ms = start.elapsed_time(end)
 
     # Per call: a graph of G launches of that call alone (on metadata and
     # buffers the steps above prepared), timed around its replays. No event
@@ -433,17 +502,18 @@ def time_path(torch, ra, reps, stream, path, steps, G, clocks=None, dist=None):
         with torch.cuda.stream(stream):
             gr.replay()
         stream.synchronize()
+        reps_n = max(3, int(math.ceil(0.05e3 / max(1e-3, statistics.median(ms) * G / steps))))
         c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(stream):
             c0.record()
-            for _ in range(3):
+            for _ in range(reps_n):
                 gr.replay()
             c1.record()
         stream.synchronize()
-        durs[name] = [c0.elapsed_time(c1) / (3 * G)]
+        durs[name] = c0.elapsed_time(c1) / (reps_n * G)
     how = (f"each call alone: CUDA-graph replays of {G} launches of that call on prepared inputs, "
            f"CUDA events around the replays")
-    return elapsed_ms, {k: statistics.mean(v) for k, v in durs.items()}, how, per_step
+    return ms, durs, how, per_step
 
 
 def reduce_over_ranks(torch, dist, elapsed_ms, e2e_ms, lora_tokens, device):
@@ -459,8 +529,7 @@ def reduce_over_ranks(torch, dist, elapsed_ms, e2e_ms, lora_tokens, device):
     return float(mx[0]), float(mx[1]), float(tl[2])
 
 
-def run_ours(args):
-    import numpy as np
+def init_dist():
     import torch
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -470,11 +539,35 @@ def run_ours(args):
         import torch.distributed as dist
         dist.init_process_group("nccl")
     torch.cuda.set_device(local)
+    return world, rank, local, dist
+
+
+def clock_sampler(local):
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    return ClockSampler(vis.split(",")[local].strip() if vis else str(local))
+
+
+def replica_bytes(inst):
+    """Device bytes of one replica of a step's inputs (slot table, x, y)."""
+    es = 2 if inst.dtype == "bf16" else 4
+    table = es * inst.num_slots * inst.r_max * (inst.n_slices * inst.d_in + inst.d_out_total)
+    x = 4 * inst.num_tokens if inst.token_ids is not None else es * inst.num_tokens * inst.d_in
+    return table + x + es * inst.num_tokens * inst.d_out_total
+
+
+def measure_dense(name, args, world=1, rank=0, local=0, dist=None, with_e2e=True, min_seconds=None,
+                  with_other_path=True):
+    """Everything the bench reports for one single-projection workload (decode, prefill, mixed, toy,
+    lm_head, embedding): the timed step, per-call durations, roofline, e2e. Returns a dict of line
+    fields on every rank (rank 0 prints)."""
+    import numpy as np
+    import torch
     import rank_adapter_gb300 as ra
 
     kind = {"auto": ra.LORA_AUTO, "bgmv": ra.LORA_BGMV, "sgmv": ra.LORA_SGMV}[args.kind]
-    inst = make_workload(args.workload, seed_offset=rank)
+    inst = make_workload(name, seed_offset=rank)
     alg = algorithmic(inst)
+    min_seconds = args.min_seconds if min_seconds is None else min_seconds
 
     def dev(a, dt):
         a = np.ascontiguousarray(a)
@@ -492,9 +585,10 @@ def run_ours(args):
     y0 = dev(inst.y_in, inst.dtype)
     ts0 = torch.from_numpy(inst.token_slot).cuda()
 
-    per = master.nbytes() + x0.numel() * x0.element_size() + y0.numel() * y0.element_size()
+    per = replica_bytes(inst)
     R = args.replicas or max(2, int(np.ceil(3 * L2_BYTES / per)))
     reps = [Replica(ra, torch, inst, master, x0, y0, ts0, kind) for _ in range(R)]
+    del master
     torch.cuda.synchronize()
 
     stream = torch.cuda.Stream()
@@ -505,13 +599,24 @@ def run_ours(args):
 
     G = args.graph_steps or R * max(1, 64 // R)
     G = min(G, max(1, args.steps))
-    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
-    clocks = ClockSampler(vis.split(",")[local].strip() if vis else str(local))
-    elapsed_ms, avg, kernel_timing, per_step = time_path(torch, ra, reps, stream, args.path, args.steps, G, clocks,
-                                                         dist)
-    other = "split" if args.path == "fused" else "fused"
-    other_steps = min(args.steps, 20 * G)
-    o_ms, o_avg, _, _ = time_path(torch, ra, reps, stream, other, other_steps, G)
+    clocks = clock_sampler(local)
+    ms, avg, kernel_timing, per_step = time_path(torch, ra, reps, stream, args.path, args.steps, G, min_seconds,
+                                                 clocks, dist)
+    st = region_stats(ms)
+    out = {"alg": alg, "inst": inst, "regions": st, "kernel_ms": avg, "kernel_timing": kernel_timing,
+           "per_step_launches": per_step, "clocks": clocks.summary(), "G": G, "R": R, "per": per}
+    if with_other_path:
+        other = "split" if args.path == "fused" else "fused"
+        other_steps = min(args.steps, 20 * G)
+        o_ms, o_avg, _, _ = time_path(torch, ra, reps, stream, other, other_steps, G, min(0.1, min_seconds))
+        out["other"] = (other, statistics.median(o_ms) / other_steps, o_avg, other_steps)
+    med_ms, _, total_TL = reduce_over_ranks(torch, dist, st["median_ms"], 0.0, alg["T_L"], "cuda")
+    out["median_ms_all"] = med_ms
+    out["total_TL"] = total_TL
+    if not with_e2e:
+        del reps
+        torch.cuda.empty_cache()
+        return out
 
     # End to end: every step copies its inputs in from pinned host memory, runs through the ABI and
     # copies its result back to pinned host memory. A serving loop double-buffers: two replicas on two
@@ -579,50 +684,107 @@ def run_ours(args):
     ref_y = pair[last].y.cpu()
     if not torch.equal(h_out[last], ref_y):
         raise RuntimeError("end-to-end step: the host copy of y differs from the device result")
+    _, e2e_ms, _ = reduce_over_ranks(torch, dist, 0.0, e2e_ms, alg["T_L"], "cuda")
+    out["e2e"] = {"value": total_TL * ne / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                  "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / ne, "wall_s": e2e_wall,
+                  "path": f"per step: pinned host x, y_in, token_slot -> device; one step; y -> host; "
+                          f"{nbuf} replica(s) on {nbuf} stream(s) alternating, each step one CUDA-graph replay"}
+    del reps, pair, e2e_graphs
+    torch.cuda.empty_cache()
+    return out
 
-    elapsed_ms, e2e_ms, total_TL = reduce_over_ranks(torch, dist, elapsed_ms, e2e_ms, alg["T_L"], "cuda")
-    launches = int(round(per_step * args.steps))  # counted by the library while capturing the step graph
+
+def dense_roofline(name, m, path):
+    """Roofline record of the dominant call of a measured dense workload."""
+    hbm, tc, src = load_peaks()
+    alg, avg = m["alg"], m["kernel_ms"]
+    kbytes = {"apply": alg["step_bytes"], "shrink": alg["shrink_bytes"], "expand": alg["expand_bytes"]}
+    kflops = {"apply": alg["flops"], "shrink": alg["shrink_flops"], "expand": alg["expand_flops"]}
+    kern = max((k for k in avg if k != "meta"), key=lambda k: avg[k])
+    kb = kbytes[kern]
+    ach = kb / (avg[kern] * 1e-3) / 1e9
+    rl = {"bound": "hbm", "kernel": kern, "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm,
+          "peak_source": src, "algorithmic_bytes_per_launch": kb, "traffic": profiled_traffic(name, kern)}
+    # The tensor pipe's share where the dense contraction runs on it, next to the ceiling the
+    # arithmetic intensity allows when HBM is saturated.
+    tflops = kflops[kern] / (avg[kern] * 1e-3) / 1e12
+    rl["tensor"] = {"achieved_tflops": tflops, "peak_tflops": tc, "frac": tflops / tc,
+                    "ceiling_frac_at_hbm_peak": min(1.0, (kflops[kern] / kb) * hbm * 1e9 / (tc * 1e12))}
+    return rl
+
+
+def sub_record(name, m, args, cpu=None):
+    """The compact per-workload record of the default run's "configs"."""
+    hbm, _, _ = load_peaks()
+    alg, st = m["alg"], m["regions"]
+    step_s = st["median_ms"] / args.steps * 1e-3
+    rl = dense_roofline(name, m, args.path)
+    rec = {"desc": WORKLOADS[name], "dtype": m["inst"].dtype, "T": alg["T"], "lora_tokens": alg["T_L"],
+           "active_adapters": alg["active"], "tokens_per_s": alg["T_L"] / step_s,
+           "step_us": st["median_ms"] / args.steps * 1e3, "step_us_min": st["min_ms"] / args.steps * 1e3,
+           "step_us_max": st["max_ms"] / args.steps * 1e3, "regions": st["regions"],
+           "kernel_us": {k: v * 1e3 for k, v in m["kernel_ms"].items()},
+           "step_algorithmic_bytes": alg["step_bytes"],
+           "step_frac_of_hbm": alg["step_bytes"] / step_s / 1e9 / hbm,
+           "roofline": rl, "gpu_launches_per_step": m["per_step_launches"],
+           "l2": f"rotating {m['R']} device replicas x {m['per'] / 2**20:.1f} MiB (> 3x {L2_BYTES >> 20} MiB L2)",
+           "clocks": m["clocks"]}
+    if cpu is not None:
+        rec["cpu_baseline"] = cpu
+    return rec
+
+
+def run_ours(args):
+    world, rank, local, dist = init_dist()
+    m = measure_dense(args.workload, args, world, rank, local, dist)
+    launches = int(round(m["per_step_launches"] * args.steps))  # counted by the library while capturing the step graph
+    sub = {}
+    if args.workload == "decode_qkv" and world == 1 and not args.no_configs:
+        for name in ("toy_fp32", "prefill_gate_up", "mixed_o_proj"):
+            ms = measure_dense(name, args, with_e2e=False, with_other_path=False)
+            cpu = None if args.no_cpu_baseline else run_cpu_baseline(name, args.sub_cpu_seconds)
+            sub[name] = sub_record(name, ms, args, cpu)
+            del ms
+        fd = measure_full_decode(args, min_seconds=args.min_seconds, with_e2e=False)
+        sub["full_decode"] = fd["record"]
+        if not args.no_cpu_baseline:
+            sub["full_decode"]["cpu_baseline"] = run_cpu_baseline("full_decode", args.sub_cpu_seconds)
 
     if rank == 0:
         hbm, tc, src = load_peaks()
-        step_ms = elapsed_ms / args.steps
-        kbytes = {"apply": alg["step_bytes"], "shrink": alg["shrink_bytes"], "expand": alg["expand_bytes"]}
-        kern = max((k for k in avg if k != "meta"), key=lambda k: avg[k])
-        kb = kbytes[kern]
-        ach = kb / (avg[kern] * 1e-3) / 1e9
+        alg, st = m["alg"], m["regions"]
+        med_ms = m["median_ms_all"]
+        step_ms = med_ms / args.steps
+        other, o_ms, o_avg, other_steps = m["other"]
         line = {
-            "metric": METRIC, "value": total_TL * args.steps / (elapsed_ms * 1e-3), "unit": "tokens/s",
+            "metric": METRIC, "value": m["total_TL"] * args.steps / (med_ms * 1e-3), "unit": "tokens/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
+            "ms_per_step_min": st["min_ms"] / args.steps, "ms_per_step_max": st["max_ms"] / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": inst.dtype, "data": "synthetic",
-            "config": {"workload": args.workload, "desc": WORKLOADS[args.workload], "kind": args.kind,
-                       "path": args.path, "global_batch": inst.num_tokens * world,
-                       "lora_tokens_per_gpu": alg["T_L"], "active_adapters": alg["active"],
-                       "parallelism": f"dp{world}",
-                       "l2": f"rotating {R} device replicas x {per / 2**20:.1f} MiB "
-                             f"(> 3x {L2_BYTES >> 20} MiB L2)",
-                       "timing": f"CUDA-graph replays of {G} steps (library launches only), CUDA events "
-                                 f"on the launching stream"},
+            "dtype": m["inst"].dtype, "data": "synthetic",
+            "config": workload_config(args.workload, args.kind, args.path, world, m["inst"].num_tokens, alg["T_L"],
+                                      alg["active"]),
+            "timing": f"{st['regions']} regions of exactly {args.steps} steps each ({st['timed_s']:.2f} s of device "
+                      f"time), each region CUDA-graph replays of {m['G']} steps (library launches only) between "
+                      f"CUDA events on the launching stream; value and ms_per_step from the median region; inputs: "
+                      f"{m['R']} rotating device replicas x {m['per'] / 2**20:.1f} MiB (> 3x {L2_BYTES >> 20} MiB L2)",
             "gpu_launches": launches,
             "step_algorithmic_bytes": alg["step_bytes"],
             "step_hbm_gbs": alg["step_bytes"] / (step_ms * 1e-3) / 1e9,
             "step_frac_of_hbm": alg["step_bytes"] / (step_ms * 1e-3) / 1e9 / hbm,
-            "kernel_us": {k: v * 1e3 for k, v in avg.items()},
-            "kernel_timing": kernel_timing,
-            f"{other}_path": {"ms_per_step": o_ms / other_steps, "kernel_us": {k: v * 1e3 for k, v in o_avg.items()},
+            "kernel_us": {k: v * 1e3 for k, v in m["kernel_ms"].items()},
+            "kernel_timing": m["kernel_timing"],
+            f"{other}_path": {"ms_per_step": o_ms, "kernel_us": {k: v * 1e3 for k, v in o_avg.items()},
                               "steps": other_steps},
-            "roofline": {"bound": "hbm", "kernel": kern, "achieved": ach, "peak": hbm, "unit": "GB/s",
-                         "frac": ach / hbm, "peak_source": src,
-                         "algorithmic_bytes_per_launch": kb,
-                         "traffic": profiled_traffic(args.workload, kern)},
-            "clocks": clocks.summary(),
-            "e2e": {"value": total_TL * ne / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / ne, "wall_s": e2e_wall,
-                    "path": f"per step: pinned host x, y_in, token_slot -> device; one step; y -> host; "
-                            f"{nbuf} replica(s) on {nbuf} stream(s) alternating, each step one CUDA-graph replay"},
+            "roofline": dense_roofline(args.workload, m, args.path),
+            "clocks": m["clocks"],
+            "e2e": m["e2e"],
         }
         if world == 1 and not args.no_cpu_baseline:
-            line["cpu_baseline"] = run_cpu_baseline(args)
+            line["cpu_baseline"] = run_cpu_baseline(args.workload, args.cpu_seconds)
+            line["cpu_baseline_single_thread"] = run_cpu_baseline(args.workload, args.sub_cpu_seconds, threads=1)
+        if sub:
+            line["configs"] = sub
         print(json.dumps(line))
     if dist is not None:
         dist.destroy_process_group()
@@ -634,6 +796,8 @@ def full_decode_cpu(args):
     import numpy as np
     import oracle
     import workloads as wl
+    if args.cpu_threads == 1:
+        os.sched_setaffinity(0, {sorted(os.sched_getaffinity(0))[0]})
     groups = []
     for inst in wl.full_decode_groups():
         groups.append(inst)
@@ -652,31 +816,26 @@ def full_decode_cpu(args):
             break
     el = time.perf_counter() - t0
     sec_per_step = el / reps * 32          # 32 layers per step
-    T_L = int((groups[0].token_slot > 0).sum())
-    print(json.dumps({"value": T_L / sec_per_step, "seconds": el, "reps": reps, "sec_per_step": sec_per_step}))
+    ts = groups[0].token_slot
+    T_L = int((ts > 0).sum())
+    print(json.dumps({"value": T_L / sec_per_step, "seconds": el, "reps": reps, "sec_per_step": sec_per_step,
+                      "T_L": T_L, "T": int(len(ts)), "active": int(len(np.unique(ts[ts > 0])))}))
 
 
-def run_full_decode(args):
-    """Full-model decode step: one lora_prepare_meta, then lora_apply for each
-    of the 32 x 4 projection groups (own slot table, x and y each)."""
+def measure_full_decode(args, world=1, rank=0, local=0, dist=None, min_seconds=None, with_e2e=True):
+    """Full-model decode step: one lora_prepare_meta, then lora_apply for each of the 32 x 4 projection
+    groups (own slot table, x and y each). Returns {"record": the sub-record, ...line fields}."""
     import numpy as np
     import torch
     import workloads as wl
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl")
-    torch.cuda.set_device(local)
     import rank_adapter_gb300 as ra
     kind = {"auto": ra.LORA_AUTO, "bgmv": ra.LORA_BGMV, "sgmv": ra.LORA_SGMV}[args.kind]
+    min_seconds = args.min_seconds if min_seconds is None else min_seconds
 
     def dev(a):
         return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
 
-    tables, xs, ys, step_bytes, T_L, ts = [], [], [], 0, 0, None
+    tables, xs, ys, step_bytes, T_L, ts, active = [], [], [], 0, 0, None, 0
     for inst in wl.full_decode_groups(seed=5 + 1000 * rank):
         t = ra.SlotTable(inst.d_in, inst.out_sizes, inst.num_slots, inst.r_max, ra.LORA_BF16)
         for k, ad in sorted(inst.adapters.items()):
@@ -686,7 +845,7 @@ def run_full_decode(args):
         ys.append(dev(inst.y_in))
         alg = algorithmic(inst)
         step_bytes += alg["step_bytes"]
-        T_L, ts, S = alg["T_L"], inst.token_slot, inst.num_slots
+        T_L, ts, S, active = alg["T_L"], inst.token_slot, inst.num_slots, alg["active"]
     torch.cuda.synchronize()
     T = len(ts)
     meta = ra.TokenMeta(T, S)
@@ -715,25 +874,41 @@ def run_full_decode(args):
         for _ in range(2):
             graph.replay()
     stream.synchronize()
-    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
-    clocks = ClockSampler(vis.split(",")[local].strip() if vis else str(local))
+    clocks = clock_sampler(local)
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
     clocks.start()
     time.sleep(0.3)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        e0.record()
+
+    def region():
         for _ in range(args.steps):
             graph.replay()
-        e1.record()
-    stream.synchronize()
+
+    ms = time_regions(torch, stream, region, min_seconds)
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
     clocks.stop()
-    elapsed_ms = e0.elapsed_time(e1)
+    st = region_stats(ms)
+    hbm, tc, src = load_peaks()
+    step_ms = st["median_ms"] / args.steps
+    ach = step_bytes / (step_ms * 1e-3) / 1e9
+    roof = {"bound": "hbm", "kernel": "step (1 metadata + 128 lora_apply)", "achieved": ach,
+            "peak": hbm, "unit": "GB/s", "frac": ach / hbm, "peak_source": src,
+            "algorithmic_bytes_per_launch": step_bytes, "traffic": None}
+    out = {"regions": st, "clocks": clocks.summary(), "per_step": per_step, "T": T, "T_L": T_L, "active": active,
+           "step_bytes": step_bytes, "roofline": roof, "groups": len(tables)}
+    out["record"] = {"desc": WORKLOADS["full_decode"], "dtype": "bf16", "T": T, "lora_tokens": T_L,
+                     "active_adapters": active, "tokens_per_s": T_L / (step_ms * 1e-3), "step_us": step_ms * 1e3,
+                     "step_us_min": st["min_ms"] / args.steps * 1e3, "step_us_max": st["max_ms"] / args.steps * 1e3,
+                     "regions": st["regions"], "step_algorithmic_bytes": step_bytes, "step_frac_of_hbm": ach / hbm,
+                     "roofline": roof, "gpu_launches_per_step": per_step,
+                     "l2": L2_NOTES["full_decode"], "clocks": out["clocks"]}
+    if not with_e2e:
+        del graph, tables, xs, ys, ws
+        torch.cuda.empty_cache()
+        return out
 
     # End to end: token slots and every group's x and y_in in from pinned host memory, every y out.
     hx = [torch.empty_like(x, device="cpu").pin_memory().copy_(x) for x in xs]
@@ -770,45 +945,38 @@ def run_full_decode(args):
         f1.record()
     stream.synchronize()
     e2e_ms = f0.elapsed_time(f1)
-    elapsed_ms, e2e_ms, total_TL = reduce_over_ranks(torch, dist, elapsed_ms, e2e_ms, T_L, "cuda")
+    med_ms, e2e_ms, total_TL = reduce_over_ranks(torch, dist, st["median_ms"], e2e_ms, T_L, "cuda")
+    out.update(median_ms_all=med_ms, total_TL=total_TL)
+    out["e2e"] = {"value": total_TL * ne / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                  "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / ne,
+                  "path": "pinned host token slots and every group's x, y_in -> device; one step; every y -> host; "
+                          "each step one CUDA-graph replay"}
+    return out
+
+
+def run_full_decode(args):
+    world, rank, local, dist = init_dist()
+    m = measure_full_decode(args, world, rank, local, dist)
     if rank == 0:
-        hbm, tc, src = load_peaks()
-        step_ms = elapsed_ms / args.steps
-        ach = step_bytes / (step_ms * 1e-3) / 1e9
+        st = m["regions"]
+        step_ms = m["median_ms_all"] / args.steps
         line = {
-            "metric": METRIC, "value": total_TL * args.steps / (elapsed_ms * 1e-3), "unit": "tokens/s",
+            "metric": METRIC, "value": m["total_TL"] * args.steps / (m["median_ms_all"] * 1e-3), "unit": "tokens/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
+            "ms_per_step_min": st["min_ms"] / args.steps, "ms_per_step_max": st["max_ms"] / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
-            "config": {"workload": "full_decode", "desc": WORKLOADS["full_decode"], "kind": args.kind,
-                       "path": "fused", "global_batch": T * world, "lora_tokens_per_gpu": T_L,
-                       "parallelism": f"dp{world}", "groups": len(tables),
-                       "l2": f"{step_bytes / 2**30:.1f} GiB touched per step (>> L2)",
-                       "timing": "CUDA-graph replays of one step (library launches only), CUDA events"},
-            "gpu_launches": per_step * args.steps,
-            "step_algorithmic_bytes": step_bytes,
-            "roofline": {"bound": "hbm", "kernel": "step (1 metadata + 128 lora_apply)", "achieved": ach,
-                         "peak": hbm, "unit": "GB/s", "frac": ach / hbm, "peak_source": src,
-                         "algorithmic_bytes_per_launch": step_bytes, "traffic": None},
-            "clocks": clocks.summary(),
-            "e2e": {"value": total_TL * ne / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms / ne,
-                    "path": "pinned host token slots and every group's x, y_in -> device; one step; every y -> host; "
-                            "each step one CUDA-graph replay"},
+            "config": workload_config("full_decode", args.kind, "fused", world, m["T"], m["T_L"], m["active"]),
+            "timing": f"{st['regions']} regions of exactly {args.steps} steps ({st['timed_s']:.2f} s of device time), "
+                      f"each step one CUDA-graph replay (library launches only), CUDA events; median region",
+            "gpu_launches": m["per_step"] * args.steps,
+            "step_algorithmic_bytes": m["step_bytes"],
+            "roofline": m["roofline"],
+            "clocks": m["clocks"],
+            "e2e": m["e2e"],
         }
         if world == 1 and not args.no_cpu_baseline:
-            cores = len(os.sched_getaffinity(0))
-            env = dict(os.environ)
-            for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
-                env[v] = str(cores)
-            p = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-child", "--workload", "full_decode",
-                                "--cpu-seconds", str(args.cpu_seconds)], capture_output=True, text=True, env=env,
-                               cwd=ROOT)
-            if p.returncode == 0:
-                r = json.loads(p.stdout.strip().splitlines()[-1])
-                line["cpu_baseline"] = {"value": r["value"], "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                                        "sample": f"{r['reps']} x one layer (4 groups) of the step, scaled x32, "
-                                                  f"{r['seconds']:.1f} s", "sec_per_step": r["sec_per_step"]}
+            line["cpu_baseline"] = run_cpu_baseline("full_decode", args.cpu_seconds)
         print(json.dumps(line))
     if dist is not None:
         dist.destroy_process_group()
@@ -837,6 +1005,8 @@ def moe_cpu(args):
     import numpy as np
     import oracle
     import workloads as wl
+    if args.cpu_threads == 1:
+        os.sched_setaffinity(0, {sorted(os.sched_getaffinity(0))[0]})
     m = wl.make_moe_instance()
     a13, a2 = oracle.adapters_f64(m.w13), oracle.adapters_f64(m.w2)
     x = m.w13.to_f32(m.w13.x).astype(np.float64)
@@ -855,8 +1025,10 @@ def moe_cpu(args):
         el = time.perf_counter() - t0
         if el >= args.cpu_seconds:
             break
-    T_L = int((m.token_slot > 0).sum())
-    print(json.dumps({"value": reps * T_L / el, "seconds": el, "reps": reps, "sec_per_step": el / reps}))
+    alg = moe_algorithmic(m, pair)
+    print(json.dumps({"value": reps * alg["T_L"] / el, "seconds": el, "reps": reps, "sec_per_step": el / reps,
+                      "T_L": alg["T_L"], "T": m.num_tokens, "pairs": m.num_tokens * m.topk,
+                      "live_pairs": alg["pairs_live"], "active_composite_slots": alg["active"]}))
 
 
 def run_moe(args):
@@ -925,25 +1097,24 @@ def run_moe(args):
         for _ in range(2):
             graph.replay()
     stream.synchronize()
-    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
-    clocks = ClockSampler(vis.split(",")[local].strip() if vis else str(local))
+    clocks = clock_sampler(local)
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
     clocks.start()
     time.sleep(0.3)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        e0.record()
+
+    def region():
         for _ in range(args.steps):
             graph.replay()
-        e1.record()
-    stream.synchronize()
+
+    ms = time_regions(torch, stream, region, args.min_seconds)
+    st = region_stats(ms)
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
     clocks.stop()
-    elapsed_ms = e0.elapsed_time(e1)
+    elapsed_ms = st["median_ms"]
 
     # End to end: routing, x and the base outputs h1, h2, h3 in from pinned host memory, h1 and h3 out;
     # each step one CUDA-graph replay of its copies and calls.
@@ -986,14 +1157,14 @@ def run_moe(args):
         line = {
             "metric": METRIC, "value": total_TL * args.steps / (elapsed_ms * 1e-3), "unit": "tokens/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
+            "ms_per_step_min": st["min_ms"] / args.steps, "ms_per_step_max": st["max_ms"] / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
-            "config": {"workload": "moe_decode", "desc": WORKLOADS["moe_decode"], "kind": args.kind,
-                       "path": "fused", "global_batch": T * world, "lora_tokens_per_gpu": alg["T_L"],
-                       "pairs": P, "live_pairs": alg["pairs_live"], "active_composite_slots": alg["active"],
-                       "parallelism": f"dp{world}",
-                       "l2": f"{alg['step_bytes'] / 2**20:.0f} MiB touched per step (> L2)",
-                       "timing": "CUDA-graph replays of one step (library launches only), CUDA events"},
+            "config": workload_config("moe_decode", args.kind, "fused", world, T, alg["T_L"], None,
+                                      {"pairs": P, "live_pairs": alg["pairs_live"],
+                                       "active_composite_slots": alg["active"]}),
+            "timing": f"{st['regions']} regions of exactly {args.steps} steps ({st['timed_s']:.2f} s of device time), "
+                      f"each step one CUDA-graph replay (library launches only), CUDA events; median region",
             "gpu_launches": per_step * args.steps,
             "step_algorithmic_bytes": alg["step_bytes"],
             "roofline": {"bound": "hbm", "kernel": "step (pair slots + metadata + w13 and w2 lora_apply)",
@@ -1006,7 +1177,7 @@ def run_moe(args):
                             "each step one CUDA-graph replay"},
         }
         if world == 1 and not args.no_cpu_baseline:
-            line["cpu_baseline"] = run_cpu_baseline(args)
+            line["cpu_baseline"] = run_cpu_baseline("moe_decode", args.cpu_seconds)
         print(json.dumps(line))
     if dist is not None:
         dist.destroy_process_group()

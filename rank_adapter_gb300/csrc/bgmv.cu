@@ -179,8 +179,12 @@ __device__ __forceinline__ void store4(T *p, const float *f) {
 }
 
 // Sum N values per lane over the lanes that share bits [0, log2(NV)) of the
-// lane id (recursive halving). Afterwards the lane keeps N / (32 / NV) sums
-// in vals[0..), whose positions in the original array start at the returned offset.
+// lane id (recursive halving). Afterwards the lane keeps max(1, N / (32 / NV))
+// sums in vals[0..), whose positions in the original array start at the
+// returned offset. When the lanes outnumber the values (N < 32 / NV), the
+// levels left after the last halving add the single remaining value across
+// lanes (butterfly), so the lanes that end up with the same position hold
+// the same complete sum.
 template <int N, int NV>
 __device__ __forceinline__ int reduce_scatter(float (&vals)[N]) {
   const int lane = threadIdx.x & 31;
@@ -188,7 +192,10 @@ __device__ __forceinline__ int reduce_scatter(float (&vals)[N]) {
 #pragma unroll
   for (int lvl = 0, o = NV; o < 32; ++lvl, o <<= 1) {
     const int half = (N >> lvl) >> 1;
-    if (half == 0) break;
+    if (half == 0) {
+      vals[0] += __shfl_xor_sync(0xffffffffu, vals[0], o);
+      continue;
+    }
     const bool up = (lane & o) != 0;
 #pragma unroll
     for (int i = 0; i < N / 2; ++i) {

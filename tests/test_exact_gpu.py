@@ -100,8 +100,8 @@ def test_auto_split_exact(lib):
     """A batch of >= LORA_AUTO_SGMV_MIN_TOKENS tokens with long and short segments: AUTO runs the long
     ones on the tensor-core family and the short ones on BGMV in one call; both bitwise."""
     rng = np.random.default_rng(12)
-    lengths = [int(v) for v in rng.integers(1, 12, size=90)] + [200, 64, 63, 130]
-    slots = [int(v) for v in rng.integers(0, 8, size=90)] + [3, 5, 6, 7]
+    lengths = [int(v) for v in rng.integers(1, 12, size=110)] + [200, 64, 63, 130]
+    slots = [int(v) for v in rng.integers(0, 8, size=110)] + [3, 5, 6, 7]
     inst = _int_instance("bf16", 32, 96, (48, 32), lengths, slots, 8,
                          {k: [3, 32, 16, 7, 32, 1, 20][k - 1] for k in range(1, 8)},
                          {k: 2.0 ** (k % 3 - 1) for k in range(1, 8)}, seed=12)
