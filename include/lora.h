@@ -304,6 +304,22 @@ int lora_moe_pair_slots(const int32_t *token_slot, const int32_t *topk_ids, int3
 int lora_query_status(const lora_meta *meta, int32_t *out, lora_stream_t stream);
 
 /*
+ * Diagnostic of the device-side failure path. The tensor-core (SGMV)
+ * kernels wait on their own pipeline barriers with a time limit (200 ms):
+ * a wait that runs out records a bit in the metadata's device error word and
+ * the kernel winds down instead of hanging, and lora_query_status then
+ * returns LORA_EDEVICE. The multi-LoRA pages have no counterpart; this call
+ * lets a caller (or a test) see that path work without any fault: it launches
+ * one thread that runs the same bounded wait, with a limit of limit_us
+ * microseconds, on a barrier nothing will ever arm. After it, until the next
+ * lora_prepare_meta on `meta` (which clears the error word),
+ * lora_query_status(meta) returns LORA_EDEVICE; the stream and the context
+ * stay usable. The kernel issues no memory copy or MMA.
+ *   limit_us: 1 .. 1,000,000, else LORA_ERANGE; meta as for lora_prepare_meta.
+ */
+int lora_probe_bounded_wait(const lora_meta *meta, uint32_t limit_us, lora_stream_t stream);
+
+/*
  * Embedding lookup: the shrink of an embedding layer's LoRA (page "vLLM 源码完全
  * 拆解(十八): 多 LoRA 服务", section "embedding 的 LoRA 是一个查表增量"). With
  * desc->d_in the vocabulary size and one slice, A[0] = [num_slots, vocab, r_max]

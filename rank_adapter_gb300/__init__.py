@@ -29,7 +29,7 @@ __all__ = [
     "lora_set_slot", "lora_reset_slot", "lora_prepare_meta", "lora_shrink", "lora_expand", "lora_apply",
     "lora_shrink_noalloc", "lora_noalloc_scratch_bytes", "lora_embed_shrink", "embed_shrink",
     "lora_moe_pair_slots", "moe_pair_slots",
-    "lora_workspace_bytes", "lora_meta_tiles_bytes", "lora_query_status", "lora_strerror",
+    "lora_workspace_bytes", "lora_meta_tiles_bytes", "lora_query_status", "lora_probe_bounded_wait", "lora_strerror",
     "lora_last_cuda_error", "lora_launch_count", "SlotTable", "TokenMeta", "shrink", "expand", "apply", "workspace", "check",
 ]
 
@@ -97,6 +97,7 @@ _sig = {
     "lora_workspace_bytes": (ctypes.c_size_t, [_P(LayerDesc), _i32, _i32]),
     "lora_meta_tiles_bytes": (ctypes.c_size_t, [_i32]),
     "lora_query_status": (_i32, [_P(Meta), _P(_i32), _vp]),
+    "lora_probe_bounded_wait": (_i32, [_P(Meta), ctypes.c_uint32, _vp]),
     "lora_embed_shrink": (_i32, [_P(LayerDesc), _P(Meta), _vp, _vp, _vp]),
     "lora_moe_pair_slots": (_i32, [_vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _vp]),
     "lora_strerror": (ctypes.c_char_p, [_i32]),
@@ -207,6 +208,10 @@ def lora_query_status(meta: Meta, stream=None):
     out = _i32(0)
     st = _lib.lora_query_status(ctypes.byref(meta), ctypes.byref(out), _stream(stream))
     return st, int(out.value)
+
+
+def lora_probe_bounded_wait(meta: Meta, limit_us: int, stream=None) -> int:
+    return _lib.lora_probe_bounded_wait(ctypes.byref(meta), limit_us, _stream(stream))
 
 
 def lora_strerror(status: int) -> str:

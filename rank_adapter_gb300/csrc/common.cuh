@@ -261,6 +261,8 @@ cudaError_t launch_embed_shrink(const lora_layer_desc &d, const MetaView &mv, co
                                 const int32_t *token_id, float *buf, cudaStream_t st);
 // SGMV family (sgmv.cu, tcgen05). part: split partials, sgmv_workspace_bytes() bytes.
 bool sgmv_supported();
+// The pipelines' bounded wait, run against a barrier nothing arms (see lora_probe_bounded_wait).
+cudaError_t launch_wait_probe(const MetaView &mv, uint32_t limit_us, cudaStream_t st);
 size_t sgmv_workspace_bytes(const lora_layer_desc &d, int max_tokens);
 // behind: launched right behind this library's BGMV kernel(s) of the same
 // call over the other segments (the kernel then works before its wait).

@@ -327,6 +327,14 @@ int lora_query_status(const lora_meta *meta, int32_t *out, lora_stream_t stream)
   return v[0] == 0 ? LORA_OK : LORA_EBADSLOT;
 }
 
+int lora_probe_bounded_wait(const lora_meta *meta, uint32_t limit_us, lora_stream_t stream) {
+  clear_stale_error();
+  const int st = check_meta(meta);
+  if (st != LORA_OK) return st;
+  if (limit_us < 1 || limit_us > 1000000) return LORA_ERANGE;
+  return cuda_status(ra::launch_wait_probe(view_of(meta), limit_us, (cudaStream_t)stream));
+}
+
 int lora_embed_shrink(const lora_layer_desc *desc, const lora_meta *meta, const int32_t *token_id, float *buf,
                       lora_stream_t stream) {
   clear_stale_error();

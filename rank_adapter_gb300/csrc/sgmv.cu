@@ -51,6 +51,7 @@ constexpr uint64_t kWaitNs = 200000000ull;  // a pipeline wait longer than 200 m
 // Error bits in the work-list header (word WorkLists::kErrWord).
 constexpr int kErrShrink = 1;
 constexpr int kErrExpand = 2;
+constexpr int kErrProbe = 4;  // lora_probe_bounded_wait
 
 // Shared-memory descriptor layouts.
 constexpr uint32_t kSw128 = 2, kSw64 = 4, kSw32 = 6;
@@ -82,15 +83,16 @@ __device__ __forceinline__ uint64_t global_ns() {
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
-// Wait for the phase of the given parity. Gives up after kWaitNs: records
-// `code` in *err and returns false.
-__device__ __forceinline__ bool mbar_wait(uint64_t *b, uint32_t parity, int *err, int code) {
+// Wait for the phase of the given parity. Gives up after limit_ns (by
+// default kWaitNs): records `code` in *err and returns false.
+__device__ __forceinline__ bool mbar_wait(uint64_t *b, uint32_t parity, int *err, int code,
+                                          uint64_t limit_ns = kWaitNs) {
   if (mbar_try(b, parity)) return true;
   const uint64_t t0 = global_ns();
   for (;;) {
     for (int i = 0; i < 64; ++i)
       if (mbar_try(b, parity)) return true;
-    if (global_ns() - t0 > kWaitNs) {
+    if (global_ns() - t0 > limit_ns) {
       atomicOr(err, code);
       return false;
     }
@@ -1200,9 +1202,29 @@ int shrink_grid() { return sm_count(); }
 // range of at most ceil(U / G) units spans at most n_tiles / G + 2 tiles.
 int maxp_of(int T, int S, int G) { return (int)(tiles_bound(T, S) / G) + 2; }
 
+// The pipelines' bounded wait on a barrier that nothing will ever arm: one
+// thread initialises an mbarrier expecting one arrival and waits for its
+// first phase with a limit of limit_ns; no copy or MMA is issued, so when the
+// wait gives up (recording kErrProbe) nothing of this kernel is in flight.
+__global__ void __launch_bounds__(32) wait_probe_kernel(int *err, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  pdl_wait();
+  pdl_trigger();
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    (void)mbar_wait(&bar, 0, err, kErrProbe, limit_ns);
+  }
+}
+
 }  // namespace
 
 bool sgmv_supported() { return encode_fn() != nullptr; }
+
+cudaError_t launch_wait_probe(const MetaView &mv, uint32_t limit_us, cudaStream_t st) {
+  int *err = const_cast<int32_t *>(mv.work) + WorkLists::kErrWord;
+  return launch_pdl(wait_probe_kernel, dim3(1), dim3(32), 0, st, 1u, err, (uint64_t)limit_us * 1000ull);
+}
 
 size_t sgmv_workspace_bytes(const lora_layer_desc &d, int max_tokens) {
   if (max_tokens <= 0) return 0;
