@@ -186,6 +186,18 @@ __device__ __forceinline__ void store4(T *p, const float *f) {
   }
 }
 
+// acc += (lo(w), hi(w)) * x for a word w holding two bf16 values and a bf16
+// x: two mixed-precision FMAs (bf16 products, fp32 accumulation, one rounding
+// each: the same result as an fp32 FMA of the widened operands).
+__device__ __forceinline__ void fma2_bf16(uint32_t w, uint16_t x, float2 &acc) {
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "mov.b32 {lo, hi}, %2;\n\t"
+      "fma.rn.f32.bf16 %0, lo, %3, %0;\n\t"
+      "fma.rn.f32.bf16 %1, hi, %3, %1;\n\t}"
+      : "+f"(acc.x), "+f"(acc.y)
+      : "r"(w), "h"(x));
+}
+
 // Sum N values per lane over the lanes that share bits [0, log2(NV)) of the
 // lane id (recursive halving). Afterwards the lane keeps max(1, N / (32 / NV))
 // sums in vals[0..), whose positions in the original array start at the
@@ -308,17 +320,34 @@ struct TileMath {
         const int nr = min(g.sc, klen - s * g.sc);
         const TW *As = reinterpret_cast<const TW *>(smem + g.off_ring + s * (g.a_stage + g.x_stage)) + v * VEC;
         const TW *xs = reinterpret_cast<const TW *>(smem + g.off_ring + s * (g.a_stage + g.x_stage) + g.a_stage);
+        if constexpr (sizeof(TW) == 2) {
+          // bf16 operands straight into mixed-precision FMAs (one rounding, as
+          // an fp32 FMA of the widened values): no widening instructions.
+          const uint16_t *xr = reinterpret_cast<const uint16_t *>(xs);
 #pragma unroll 4
-        for (int j = rq; j < nr; j += NRG) {
-          float w[VEC];
-          widen16<TW>(*reinterpret_cast<const uint4 *>(As + j * g.r_max), w);
+          for (int j = rq; j < nr; j += NRG) {
+            const uint4 q = *reinterpret_cast<const uint4 *>(As + j * g.r_max);
+            const uint32_t wq[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-          for (int t = 0; t < NT; ++t) {
-            const float xt = Elem<TW>::to_f(xs[t * g.sc + j]);
-            const float2 xx = make_float2(xt, xt);
+            for (int t = 0; t < NT; ++t) {
+              const uint16_t xt = xr[t * g.sc + j];
 #pragma unroll
-            for (int p = 0; p < VEC / 2; ++p)
-              acc2[t * (VEC / 2) + p] = __ffma2_rn(xx, make_float2(w[2 * p], w[2 * p + 1]), acc2[t * (VEC / 2) + p]);
+              for (int p = 0; p < VEC / 2; ++p) fma2_bf16(wq[p], xt, acc2[t * (VEC / 2) + p]);
+            }
+          }
+        } else {
+#pragma unroll 4
+          for (int j = rq; j < nr; j += NRG) {
+            float w[VEC];
+            widen16<TW>(*reinterpret_cast<const uint4 *>(As + j * g.r_max), w);
+#pragma unroll
+            for (int t = 0; t < NT; ++t) {
+              const float xt = Elem<TW>::to_f(xs[t * g.sc + j]);
+              const float2 xx = make_float2(xt, xt);
+#pragma unroll
+              for (int p = 0; p < VEC / 2; ++p)
+                acc2[t * (VEC / 2) + p] = __ffma2_rn(xx, make_float2(w[2 * p], w[2 * p + 1]), acc2[t * (VEC / 2) + p]);
+            }
           }
         }
       }
