@@ -198,6 +198,21 @@ __device__ __forceinline__ void fma2_bf16(uint32_t w, uint16_t x, float2 &acc) {
       : "r"(w), "h"(x));
 }
 
+// Four consecutive y values as loaded (bf16 bits or fp32), widened later.
+template <typename T> struct YRaw;
+template <> struct YRaw<__nv_bfloat16> {
+  uint2 q;
+  __device__ static __forceinline__ YRaw load(const __nv_bfloat16 *p) { return {*reinterpret_cast<const uint2 *>(p)}; }
+  __device__ __forceinline__ void to_f(float *f) const {
+    f[0] = bf_lo(q.x); f[1] = bf_hi(q.x); f[2] = bf_lo(q.y); f[3] = bf_hi(q.y);
+  }
+};
+template <> struct YRaw<float> {
+  float4 q;
+  __device__ static __forceinline__ YRaw load(const float *p) { return {*reinterpret_cast<const float4 *>(p)}; }
+  __device__ __forceinline__ void to_f(float *f) const { f[0] = q.x; f[1] = q.y; f[2] = q.z; f[3] = q.w; }
+};
+
 // Sum N values per lane over the lanes that share bits [0, log2(NV)) of the
 // lane id (recursive halving). Afterwards the lane keeps max(1, N / (32 / NV))
 // sums in vals[0..), whose positions in the original array start at the
@@ -252,6 +267,11 @@ __device__ __forceinline__ void expand_pass_nt(const TW *Bs, int pw, const float
                                                const int *rows, int rbase, TY *y, int64_t ldy, int col_base,
                                                int pcn, int lt) {
   for (int cq = lt * 4; cq < pcn; cq += GS * 4) {
+    // The y values are requested before the products so that their latency
+    // overlaps the FMAs (kept as loaded: 8 or 16 bytes per token).
+    YRaw<TY> yr[NT];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) yr[t] = YRaw<TY>::load(y + (int64_t)rows[(rbase + t) % kRowsWin] * ldy + col_base + cq);
     float2 acc[NT][4];
 #pragma unroll
     for (int t = 0; t < NT; ++t)
@@ -272,12 +292,11 @@ __device__ __forceinline__ void expand_pass_nt(const TW *Bs, int pw, const float
     }
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
-      TY *yp = y + (int64_t)rows[(rbase + t) % kRowsWin] * ldy + col_base + cq;
       float yv[4];
-      load4(yp, yv);
+      yr[t].to_f(yv);
 #pragma unroll
       for (int c = 0; c < 4; ++c) yv[c] += acc[t][c].x + acc[t][c].y;
-      store4(yp, yv);
+      store4(y + (int64_t)rows[(rbase + t) % kRowsWin] * ldy + col_base + cq, yv);
     }
   }
 }
