@@ -75,20 +75,25 @@ typedef enum { LORA_F32 = 0, LORA_BF16 = 1 } lora_dtype;
  * BGMV: per-segment streaming of each adapter's A/B on CUDA cores (decode).
  * SGMV: tensor-core (tcgen05) tiles of 128 rows over same-adapter segments
  *       (prefill); bf16 tables with r_max >= 16 only (else LORA_EUNSUPPORTED).
- * AUTO: in a batch of at least LORA_AUTO_SGMV_MIN_TOKENS tokens, segments
- *       with at least LORA_SGMV_MIN_ROWS tokens go to SGMV and the others to
- *       BGMV; smaller batches, and tables SGMV does not take, run all on BGMV.
- *       The choice depends only on num_tokens, the table and the metadata,
- *       so lora_shrink and lora_expand of one batch agree on it. */
+ * AUTO: in a batch of at least LORA_AUTO_SGMV_MIN_TOKENS tokens that averages
+ *       at least LORA_AUTO_SGMV_MIN_AVG tokens per adapter slot (num_tokens >=
+ *       LORA_AUTO_SGMV_MIN_AVG * (num_slots - 1)), segments with at least
+ *       LORA_SGMV_MIN_ROWS tokens go to SGMV and the others to BGMV; other
+ *       batches, and tables SGMV does not take, run all on BGMV (a batch that
+ *       averages a few tokens per slot is decode-shaped, and its SGMV kernels
+ *       would most likely find no segment to take). The choice depends only on
+ *       num_tokens, the table and the metadata, so lora_shrink and lora_expand
+ *       of one batch agree on it. */
 typedef enum { LORA_AUTO = 0, LORA_BGMV = 1, LORA_SGMV = 2 } lora_kind;
 
 #define LORA_MAX_SLICES 4
 #define LORA_MAX_NUM_SLOTS 1024
 #define LORA_MAX_RANK 128
 #define LORA_MAX_TOKENS (1 << 24)
-#define LORA_SGMV_MIN_ROWS 64      /* AUTO threshold: segment rows routed to SGMV */
+#define LORA_SGMV_MIN_ROWS 32      /* AUTO threshold: segment rows routed to SGMV */
 #define LORA_SGMV_TILE_M 128       /* rows per SGMV tile (work-list granularity) */
 #define LORA_AUTO_SGMV_MIN_TOKENS 1024  /* AUTO: smaller batches run all on BGMV */
+#define LORA_AUTO_SGMV_MIN_AVG 20  /* AUTO: batches averaging fewer tokens per slot run all on BGMV */
 
 /*
  * One LoRA-wrapped layer: the stacked slot table of one (packed) projection.

@@ -90,9 +90,11 @@ bool sgmv_available(const lora_layer_desc *d) {
 }
 
 // AUTO sends its large segments to SGMV only in batches of at least
-// LORA_AUTO_SGMV_MIN_TOKENS tokens; smaller batches run entirely on BGMV.
+// LORA_AUTO_SGMV_MIN_TOKENS tokens that average at least
+// LORA_AUTO_SGMV_MIN_AVG tokens per adapter slot; other batches run entirely on BGMV.
 bool auto_uses_sgmv(const lora_layer_desc *d, int num_tokens) {
-  return num_tokens >= LORA_AUTO_SGMV_MIN_TOKENS && sgmv_available(d);
+  return num_tokens >= LORA_AUTO_SGMV_MIN_TOKENS &&
+         (int64_t)num_tokens >= (int64_t)LORA_AUTO_SGMV_MIN_AVG * (d->num_slots - 1) && sgmv_available(d);
 }
 
 // Which families a (kind, batch) runs and where their scratch lives in the

@@ -134,8 +134,9 @@ def test_auto_mixed_full_size(lib):
 
 
 def test_auto_small_batches_stay_on_bgmv(lib):
-    """Below LORA_AUTO_SGMV_MIN_TOKENS, AUTO is the BGMV family bitwise; above it, a batch
-    with no long segment is too (the SGMV kernels find no tiles)."""
+    """Below LORA_AUTO_SGMV_MIN_TOKENS, or below LORA_AUTO_SGMV_MIN_AVG tokens per slot, AUTO is
+    the BGMV family bitwise; a batch above both with no long segment is too (the SGMV kernels
+    find no tiles)."""
     inst = wl.make_instance("prefill_gate_up", num_tokens=900, d_in=512, out_sizes=[256, 128], num_slots=5)
     t = load_table(inst)
     _, ya, _ = run_gpu(inst, table=t, kind=lib.LORA_AUTO, path="apply")
@@ -148,6 +149,19 @@ def test_auto_small_batches_stay_on_bgmv(lib):
     bb, yb, _ = run_gpu(dec, table=t2, kind=lib.LORA_BGMV, path="split")
     assert np.array_equal(ya, yb) and np.array_equal(ba, bb, equal_nan=True)
     _status_ok(lib, meta)
+    # 22 tokens on each of 47 slots: at least 1024 tokens and 20 per slot, no segment of 32
+    S = 48
+    ts = np.tile(np.arange(1, S, dtype=np.int32), 22)
+    assert len(ts) >= lib.LORA_AUTO_SGMV_MIN_TOKENS and len(ts) >= lib.LORA_AUTO_SGMV_MIN_AVG * (S - 1)
+    assert np.bincount(ts)[1:].max() < lib.LORA_SGMV_MIN_ROWS
+    dec2 = wl.make_instance("decode_qkv", num_tokens=len(ts), d_in=512, out_sizes=[256], num_slots=S)
+    dec2 = _with_tokens(dec2, ts, np.random.default_rng(5))
+    t3 = load_table(dec2)
+    for path in ("split", "apply"):
+        ba, ya, meta = run_gpu(dec2, table=t3, kind=lib.LORA_AUTO, path=path, token_slot=ts)
+        bb, yb, _ = run_gpu(dec2, table=t3, kind=lib.LORA_BGMV, path=path, token_slot=ts)
+        assert np.array_equal(ya, yb) and np.array_equal(ba, bb, equal_nan=True)
+        _status_ok(lib, meta)
 
 
 def test_sgmv_prefill_full_size_every_row(lib):
