@@ -57,7 +57,7 @@ constexpr int kBPassBytes = 32768;   // B bytes per expand CTA (twice that for d
 constexpr int kWideGrid = 2048;
 constexpr int kSmallTable = 256;     // slot tables up to this size: rank / scale copied whole
 constexpr int kRowsWin = 32;         // token rows of a unit kept in shared memory (a sliding window)
-constexpr int kKCReg = 16;           // expand: chunk partials of the next tile held in registers
+constexpr int kKCReg = 4;            // expand: chunk partials of the next tile held in registers (d_in up to 4 chunks)
 constexpr int kExpandNG = 4;         // expand: most token tiles of a unit run side by side
 constexpr int kReach = kThreads * 4; // expand: columns one tile pass of the whole block covers
 
