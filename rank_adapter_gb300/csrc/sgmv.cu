@@ -846,7 +846,21 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
   const int n_list = a.work[a.L.hdr_segs];
   const int nbt = a.nb_start[n_slices];
   const int64_t n_items = (int64_t)n_tiles * nbt;
-  const int64_t it0 = n_items * blockIdx.x / gridDim.x, it1 = n_items * (blockIdx.x + 1) / gridDim.x;
+  int64_t it0, it1;
+  if ((int64_t)n_tiles * kMaxFanIn <= gridDim.x) {
+    // Few tiles: each tile gets its own CTAs (as many per tile as the grid
+    // allows, within one) and a CTA's items never cross into the next tile,
+    // so no CTA forms the u rows of two tiles one after the other.
+    const int t = (int)((int64_t)blockIdx.x * n_tiles / gridDim.x);  // tile t's CTAs: [ceil(t G / n), ceil((t + 1) G / n))
+    const int cb = (int)(((int64_t)t * gridDim.x + n_tiles - 1) / n_tiles);
+    const int ce = (int)(((int64_t)(t + 1) * gridDim.x + n_tiles - 1) / n_tiles);
+    const int k = (int)blockIdx.x - cb, nk = ce - cb;
+    it0 = (int64_t)t * nbt + (int64_t)nbt * k / nk;
+    it1 = (int64_t)t * nbt + (int64_t)nbt * (k + 1) / nk;
+  } else {
+    it0 = n_items * blockIdx.x / gridDim.x;
+    it1 = n_items * (blockIdx.x + 1) / gridDim.x;
+  }
   TY *y = static_cast<TY *>(a.y);
 
   if (warp < kEpiWarps) {
