@@ -561,6 +561,23 @@ __device__ __forceinline__ float u_from_partials(const BgmvArgs &a, int slice, i
   return u.scale * sum;
 }
 
+// The y lines of n token rows (rows r0.. of the unit's window), columns
+// [col_base, col_base + pcn), into this SM's L1: issued while the current
+// tile computes, so the next tile's read-modify-write finds them there
+// (one tile at a time; with tiles side by side it measured no better).
+// Called after the kernel's wait only (no earlier kernel still writes y).
+template <typename TY>
+__device__ __forceinline__ void prefetch_rows_l1(const TY *y, int64_t ldy, int col_base, int pcn, const int *rows,
+                                                 int r0, int n) {
+  const int row_bytes = pcn * (int)sizeof(TY);
+  const int lines = (row_bytes + 127) / 128;
+  for (int i = threadIdx.x; i < n * lines; i += kThreads) {
+    const int t = i / lines, l = i - t * lines;
+    const char *p = reinterpret_cast<const char *>(y + (int64_t)rows[(r0 + t) % kRowsWin] * ldy + col_base) + l * 128;
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
+  }
+}
+
 // The token passes of one expand unit of several tiles: a pass takes NG
 // tiles (kTT * NG tokens) at once, tile q of the pass on thread group q of
 // kThreads / NG threads; u of a pass is [kTT * NG][r_max] in shared memory,
@@ -735,6 +752,7 @@ __global__ void __launch_bounds__(kThreads, 3) bgmv_expand_kernel(BgmvArgs a) {
       for (int c = 0; c < kKCReg; ++c)
         if (c < g.kc_count) pref[c] = p[c * r_max];
     }
+    if (next_in_window) prefetch_rows_l1(y, a.ldy, col_base, pcn, rows, nxt * kTT, min(kTT, u.cnt - nxt * kTT));
     expand_pass<TW, TY, kThreads>(Bs, g.pw, cur, r_max, r_pad, rows, tile * kTT, nt, y, a.ldy, col_base,
                                     pcn, (int)threadIdx.x);
     if (nxt < ntiles) {
