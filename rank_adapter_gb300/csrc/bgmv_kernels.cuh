@@ -93,6 +93,7 @@ struct BgmvArgs {
   int list;      // int offset of the unit-record list inside the work lists
   int by_slot;   // shrink: grid rows are slots 1..S-1 (A prefetched before the wait)
   int small_only;  // by_slot on the short-segment list: skip slots whose segment is long
+  int wave;      // by_slot shrink grids deeper than one wave: CTAs resident at once (else 0)
   int pre;       // expand: runs right behind this library's shrink / reduce
   const int32_t *slot_rank;
   const float *slot_scale;
@@ -516,6 +517,21 @@ __global__ void __launch_bounds__(kSThreads, kSMinBlocks) bgmv_shrink_kernel(Bgm
     u.r_a = min(max(a.slot_rank[u.slot], 0), r_max);
     u.scale = a.slot_scale[u.slot];
     issue_a(u.slot, (u.r_a + VEC - 1) / VEC);
+    if (a.wave > 0 && tid == 0) {
+      // A grid deeper than one wave: the CTA one wave later in launch order
+      // starts only as a CTA of this wave leaves, so this one brings that
+      // CTA's A chunk (a full-rank slot's, one contiguous block) into L2 now.
+      const int b2 = (int)(blockIdx.y * gridDim.x + blockIdx.x) + a.wave;
+      if (b2 < (int)(gridDim.x * gridDim.y)) {
+        const int x2 = b2 % (int)gridDim.x, kc2 = b2 / (int)gridDim.x;
+        const int slot2 = 1 + x2 % rows_per;
+        if (a.slot_rank[slot2] >= r_max) {
+          const int k02 = kc2 * g.kchunk, klen2 = min(g.kchunk, g.d_in - k02);
+          const TW *src = static_cast<const TW *>(a.A[a.slice_order[x2 / rows_per]]) + ((int64_t)slot2 * g.d_in + k02) * r_max;
+          prefetch_l2(src, (uint32_t)(klen2 * r_max * (int)sizeof(TW)));
+        }
+      }
+    }
     pdl_wait();
     pdl_trigger();
     // The slot-indexed copy of the slot's record: one load, no index lookup.
