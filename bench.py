@@ -351,11 +351,13 @@ class Replica:
         return self.table.nbytes() + self.x.numel() * self.x.element_size() + \
             self.y.numel() * self.y.element_size()
 
-    def launch(self, ra, i, ev=None, path="fused", only=None):
+    def launch(self, ra, i, ev=None, path="fused", only=None, unshared=False):
         """Enqueue one step on the current stream: prepare_meta then lora_apply (path "fused")
         or lora_shrink + lora_expand (path "split"). ev: optional events around each call.
         only: enqueue just that call ("meta", "apply", "shrink" or "expand"; the metadata and
-        buffers it reads were prepared by earlier steps)."""
+        buffers it reads were prepared by earlier steps). unshared: the previous step on the
+        stream used another replica's metadata, so lora_prepare_meta_unshared may write this
+        step's metadata without waiting for that step's kernels."""
         st = None
         if only is not None:
             if only == "meta":
@@ -378,7 +380,10 @@ class Replica:
             return
         if ev is not None:
             ev[0].record()
-        ra.check(ra.lora_prepare_meta(self.meta.c, st), "prepare_meta")
+        if unshared:
+            ra.check(ra.lora_prepare_meta_unshared(self.meta.c, st), "prepare_meta_unshared")
+        else:
+            ra.check(ra.lora_prepare_meta(self.meta.c, st), "prepare_meta")
         if ev is not None:
             ev[1].record()
         if self.embed:  # both paths: the lookup, then the expand
@@ -455,10 +460,13 @@ def time_path(torch, ra, reps, stream, path, steps, G, min_seconds, clocks=None,
     names = KERNELS[path]
 
     def capture(n):
+        # Consecutive steps use different replicas (R >= 2), so every step but a graph's first
+        # prepares its metadata with lora_prepare_meta_unshared: the previous step's kernels read
+        # the other replica's metadata (a serving loop alternating two metadata buffers).
         gr = torch.cuda.CUDAGraph()
         with torch.cuda.graph(gr, stream=stream):
             for i in range(n):
-                reps[i % R].launch(ra, i, path=path)
+                reps[i % R].launch(ra, i, path=path, unshared=i > 0 and R > 1)
         return gr
 
     n0 = ra.lora_launch_count()
@@ -768,7 +776,9 @@ def run_ours(args):
             "timing": f"{st['regions']} regions of exactly {args.steps} steps each ({st['timed_s']:.2f} s of device "
                       f"time), each region CUDA-graph replays of {m['G']} steps (library launches only) between "
                       f"CUDA events on the launching stream; value and ms_per_step from the median region; inputs: "
-                      f"{m['R']} rotating device replicas x {m['per'] / 2**20:.1f} MiB (> 3x {L2_BYTES >> 20} MiB L2)",
+                      f"{m['R']} rotating device replicas x {m['per'] / 2**20:.1f} MiB (> 3x {L2_BYTES >> 20} MiB L2), "
+                      f"each with its own metadata buffers, so every step but a graph's first prepares its "
+                      f"metadata with lora_prepare_meta_unshared",
             "gpu_launches": launches,
             "step_algorithmic_bytes": alg["step_bytes"],
             "step_hbm_gbs": alg["step_bytes"] / (step_ms * 1e-3) / 1e9,

@@ -192,6 +192,22 @@ int lora_reset_slot(const lora_layer_desc *desc, int32_t slot, lora_stream_t str
 int lora_prepare_meta(const lora_meta *meta, lora_stream_t stream);
 
 /*
+ * lora_prepare_meta for a metadata buffer that no kernel of the previous call
+ * of this library on `stream` reads: the usual case is a serving loop that
+ * alternates two lora_meta between steps, so the previous step's applies
+ * read the other one. The outputs are the same, bit for bit, but they are
+ * written as soon as they are computed instead of after the previous kernel
+ * has finished, so the next shrink passes its wait as soon as the previous
+ * step ends. When this call's kernel starts, everything before the previous
+ * call's kernels is complete (this library's kernels release their successor
+ * only after their own wait; a kernel launched without programmatic
+ * dependent launch releases it when it ends), so only those kernels can
+ * still be running. If one of them does read `meta`, the results of both
+ * calls are undefined. Errors: as for lora_prepare_meta.
+ */
+int lora_prepare_meta_unshared(const lora_meta *meta, lora_stream_t stream);
+
+/*
  * Shrink: for every token t whose slot a != 0 and every slice s,
  *   buf[s, t, k] = slot_scale[a] * sum_j x[t, j] * A[s][a, j, k]   (k < rank a)
  *   buf[s, t, k] = 0                                               (rank a <= k < r_max)

@@ -26,7 +26,7 @@ __all__ = [
     "LORA_MAX_SLICES", "LORA_MAX_NUM_SLOTS", "LORA_MAX_RANK", "LORA_SGMV_MIN_ROWS", "LORA_SGMV_TILE_M",
     "LORA_AUTO_SGMV_MIN_TOKENS", "LORA_AUTO_SGMV_MIN_AVG",
     "LayerDesc", "Meta", "LoraError", "lib_path", "exported_symbols",
-    "lora_set_slot", "lora_reset_slot", "lora_prepare_meta", "lora_shrink", "lora_expand", "lora_apply",
+    "lora_set_slot", "lora_reset_slot", "lora_prepare_meta", "lora_prepare_meta_unshared", "lora_shrink", "lora_expand", "lora_apply",
     "lora_shrink_noalloc", "lora_noalloc_scratch_bytes", "lora_embed_shrink", "embed_shrink",
     "lora_moe_pair_slots", "moe_pair_slots",
     "lora_workspace_bytes", "lora_meta_tiles_bytes", "lora_query_status", "lora_probe_bounded_wait", "lora_strerror",
@@ -89,6 +89,7 @@ _sig = {
     "lora_set_slot": (_i32, [_P(LayerDesc), _i32, _i32, ctypes.c_float, _P(_vp), _P(_vp), _vp]),
     "lora_reset_slot": (_i32, [_P(LayerDesc), _i32, _vp]),
     "lora_prepare_meta": (_i32, [_P(Meta), _vp]),
+    "lora_prepare_meta_unshared": (_i32, [_P(Meta), _vp]),
     "lora_shrink": (_i32, [_P(LayerDesc), _P(Meta), _vp, ctypes.c_int64, _vp, _i32, _vp, ctypes.c_size_t, _vp]),
     "lora_expand": (_i32, [_P(LayerDesc), _P(Meta), _vp, _vp, ctypes.c_int64, _i32, _i32, _vp]),
     "lora_apply": (_i32, [_P(LayerDesc), _P(Meta), _vp, ctypes.c_int64, _vp, _vp, ctypes.c_int64, _i32, _i32, _vp,
@@ -156,6 +157,10 @@ def lora_reset_slot(desc: LayerDesc, slot: int, stream=None) -> int:
 
 def lora_prepare_meta(meta: Meta, stream=None) -> int:
     return _lib.lora_prepare_meta(ctypes.byref(meta), _stream(stream))
+
+
+def lora_prepare_meta_unshared(meta: Meta, stream=None) -> int:
+    return _lib.lora_prepare_meta_unshared(ctypes.byref(meta), _stream(stream))
 
 
 def lora_shrink(desc: LayerDesc, meta: Meta, x: int, ldx: int, buf: int, kind: int = LORA_AUTO,
@@ -310,14 +315,19 @@ class TokenMeta:
             raise ValueError(f"num_tokens {n} outside [0, {self.max_tokens}]")
         self.c.num_tokens = n
 
-    def prepare(self, token_slot=None, stream=None) -> None:
-        """Copy ``token_slot`` (int32 device tensor) in if given, then run lora_prepare_meta."""
+    def prepare(self, token_slot=None, stream=None, unshared=False) -> None:
+        """Copy ``token_slot`` (int32 device tensor) in if given, then run lora_prepare_meta
+        (lora_prepare_meta_unshared when ``unshared``: no kernel of the previous library call on
+        the stream reads this metadata)."""
         if token_slot is not None:
             n = int(token_slot.numel())
             self.set_num_tokens(n)
             if n:
                 self.token_slot[:n].copy_(token_slot, non_blocking=True)
-        check(lora_prepare_meta(self.c, stream), "lora_prepare_meta")
+        if unshared:
+            check(lora_prepare_meta_unshared(self.c, stream), "lora_prepare_meta_unshared")
+        else:
+            check(lora_prepare_meta(self.c, stream), "lora_prepare_meta")
 
     @property
     def num_segs(self):

@@ -236,7 +236,7 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 
 cudaError_t launch_slot_write(const lora_layer_desc &d, int slot, int rank, float scale,
                               const void *const *A_src, const void *const *B_src, cudaStream_t st);
-cudaError_t launch_prepare_meta(const lora_meta &m, cudaStream_t st);
+cudaError_t launch_prepare_meta(const lora_meta &m, cudaStream_t st, bool early = false);
 // BGMV family (bgmv.cu). ws: chunk partials, bgmv_workspace_bytes() bytes (may be null when 0).
 size_t bgmv_workspace_bytes(const lora_layer_desc &d, int max_tokens);
 cudaError_t launch_bgmv_shrink(const lora_layer_desc &d, const MetaView &mv, ListSel sel, const void *x,

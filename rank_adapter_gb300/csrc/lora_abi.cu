@@ -201,6 +201,13 @@ int lora_prepare_meta(const lora_meta *meta, lora_stream_t stream) {
   return cuda_status(ra::launch_prepare_meta(*meta, (cudaStream_t)stream));
 }
 
+int lora_prepare_meta_unshared(const lora_meta *meta, lora_stream_t stream) {
+  clear_stale_error();
+  int st = check_meta(meta);
+  if (st != LORA_OK) return st;
+  return cuda_status(ra::launch_prepare_meta(*meta, (cudaStream_t)stream, true));
+}
+
 int lora_shrink(const lora_layer_desc *desc, const lora_meta *meta, const void *x, int64_t ldx,
                 float *buf, int32_t kind, void *ws, size_t ws_bytes, lora_stream_t stream) {
   clear_stale_error();

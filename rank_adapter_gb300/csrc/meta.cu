@@ -26,6 +26,7 @@ struct MetaArgs {
   int32_t T, S;
   int32_t *sorted_rows, *seg_slot, *seg_count, *seg_start, *num_segs, *no_lora, *status;
   int32_t *work;
+  int early;  // the previous call's kernels do not read these outputs: write them without waiting
 };
 
 __device__ __forceinline__ uint32_t lanemask_lt() {
@@ -160,7 +161,10 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_meta_kernel(MetaArgs a) {
     rec_k[tid] = small ? WorkLists::list(S, kListSmall) + ex[3] * R
                : large ? WorkLists::list(S, kListLarge) + ex[4] * R : -1;
   }
-  pdl_wait();
+  // The outputs may still be read by the kernels of the previous call; with
+  // `early` the caller has promised they are not (another metadata buffer),
+  // and the wait moves to the kernel's exit.
+  if (!a.early) pdl_wait();
   if (tid < S) {
     W[WorkLists::slot_rec(S, kListAll) + tid] = lora ? ex[2] : -1;
     W[WorkLists::slot_rec(S, kListSmall) + tid] = small ? ex[3] : -1;
@@ -253,12 +257,14 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_meta_kernel(MetaArgs a) {
     if (valid && lane == __ffs(peers) - 1) hist[warp * hs + s] += __popc(peers);
     __syncwarp();
   }
+  if (a.early) pdl_wait();  // this kernel's completion still implies its predecessors'
 }
 
 }  // namespace
 
-cudaError_t launch_prepare_meta(const lora_meta &m, cudaStream_t st) {
+cudaError_t launch_prepare_meta(const lora_meta &m, cudaStream_t st, bool early) {
   MetaArgs a;
+  a.early = early ? 1 : 0;
   a.token_slot = m.token_slot;
   a.T = m.num_tokens;
   a.S = m.num_slots;
