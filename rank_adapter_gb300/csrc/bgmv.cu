@@ -1,6 +1,8 @@
 // Host side of the BGMV family: CTA geometry of a layer, work lists, and the
 // launch sequences of lora_shrink / lora_expand / lora_apply (kernels in
 // bgmv_kernels.cuh, instantiated by bgmv_shrink_k.cu and bgmv_expand_k.cu).
+#include <map>
+#include <mutex>
 #include <utility>
 
 #include "bgmv_kernels.cuh"
@@ -10,6 +12,22 @@ namespace bgmvk {
 namespace {
 
 int align16(int v) { return (v + 15) & ~15; }
+
+constexpr int kBySlotMaxWaves = 2;  // see fill_common
+
+// Multiprocessors of the current device (cached per device).
+int sm_count_cached() {
+  static std::mutex mu;
+  static std::map<int, int> cache;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = cache.find(dev);
+  if (it != cache.end()) return it->second;
+  int n = 1;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) n = 1;
+  return cache[dev] = n;
+}
 
 // Geometry of the shrink and expand CTAs for a layer.
 Geo make_geo(const lora_layer_desc &d, bool wide = false) {
@@ -93,6 +111,15 @@ void fill_common(BgmvArgs &a, const lora_layer_desc &d, const MetaView &mv, List
     a.chunk_start[d.n_slices] = chunks;
     if ((int64_t)chunks * a.max_items <= kWideGrid) break;  // a shallow expand grid keeps the narrow CTAs
   }
+  // A slot-indexed shrink grid of a whole batch several waves deep gains
+  // little from reading A before the metadata wait (only its first wave does)
+  // and reads the A of every slot without tokens; such grids are
+  // record-indexed instead (MoE step 124.9 -> 123.9 us). AUTO's short list
+  // keeps its slot-indexed grid: there the first wave's early A measured
+  // better (mixed batch 83.1 vs 84.8 us).
+  if (a.by_slot && !a.small_only &&
+      (int64_t)S1 * a.n_slices * a.g.kc_count > (int64_t)kBySlotMaxWaves * kSMinBlocks * sm_count_cached())
+    a.by_slot = 0;
 }
 
 }  // namespace
