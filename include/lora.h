@@ -77,7 +77,8 @@ typedef enum { LORA_F32 = 0, LORA_BF16 = 1 } lora_dtype;
  *       (prefill); bf16 tables with r_max >= 16 only (else LORA_EUNSUPPORTED).
  * AUTO: in a batch of at least LORA_AUTO_SGMV_MIN_TOKENS tokens that averages
  *       at least LORA_AUTO_SGMV_MIN_AVG tokens per adapter slot (num_tokens >=
- *       LORA_AUTO_SGMV_MIN_AVG * (num_slots - 1)), segments with at least
+ *       LORA_AUTO_SGMV_MIN_AVG * (num_slots - 1)) and has a segment of at
+ *       least LORA_AUTO_LONG_ROWS tokens, segments with at least
  *       LORA_SGMV_MIN_ROWS tokens go to SGMV and the others to BGMV; other
  *       batches, and tables SGMV does not take, run all on BGMV (a batch that
  *       averages a few tokens per slot is decode-shaped, and its SGMV kernels
@@ -94,6 +95,7 @@ typedef enum { LORA_AUTO = 0, LORA_BGMV = 1, LORA_SGMV = 2 } lora_kind;
 #define LORA_SGMV_TILE_M 128       /* rows per SGMV tile (work-list granularity) */
 #define LORA_AUTO_SGMV_MIN_TOKENS 1024  /* AUTO: smaller batches run all on BGMV */
 #define LORA_AUTO_SGMV_MIN_AVG 20  /* AUTO: batches averaging fewer tokens per slot run all on BGMV */
+#define LORA_AUTO_LONG_ROWS 64     /* AUTO: batches without a segment this long run all on BGMV */
 
 /*
  * One LoRA-wrapped layer: the stacked slot table of one (packed) projection.

@@ -24,7 +24,7 @@ __all__ = [
     "LORA_OK", "LORA_EINVAL", "LORA_ERANGE", "LORA_EALIGN", "LORA_EUNSUPPORTED", "LORA_ECUDA",
     "LORA_EBADSLOT", "LORA_EDEVICE", "LORA_EBADTOKEN", "LORA_F32", "LORA_BF16", "LORA_AUTO", "LORA_BGMV", "LORA_SGMV",
     "LORA_MAX_SLICES", "LORA_MAX_NUM_SLOTS", "LORA_MAX_RANK", "LORA_SGMV_MIN_ROWS", "LORA_SGMV_TILE_M",
-    "LORA_AUTO_SGMV_MIN_TOKENS", "LORA_AUTO_SGMV_MIN_AVG",
+    "LORA_AUTO_SGMV_MIN_TOKENS", "LORA_AUTO_SGMV_MIN_AVG", "LORA_AUTO_LONG_ROWS",
     "LayerDesc", "Meta", "LoraError", "lib_path", "exported_symbols",
     "lora_set_slot", "lora_reset_slot", "lora_prepare_meta", "lora_prepare_meta_unshared", "lora_shrink", "lora_expand", "lora_apply",
     "lora_shrink_noalloc", "lora_noalloc_scratch_bytes", "lora_embed_shrink", "embed_shrink",
@@ -45,6 +45,7 @@ LORA_SGMV_MIN_ROWS = 32
 LORA_SGMV_TILE_M = 128
 LORA_AUTO_SGMV_MIN_TOKENS = 1024
 LORA_AUTO_SGMV_MIN_AVG = 20
+LORA_AUTO_LONG_ROWS = 64
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 

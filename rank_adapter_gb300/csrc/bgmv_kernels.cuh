@@ -537,8 +537,9 @@ __global__ void __launch_bounds__(kSThreads, kSMinBlocks) bgmv_shrink_kernel(Bgm
     // The slot-indexed copy of the slot's record: one load, no index lookup.
     const int4 *rec = reinterpret_cast<const int4 *>(a.mv.work + WorkLists::by_slot(a.mv.num_slots) +
                                                      u.slot * WorkLists::kRec);
+    const int in_small = a.small_only ? a.mv.work[WorkLists::slot_rec(a.mv.num_slots, kListSmall) + u.slot] : 0;
     const int4 h = rec[0], r = rec[1];
-    if (h.y < 0 || (a.small_only && h.z >= LORA_SGMV_MIN_ROWS)) {  // no tokens here (or another family's)
+    if (h.y < 0 || in_small < 0) {  // no tokens here (or the segment is on the other family's list)
       cp_async_wait_upto(0);
       return;
     }

@@ -126,8 +126,9 @@ __device__ __forceinline__ void cp_async_wait_upto(int n) {
 //
 // int32 layout written by the metadata kernel and read by shrink / expand:
 //   [0] n_all    LoRA segments (slot != 0)
-//   [1] n_small  LoRA segments with < LORA_SGMV_MIN_ROWS tokens
-//   [2] n_large  LoRA segments with >= LORA_SGMV_MIN_ROWS tokens
+//   [1] n_small  LoRA segments not on the large list
+//   [2] n_large  LoRA segments with >= LORA_SGMV_MIN_ROWS tokens, when some LoRA
+//                segment has >= LORA_AUTO_LONG_ROWS tokens (else none)
 //   [3] tiles_all    sum over all LoRA segments of ceil(count / LORA_SGMV_TILE_M)
 //   [4] tiles_large  the same over the large segments
 //   [5..6] reserved (0)

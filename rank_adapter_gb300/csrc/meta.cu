@@ -87,6 +87,7 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_meta_kernel(MetaArgs a) {
   // (the slot-indexed copy of a slot's "all" record is at WorkLists::by_slot(S) + slot * kRec)
   __shared__ int tmp[7 * kWarps];
   __shared__ int s_bad;
+  __shared__ int s_long;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   // Everything up to the merged scan reads only token_slot (complete when
   // this call was enqueued) and writes only shared memory, so it runs before
@@ -131,11 +132,16 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_meta_kernel(MetaArgs a) {
   __syncthreads();
 
   // Per slot, across the kWarps warp rows: exclusive offsets (one warp scan per slot).
+  if (tid == 0) s_long = 0;
+  __syncthreads();
   for (int s = warp; s < S; s += kWarps) {
     const int c = lane < kWarps ? hist[lane * hs + s] : 0;
     const int incl = warp_incl_scan(c);
     if (lane < kWarps) hist[lane * hs + s] = incl - c;
-    if (lane == 31) tot_s[s] = incl;
+    if (lane == 31) {
+      tot_s[s] = incl;
+      if (s != 0 && incl >= LORA_AUTO_LONG_ROWS) s_long = 1;  // a long LoRA segment exists
+    }
   }
   __syncthreads();
 
@@ -143,8 +149,11 @@ __global__ void __launch_bounds__(kThreads, 1) prepare_meta_kernel(MetaArgs a) {
   const int tot = tid < S ? tot_s[tid] : 0;
   const bool present = tid < S && tot > 0;
   const bool lora = present && tid != 0;
-  const bool small = lora && tot < LORA_SGMV_MIN_ROWS;
-  const bool large = lora && tot >= LORA_SGMV_MIN_ROWS;
+  // AUTO's split: segments of LORA_SGMV_MIN_ROWS or more go to the large
+  // list only when the batch holds a segment of LORA_AUTO_LONG_ROWS or more
+  // (a prefill chunk); otherwise every segment is small (all on BGMV).
+  const bool large = lora && tot >= LORA_SGMV_MIN_ROWS && s_long != 0;
+  const bool small = lora && !large;
   const int tiles = lora ? (tot + LORA_SGMV_TILE_M - 1) / LORA_SGMV_TILE_M : 0;
   const int vals[7] = {tot, present, lora, small, large, tiles, large ? tiles : 0};
   int ex[7], tl[7];

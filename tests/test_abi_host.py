@@ -37,7 +37,8 @@ def test_every_declared_symbol_is_exported(ra):
 def test_header_constants_match_binding(ra):
     src = open(os.path.join(ROOT, "include", "lora.h")).read()
     for name in ("LORA_MAX_SLICES", "LORA_MAX_NUM_SLOTS", "LORA_MAX_RANK", "LORA_SGMV_MIN_ROWS",
-                 "LORA_SGMV_TILE_M", "LORA_AUTO_SGMV_MIN_TOKENS", "LORA_AUTO_SGMV_MIN_AVG"):
+                 "LORA_SGMV_TILE_M", "LORA_AUTO_SGMV_MIN_TOKENS", "LORA_AUTO_SGMV_MIN_AVG",
+                 "LORA_AUTO_LONG_ROWS"):
         m = re.search(rf"#define {name} (\d+)", src)
         assert m and int(m.group(1)) == getattr(ra, name), name
     for i, name in enumerate(["LORA_OK", "LORA_EINVAL", "LORA_ERANGE", "LORA_EALIGN", "LORA_EUNSUPPORTED",

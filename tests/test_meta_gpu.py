@@ -35,7 +35,8 @@ def _run(ra, ts, S):
 
 def _work_lists(ref, S):
     """The work lists by their definition: LoRA segments (slot != 0), split at
-    LORA_SGMV_MIN_ROWS, as 8-int records {segment, slot, count, start, first 4
+    LORA_SGMV_MIN_ROWS when some segment has LORA_AUTO_LONG_ROWS or more (else
+    all on the small list), as 8-int records {segment, slot, count, start, first 4
     rows (-1 past the count)}, unused records all -1, then the "all" records
     indexed by slot (all -1 for absent slots), then cumulative counts of
     128-row tiles over all LoRA segments and over the large ones, then per
@@ -44,8 +45,9 @@ def _work_lists(ref, S):
     n = ref["num_segs"]
     slot, cnt, start, rows = ref["seg_slot"], ref["seg_count"], ref["seg_start"], ref["sorted_rows"]
     segs = [i for i in range(n) if slot[i] != 0]
-    small = [i for i in segs if cnt[i] < ra.LORA_SGMV_MIN_ROWS]
-    large = [i for i in segs if cnt[i] >= ra.LORA_SGMV_MIN_ROWS]
+    has_long = any(cnt[i] >= ra.LORA_AUTO_LONG_ROWS for i in segs)
+    large = [i for i in segs if cnt[i] >= ra.LORA_SGMV_MIN_ROWS and has_long]
+    small = [i for i in segs if i not in large]
 
     def rec(i):
         return [i, slot[i], cnt[i], start[i]] + [int(rows[start[i] + j]) if j < cnt[i] else -1 for j in range(4)]

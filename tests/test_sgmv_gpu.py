@@ -164,6 +164,43 @@ def test_auto_small_batches_stay_on_bgmv(lib):
         _status_ok(lib, meta)
 
 
+def test_auto_splits_only_with_a_long_segment(lib):
+    """AUTO sends segments of LORA_SGMV_MIN_ROWS or more to SGMV only when the batch holds a
+    segment of LORA_AUTO_LONG_ROWS or more. A batch of 32..63-token segments (over both token
+    thresholds) is the BGMV family bitwise; the same batch with one slot grown past
+    LORA_AUTO_LONG_ROWS runs its 32+ segments on SGMV (their rows differ from BGMV's, within
+    tolerance of the oracle) and its short ones on BGMV (bitwise)."""
+    S = 33
+    rng = np.random.default_rng(9)
+    counts = rng.integers(10, lib.LORA_AUTO_LONG_ROWS, size=S - 1)
+    counts[:4] = [lib.LORA_SGMV_MIN_ROWS, 40, 63, 12]
+    ts = np.repeat(np.arange(1, S, dtype=np.int32), counts)
+    rng.shuffle(ts)
+    assert len(ts) >= lib.LORA_AUTO_SGMV_MIN_TOKENS and len(ts) >= lib.LORA_AUTO_SGMV_MIN_AVG * (S - 1)
+    inst = wl.make_instance("decode_qkv", num_tokens=len(ts), d_in=512, out_sizes=[256, 128], num_slots=S)
+    inst = _with_tokens(inst, ts, np.random.default_rng(10))
+    t = load_table(inst)
+    for path in ("split", "apply"):
+        ba, ya, meta = run_gpu(inst, table=t, kind=lib.LORA_AUTO, path=path, token_slot=ts)
+        bb, yb, _ = run_gpu(inst, table=t, kind=lib.LORA_BGMV, path=path, token_slot=ts)
+        assert np.array_equal(ya, yb) and np.array_equal(ba, bb, equal_nan=True)
+        _status_ok(lib, meta)
+    # one slot past LORA_AUTO_LONG_ROWS: the split is on
+    ts2 = np.concatenate([ts, np.full(lib.LORA_AUTO_LONG_ROWS, 5, np.int32)])
+    inst2 = wl.make_instance("decode_qkv", num_tokens=len(ts2), d_in=512, out_sizes=[256, 128], num_slots=S)
+    inst2 = _with_tokens(inst2, ts2, np.random.default_rng(11))
+    t2 = load_table(inst2)
+    _, ya, meta = parity(inst2, kind=lib.LORA_AUTO, table=t2, path="apply", token_slot=ts2)
+    _status_ok(lib, meta)
+    _, yb, _ = run_gpu(inst2, table=t2, kind=lib.LORA_BGMV, path="apply", token_slot=ts2)
+    c2 = np.bincount(ts2, minlength=S)
+    short = np.where((c2[ts2] < lib.LORA_SGMV_MIN_ROWS) & (ts2 > 0))[0]
+    long_ = np.where(c2[ts2] >= lib.LORA_SGMV_MIN_ROWS)[0]
+    assert len(short) and len(long_)
+    assert np.array_equal(ya[short], yb[short])
+    assert not np.array_equal(ya[long_], yb[long_])
+
+
 def test_sgmv_prefill_full_size_every_row(lib):
     """The full prefill batch (gate_up 4096 -> 2 x 14336, r = 64, ~14k tokens) through
     lora_apply with AUTO and a bf16 y, every row and column checked against the oracle.
