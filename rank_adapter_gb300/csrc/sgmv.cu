@@ -349,14 +349,16 @@ constexpr int kShrinkThreads = 288;    // + epilogue warps 4-7 + MMA warp 8
 // kernel of the same call (`behind`), it starts work at once: everything
 // older than that kernel is complete when it starts (the BGMV kernel releases
 // its successor only after its own wait), the two families touch disjoint
-// rows and workspace parts, and it waits just before it exits, so its
-// completion still implies the BGMV kernel's. Otherwise it waits first.
+// rows and workspace parts, and its first CTA waits just before it exits, so
+// its completion still implies the BGMV kernel's; the other CTAs leave as soon
+// as their work is done, handing their SM to the BGMV kernel. Otherwise it
+// waits first.
 __device__ __forceinline__ void sg_enter(int behind) {
   if (!behind) pdl_wait();
   pdl_trigger();
 }
 __device__ __forceinline__ void sg_exit(int behind) {
-  if (behind) pdl_wait();
+  if (behind && blockIdx.x == 0) pdl_wait();
 }
 
 __global__ void __launch_bounds__(kShrinkThreads, 1)
