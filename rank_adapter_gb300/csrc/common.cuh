@@ -185,8 +185,8 @@ struct MetaView {
 //   completion of everything before it on the stream;
 // * the metadata kernel triggers its successor at once (it only sorts in
 //   shared memory before its wait); an SGMV kernel launched right behind
-//   this library's BGMV kernel of the same call triggers at once too and
-//   waits just before it exits (the families touch disjoint rows and
+//   this library's BGMV kernel of the same call triggers at once too and its
+//   first CTA waits just before it exits (the families touch disjoint rows and
 //   workspace parts, and everything older than the BGMV kernel is complete
 //   when it starts); every other kernel triggers only after its own wait;
 // * apart from those SGMV kernels, a kernel reads before its wait only the
