@@ -50,11 +50,13 @@ constexpr int kTT = 4;               // tokens per tile
 constexpr int kAStageBytes = 16384;  // A bytes per stretch
 constexpr int kStretches = 2;        // stretches per shrink CTA (all in flight at once)
 constexpr int kBPassBytes = 32768;   // B bytes per expand CTA (twice that for deep grids, see kWideGrid)
-// An expand grid of more CTAs than this at kBPassBytes (about 4.5 waves of
+// An expand grid of more CTAs than this at kBPassBytes (about 2.2 waves of
 // three CTAs per SM on 152 SMs) takes CTAs of twice the columns: for a
-// vocabulary-wide output that measured 110 -> 92 us, while shallow decode
-// grids are faster with the narrower CTAs (fewer CTAs would leave SMs idle).
-constexpr int kWideGrid = 2048;
+// vocabulary-wide output that measured 110 -> 92 us, for the MoE step's
+// 2048-CTA grids 125 -> 120 us and for the mixed batch's 83 -> 80 us, while
+// shallow decode grids are faster with the narrower CTAs (fewer CTAs would
+// leave SMs idle; 512 here made the 32-layer step 1% slower).
+constexpr int kWideGrid = 1024;
 constexpr int kSmallTable = 256;     // slot tables up to this size: rank / scale copied whole
 constexpr int kRowsWin = 32;         // token rows of a unit kept in shared memory (a sliding window)
 constexpr int kKCReg = 4;            // expand: chunk partials of the next tile held in registers (d_in up to 4 chunks)
