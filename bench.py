@@ -76,7 +76,7 @@ def parse_args(argv=None):
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", choices=sorted(WORKLOADS), default="decode_qkv")
-    p.add_argument("--kind", choices=["auto", "bgmv", "sgmv"], default="auto")
+    p.add_argument("--kind", choices=["auto", "bgmv", "sgmv", "mixed"], default="auto")
     p.add_argument("--path", choices=["fused", "split"], default="fused",
                    help="fused: prepare_meta + lora_apply; split: prepare_meta + lora_shrink + lora_expand")
     p.add_argument("--replicas", type=int, default=0, help="device replicas (0: enough for 3x L2)")
@@ -572,7 +572,7 @@ def measure_dense(name, args, world=1, rank=0, local=0, dist=None, with_e2e=True
     import torch
     import rank_adapter_gb300 as ra
 
-    kind = {"auto": ra.LORA_AUTO, "bgmv": ra.LORA_BGMV, "sgmv": ra.LORA_SGMV}[args.kind]
+    kind = {"auto": ra.LORA_AUTO, "bgmv": ra.LORA_BGMV, "sgmv": ra.LORA_SGMV, "mixed": ra.LORA_MIXED}[args.kind]
     inst = make_workload(name, seed_offset=rank)
     alg = algorithmic(inst)
     min_seconds = args.min_seconds if min_seconds is None else min_seconds
@@ -840,7 +840,7 @@ def measure_full_decode(args, world=1, rank=0, local=0, dist=None, min_seconds=N
     import torch
     import workloads as wl
     import rank_adapter_gb300 as ra
-    kind = {"auto": ra.LORA_AUTO, "bgmv": ra.LORA_BGMV, "sgmv": ra.LORA_SGMV}[args.kind]
+    kind = {"auto": ra.LORA_AUTO, "bgmv": ra.LORA_BGMV, "sgmv": ra.LORA_SGMV, "mixed": ra.LORA_MIXED}[args.kind]
     min_seconds = args.min_seconds if min_seconds is None else min_seconds
 
     def dev(a):
@@ -1057,7 +1057,7 @@ def run_moe(args):
         dist.init_process_group("nccl")
     torch.cuda.set_device(local)
     import rank_adapter_gb300 as ra
-    kind = {"auto": ra.LORA_AUTO, "bgmv": ra.LORA_BGMV, "sgmv": ra.LORA_SGMV}[args.kind]
+    kind = {"auto": ra.LORA_AUTO, "bgmv": ra.LORA_BGMV, "sgmv": ra.LORA_SGMV, "mixed": ra.LORA_MIXED}[args.kind]
     m = wl.make_moe_instance(seed=8 + 1000 * rank)
 
     def dev(a):

@@ -84,8 +84,16 @@ typedef enum { LORA_F32 = 0, LORA_BF16 = 1 } lora_dtype;
  *       averages a few tokens per slot is decode-shaped, and its SGMV kernels
  *       would most likely find no segment to take). The choice depends only on
  *       num_tokens, the table and the metadata, so lora_shrink and lora_expand
- *       of one batch agree on it. */
-typedef enum { LORA_AUTO = 0, LORA_BGMV = 1, LORA_SGMV = 2 } lora_kind;
+ *       of one batch agree on it.
+ * MIXED: AUTO's split for a batch of any size: segments with at least
+ *       LORA_SGMV_MIN_ROWS tokens go to SGMV when the batch has a segment of
+ *       at least LORA_AUTO_LONG_ROWS tokens, the others to BGMV (all BGMV for
+ *       tables SGMV does not take). For a caller that knows its batch may hold
+ *       a prefill chunk below AUTO's token thresholds (one new prompt beside a
+ *       few hundred decode tokens runs several times faster this way); a
+ *       batch without a long segment pays for SGMV launches that find
+ *       nothing. */
+typedef enum { LORA_AUTO = 0, LORA_BGMV = 1, LORA_SGMV = 2, LORA_MIXED = 3 } lora_kind;
 
 #define LORA_MAX_SLICES 4
 #define LORA_MAX_NUM_SLOTS 1024

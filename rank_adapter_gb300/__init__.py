@@ -22,7 +22,7 @@ from typing import Optional, Sequence
 
 __all__ = [
     "LORA_OK", "LORA_EINVAL", "LORA_ERANGE", "LORA_EALIGN", "LORA_EUNSUPPORTED", "LORA_ECUDA",
-    "LORA_EBADSLOT", "LORA_EDEVICE", "LORA_EBADTOKEN", "LORA_F32", "LORA_BF16", "LORA_AUTO", "LORA_BGMV", "LORA_SGMV",
+    "LORA_EBADSLOT", "LORA_EDEVICE", "LORA_EBADTOKEN", "LORA_F32", "LORA_BF16", "LORA_AUTO", "LORA_BGMV", "LORA_SGMV", "LORA_MIXED",
     "LORA_MAX_SLICES", "LORA_MAX_NUM_SLOTS", "LORA_MAX_RANK", "LORA_SGMV_MIN_ROWS", "LORA_SGMV_TILE_M",
     "LORA_AUTO_SGMV_MIN_TOKENS", "LORA_AUTO_SGMV_MIN_AVG", "LORA_AUTO_LONG_ROWS",
     "LayerDesc", "Meta", "LoraError", "lib_path", "exported_symbols",
@@ -36,7 +36,7 @@ __all__ = [
 (LORA_OK, LORA_EINVAL, LORA_ERANGE, LORA_EALIGN, LORA_EUNSUPPORTED, LORA_ECUDA, LORA_EBADSLOT, LORA_EDEVICE,
  LORA_EBADTOKEN) = range(9)
 LORA_F32, LORA_BF16 = 0, 1
-LORA_AUTO, LORA_BGMV, LORA_SGMV = 0, 1, 2
+LORA_AUTO, LORA_BGMV, LORA_SGMV, LORA_MIXED = 0, 1, 2, 3
 LORA_MAX_SLICES = 4
 LORA_MAX_NUM_SLOTS = 1024
 LORA_MAX_RANK = 128

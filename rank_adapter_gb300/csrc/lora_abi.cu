@@ -106,7 +106,8 @@ struct Plan {
 
 Plan plan_of(const lora_layer_desc *d, int num_tokens, int kind) {
   Plan p{};
-  p.sgmv = kind == LORA_SGMV || (kind == LORA_AUTO && auto_uses_sgmv(d, num_tokens));
+  p.sgmv = kind == LORA_SGMV || (kind == LORA_AUTO && auto_uses_sgmv(d, num_tokens)) ||
+           (kind == LORA_MIXED && sgmv_available(d));
   p.bgmv = kind != LORA_SGMV;
   p.split = p.bgmv && p.sgmv;
   p.bgmv_bytes = p.bgmv ? ra::bgmv_workspace_bytes(*d, num_tokens) : 0;
@@ -165,7 +166,7 @@ size_t lora_meta_tiles_bytes(int32_t num_slots) {
 
 size_t lora_workspace_bytes(const lora_layer_desc *desc, int32_t max_tokens, int32_t kind) {
   if (check_desc(desc) != LORA_OK || max_tokens <= 0) return 0;
-  if (kind != LORA_AUTO && kind != LORA_BGMV && kind != LORA_SGMV) return 0;
+  if (kind != LORA_AUTO && kind != LORA_BGMV && kind != LORA_SGMV && kind != LORA_MIXED) return 0;
   if (kind == LORA_SGMV && !sgmv_available(desc)) return 0;
   return plan_of(desc, max_tokens, kind).total;
 }
@@ -216,7 +217,7 @@ int lora_shrink(const lora_layer_desc *desc, const lora_meta *meta, const void *
   st = check_meta(meta);
   if (st != LORA_OK) return st;
   if (meta->num_slots != desc->num_slots) return LORA_EINVAL;
-  if (kind != LORA_AUTO && kind != LORA_BGMV && kind != LORA_SGMV) return LORA_EINVAL;
+  if (kind != LORA_AUTO && kind != LORA_BGMV && kind != LORA_SGMV && kind != LORA_MIXED) return LORA_EINVAL;
   if (kind == LORA_SGMV && !sgmv_available(desc)) return LORA_EUNSUPPORTED;
   if (meta->num_tokens == 0) return LORA_OK;
   if (x == nullptr || buf == nullptr) return LORA_EINVAL;
@@ -248,7 +249,7 @@ int lora_expand(const lora_layer_desc *desc, const lora_meta *meta, const float 
   st = check_meta(meta);
   if (st != LORA_OK) return st;
   if (meta->num_slots != desc->num_slots) return LORA_EINVAL;
-  if (kind != LORA_AUTO && kind != LORA_BGMV && kind != LORA_SGMV) return LORA_EINVAL;
+  if (kind != LORA_AUTO && kind != LORA_BGMV && kind != LORA_SGMV && kind != LORA_MIXED) return LORA_EINVAL;
   if (y_dtype != LORA_F32 && y_dtype != LORA_BF16) return LORA_EINVAL;
   if (desc->dtype == LORA_F32 && y_dtype != LORA_F32) return LORA_EUNSUPPORTED;
   if (kind == LORA_SGMV && !sgmv_available(desc)) return LORA_EUNSUPPORTED;
@@ -279,7 +280,7 @@ int lora_apply(const lora_layer_desc *desc, const lora_meta *meta, const void *x
   st = check_meta(meta);
   if (st != LORA_OK) return st;
   if (meta->num_slots != desc->num_slots) return LORA_EINVAL;
-  if (kind != LORA_AUTO && kind != LORA_BGMV && kind != LORA_SGMV) return LORA_EINVAL;
+  if (kind != LORA_AUTO && kind != LORA_BGMV && kind != LORA_SGMV && kind != LORA_MIXED) return LORA_EINVAL;
   if (y_dtype != LORA_F32 && y_dtype != LORA_BF16) return LORA_EINVAL;
   if (desc->dtype == LORA_F32 && y_dtype != LORA_F32) return LORA_EUNSUPPORTED;
   if (kind == LORA_SGMV && !sgmv_available(desc)) return LORA_EUNSUPPORTED;

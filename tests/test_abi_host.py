@@ -44,6 +44,8 @@ def test_header_constants_match_binding(ra):
     for i, name in enumerate(["LORA_OK", "LORA_EINVAL", "LORA_ERANGE", "LORA_EALIGN", "LORA_EUNSUPPORTED",
                               "LORA_ECUDA", "LORA_EBADSLOT", "LORA_EDEVICE", "LORA_EBADTOKEN"]):
         assert re.search(rf"{name} = {i}\b", src) and getattr(ra, name) == i
+    for i, name in enumerate(["LORA_AUTO", "LORA_BGMV", "LORA_SGMV", "LORA_MIXED"]):
+        assert re.search(rf"{name} = {i}\b", src) and getattr(ra, name) == i
 
 
 def test_strerror_and_sizes(ra):

@@ -201,6 +201,36 @@ def test_auto_splits_only_with_a_long_segment(lib):
     assert not np.array_equal(ya[long_], yb[long_])
 
 
+def test_mixed_kind_small_batch_with_a_prompt(lib):
+    """LORA_MIXED below AUTO's token thresholds: a 300-token batch holding one 200-token prompt
+    beside one-token decode requests runs the prompt's segment on SGMV and the rest on BGMV,
+    within tolerance of the oracle on every row, the short rows bitwise equal to BGMV's; a
+    decode batch without a long segment is the BGMV family bitwise."""
+    S = 17
+    rng = np.random.default_rng(21)
+    ts = np.concatenate([rng.integers(0, S, size=100), np.full(200, 3)]).astype(np.int32)
+    assert len(ts) < lib.LORA_AUTO_SGMV_MIN_TOKENS
+    inst = wl.make_instance("decode_qkv", num_tokens=len(ts), d_in=1024, out_sizes=[512, 256], num_slots=S)
+    inst = _with_tokens(inst, ts, np.random.default_rng(22))
+    t = load_table(inst)
+    for path in ("apply", "split"):
+        _, ym, meta = parity(inst, kind=lib.LORA_MIXED, table=t, path=path, token_slot=ts)
+        _status_ok(lib, meta)
+        _, yb, _ = run_gpu(inst, table=t, kind=lib.LORA_BGMV, path=path, token_slot=ts)
+        c = np.bincount(ts, minlength=S)
+        short = np.where((c[ts] < lib.LORA_SGMV_MIN_ROWS) & (ts > 0))[0]
+        assert np.array_equal(ym[short], yb[short])
+        assert not np.array_equal(ym[ts == 3], yb[ts == 3])
+        assert np.array_equal(ym[ts == 0], yb[ts == 0])
+    dec = wl.make_instance("decode_qkv", num_tokens=256, d_in=512, out_sizes=[256], num_slots=33)
+    t2 = load_table(dec)
+    for path in ("apply", "split"):
+        ba, ya, meta = run_gpu(dec, table=t2, kind=lib.LORA_MIXED, path=path)
+        bb, yb, _ = run_gpu(dec, table=t2, kind=lib.LORA_BGMV, path=path)
+        assert np.array_equal(ya, yb) and np.array_equal(ba, bb, equal_nan=True)
+        _status_ok(lib, meta)
+
+
 def test_sgmv_prefill_full_size_every_row(lib):
     """The full prefill batch (gate_up 4096 -> 2 x 14336, r = 64, ~14k tokens) through
     lora_apply with AUTO and a bf16 y, every row and column checked against the oracle.
