@@ -175,6 +175,9 @@ def test_shrink_expand_validation(ra):
     assert ra.lora_workspace_bytes(d, 1000, ra.LORA_AUTO) == 2 * 1000 * 1 * 16 * 4   # < 1024 tokens: BGMV only
     assert ra.lora_workspace_bytes(d, 0, 0) == 0
     assert ra.lora_workspace_bytes(d, 16, 7) == 0                                      # bad kind
+    # MIXED is a valid kind; where SGMV does not apply (r_max < 16) it plans BGMV alone
+    assert ra.lora_workspace_bytes(r8, 1000, ra.LORA_MIXED) == ra.lora_workspace_bytes(r8, 1000, ra.LORA_BGMV) > 0
+    assert ra.lora_workspace_bytes(d, 1000, ra.LORA_MIXED) >= ra.lora_workspace_bytes(d, 1000, ra.LORA_BGMV)
     big = _desc(ra, d_in=4096, n_slices=3)
     nb = ra.lora_workspace_bytes(big, 256, 0)
     assert nb > 0 and nb % 16 == 0
