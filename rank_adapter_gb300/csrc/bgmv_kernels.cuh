@@ -14,9 +14,10 @@
 //
 // * shrink: one CTA per (segment, slice, chunk of d_in rows of 32 KB of A).
 //   All of its A rows and the matching x columns of the tile's 4 tokens are
-//   requested at once with 16-byte cp.async copies; a thread widens a
-//   16-byte weight vector once and feeds the 4 tokens with packed fp32x2
-//   FMAs; row groups combine by a recursive-halving shuffle reduce-scatter
+//   requested at once with 16-byte cp.async copies; a thread feeds a
+//   16-byte weight vector to the tile's tokens with mixed-precision FMAs
+//   (bf16 products, fp32 sums; packed fp32x2 FMAs for fp32 tables); row
+//   groups combine by a recursive-halving shuffle reduce-scatter
 //   and a fixed-order sum over warps. It writes unscaled partial rows to a
 //   caller-provided workspace (or, for lora_shrink with a single chunk, the
 //   scaled rank-r rows u = s * x A directly).
